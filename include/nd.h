@@ -1,0 +1,264 @@
+/*
+ * nd.h -- C ABI of libnd: sliding-window + KV-sink attention over a bounded
+ * int8 group-32 KV cache, and the compressed-attention variant, for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow these web pages (cited by title and section):
+ *  [N1] "256-token滑动窗口+KV sink：Needle 2工具钉住机制源码分析"
+ *  [N2] "How the 256-Token Sliding Window Works with Tools as KV Sinks in Needle"
+ *  [C3] "Compressed attention and the copy probe"
+ *
+ * Conventions for every entry point:
+ *  - Tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *    row-major, in the layout stated beside each argument.  bf16 tensors are
+ *    passed as void* holding IEEE bfloat16 values.  Pointers must be 16-byte
+ *    aligned.  The library keeps no pointer after a call returns.
+ *  - Work is enqueued on the caller's stream (NULL = the legacy default
+ *    stream) and runs asynchronously; the call returns once it is enqueued.
+ *  - No entry point allocates device or host memory.  Scratch comes from a
+ *    caller buffer sized by the matching *_workspace_size() query.
+ *  - Every entry point returns an nd_status.  Argument errors are detected on
+ *    the host before anything is enqueued and leave all buffers untouched.
+ *    ND_ERR_CUDA means a launch failed; nd_last_cuda_error() returns the CUDA
+ *    error code of the failing call on the calling thread.
+ *  - No exception crosses the ABI.  The library is thread-safe as long as
+ *    concurrent calls do not share output or workspace buffers.
+ */
+#ifndef ND_H_
+#define ND_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ND_API __attribute__((visibility("default")))
+#else
+#define ND_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA runtime header. */
+typedef struct CUstream_st *nd_stream_t;
+
+typedef enum {
+  ND_OK = 0,
+  ND_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or layout is invalid */
+  ND_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, dtype, device    */
+  ND_ERR_CUDA = 3,         /* a CUDA launch failed; see nd_last_cuda_error()  */
+  ND_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required      */
+  ND_ERR_DEVICE = 5        /* a kernel reported a device-side error flag      */
+} nd_status;
+
+typedef enum { ND_F32 = 0, ND_BF16 = 1 } nd_dtype;
+
+/* Library version string, e.g. "nd 0.1.0 sm_103a". */
+ND_API const char *nd_version(void);
+
+/* Human-readable name of a status code (never NULL). */
+ND_API const char *nd_status_string(int status);
+
+/* CUDA error code (cudaError_t as int) of the last failing CUDA call made by
+ * this library on the calling thread; 0 if none. */
+ND_API int nd_last_cuda_error(void);
+
+/*
+ * Device-side error word.  Kernels that wait on memory barriers give up after
+ * a bounded number of polls and OR a flag into this word instead of hanging;
+ * launches that read cache metadata flag out-of-range values the same way.
+ * Reads (and, when clear != 0, resets) the word of the current device.  Blocks
+ * until the device is idle.  Flags: 1 = a barrier wait timed out,
+ * 2 = cache metadata out of range (the affected sequence was skipped).
+ */
+ND_API int nd_device_errors(int *flags_out, int clear);
+
+/* ------------------------------------------------------------------------ */
+/* Bounded KV cache                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The bounded cache of [N1] "KV sink 如何「钉住」工具" and [N2] "KV Sinks for
+ * Tools": pinned sink positions that are never evicted plus a ring holding the
+ * most recent positions.  Storage is the int8 layout implied by the per-position
+ * byte count of kv_budget_window ([N2] "Effective KV Window"): per token, per KV
+ * head, head_dim int8 codes and one fp32 scale per 32 contiguous channels, for
+ * K and for V.
+ *
+ *   k_codes, v_codes  int8  [batch][n_kv_heads][sink_cap + ring_cap][head_dim]
+ *   k_scale, v_scale  fp32  [batch][n_kv_heads][sink_cap + ring_cap][head_dim/32]
+ *   slot s <  sink_cap : sink slot s (the pinned prefix, position s)
+ *   slot sink_cap + r  : ring slot r
+ *   sink_len   int32 [batch]  valid sink slots
+ *   ring_start int32 [batch]  ring slot of the oldest ring entry
+ *   ring_len   int32 [batch]  valid ring entries (<= ring_cap)
+ *   seq_len    int32 [batch]  tokens seen; the newest token has position
+ *                             seq_len - 1 and the ring's entries, oldest
+ *                             first, hold the ring_len positions ending there
+ * All pointers are device pointers; the metadata lives on the device so a
+ * decode loop can run without host synchronisation (and inside CUDA graphs).
+ * head_dim must be a multiple of 32; the kernels are built for 64 and 128.
+ */
+typedef struct {
+  int batch, n_kv_heads, head_dim, sink_cap, ring_cap;
+  int8_t *k_codes;
+  int8_t *v_codes;
+  float *k_scale;
+  float *v_scale;
+  int32_t *sink_len;
+  int32_t *ring_start;
+  int32_t *ring_len;
+  int32_t *seq_len;
+} nd_kv_cache;
+
+/*
+ * Quantise one new bf16 token per sequence and append it to the cache
+ * (fused quantise-and-append).
+ *   k_new, v_new  bf16 [batch][n_kv_heads][head_dim]
+ *   to_sink = 0   ring append: slot (ring_start + ring_len) mod ring_cap, or,
+ *                 when the ring is full, the oldest slot (ring_start advances)
+ *   to_sink = 1   sink append: slot sink_len; accepted only while ring_len == 0
+ *                 and sink_len < sink_cap (the sink is a prefix).  A rejected
+ *                 sink append writes nothing for that sequence and sets
+ *                 device error flag 2.
+ * Codec (one group = 32 contiguous channels of one token and head):
+ *   amax = max |x|, scale = amax / 127 (fp32 IEEE divide),
+ *   code = clamp(rint(x / scale), -127, 127) (fp32 IEEE divide, ties to even);
+ *   amax == 0 gives scale 0 and zero codes.
+ * seq_len advances by one for every accepted append.
+ */
+ND_API int nd_kv_append_quant(const nd_kv_cache *cache, const void *k_new,
+                       const void *v_new, int to_sink, nd_stream_t stream);
+
+/*
+ * Bulk form of the same codec: quantise n_rows bf16 rows of head_dim channels.
+ *   x       bf16 [n_rows][head_dim]
+ *   codes   int8 [n_rows][head_dim]
+ *   scales  fp32 [n_rows][head_dim/32]
+ * Used to fill cache slots in bulk (for example after a prefill).
+ */
+ND_API int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim,
+                     int8_t *codes, float *scales, nd_stream_t stream);
+
+/*
+ * One decode step ([N1] "256-token 滑动窗口：源码走读"): each sequence's query
+ * sits at position seq_len - 1 and attends to every sink slot and to the ring
+ * entries within `window` positions of it (recent = qpos - kpos < window; a
+ * sink is kept at any distance).  The caller appends the current token before
+ * calling, so the query sees its own key.  GQA: query head h reads KV head
+ * h / (n_q_heads / n_kv_heads).  Softmax scale 1/sqrt(head_dim).
+ *   q    bf16 [batch][n_q_heads][head_dim]  (already rotated, if the model
+ *             uses a rotary embedding)
+ *   out  bf16 [batch][n_q_heads][head_dim]
+ *   lse  fp32 [batch][n_q_heads] natural-log softmax denominator, or NULL
+ *   window >= 1.  n_q_heads / n_kv_heads must be 1..8.
+ * A sequence with no visible key (empty cache) gets out = 0, lse = -inf.
+ * Split-K partials go to the workspace, sized by
+ * nd_swa_sink_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+ * sink_cap + min(ring_cap, window)); the size may be 0 (no split).
+ */
+ND_API size_t nd_swa_sink_decode_workspace_size(int batch, int n_q_heads,
+                                                int n_kv_heads, int head_dim,
+                                                int max_slots);
+ND_API int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads,
+                       int window, void *out, float *lse, void *workspace,
+                       size_t workspace_bytes, nd_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Prefill                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Prefill attention under make_causal_packing_mask ([N2] "KV Sinks for
+ * Tools"): query t of row b attends key k iff
+ *   seg_ids[b][t] == seg_ids[b][k] > 0 and k <= t and
+ *   (window == 0 or t - k < window or sink[b][k] != 0)
+ * (window == 0 switches the window term off; sink == NULL means no sinks).
+ * GQA: query head h reads KV head h / (n_q_heads / n_kv_heads).  Softmax scale
+ * 1/sqrt(head_dim).  Fully masked rows (padding, seg 0) get out = 0 and
+ * lse = -inf.
+ *
+ *   q    [batch][T][n_q_heads][head_dim]    dtype
+ *   k, v [batch][T][n_kv_heads][head_dim]   dtype
+ *   seg_ids int32 [batch][T], or NULL (one segment, id 1)
+ *   sink    uint8 [batch][T], or NULL
+ *   out  [batch][T][n_q_heads][head_dim]    dtype
+ *   lse  fp32 [batch][n_q_heads][T], or NULL
+ *   rope_theta != 0 rotates q and k at their packed position t before the
+ *     product (rotate-half pairs (i, i + head_dim/2), angle t*theta^(-2i/d)).
+ *
+ * Compressed variant ([C3] "Two kinds of columns" and "Pool before rotating,
+ * not after"): when block > 0, pooled_k / pooled_v hold the T/block pooled
+ * blocks from nd_kv_compress_pool ([batch][T/block][n_kv_heads][head_dim],
+ * pooled K already rotated at its block midpoint) and every query attends
+ * one softmax over the columns [pooled blocks j visible iff
+ * (j+1)*block <= t - window + 1, exact keys k <= t with t - k < window].  The
+ * compressed variant requires seg_ids == NULL, sink == NULL and window >= 1.
+ *
+ * dtype ND_F32 runs on CUDA cores in fp32; ND_BF16 runs on the tensor cores
+ * (bf16 operands, fp32 accumulation).  head_dim 64 or 128.
+ */
+ND_API size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T,
+                                          int n_q_heads, int n_kv_heads,
+                                          int head_dim, float rope_theta,
+                                          int block);
+ND_API int nd_swa_sink_prefill(const void *q, const void *k, const void *v,
+                        nd_dtype dtype, int batch, int T, int n_q_heads,
+                        int n_kv_heads, int head_dim, const int32_t *seg_ids,
+                        const uint8_t *sink, int window, float rope_theta,
+                        const void *pooled_k, const void *pooled_v, int block,
+                        void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, nd_stream_t stream);
+
+/*
+ * Rotary embedding (rotate-half) of x at positions 0..T-1 of each row, the
+ * rotation [C3] "Pool before rotating, not after" applies to q and k.
+ *   x, y  bf16 [batch][T][n_heads][head_dim]  (y may equal x: in place)
+ * Angles are computed in fp32: angle = t * theta^(-2i/head_dim).
+ */
+ND_API int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads,
+                  int head_dim, float rope_theta, nd_stream_t stream);
+
+/*
+ * Block pooling with midpoint rotation ([C3] "Pool before rotating, not
+ * after"): pooled_k[j] = mean(k[j*block .. j*block+block-1]) rotated at
+ * position min(j*block + block/2, T-1); pooled_v[j] = the mean of v (not
+ * rotated).  Means are accumulated in fp32.  rope_theta == 0: no rotation.
+ *   k, v                bf16 [batch][T][n_heads][head_dim]  (before rotation)
+ *   pooled_k, pooled_v  bf16 [batch][T/block][n_heads][head_dim]
+ */
+ND_API int nd_kv_compress_pool(const void *k, const void *v, int batch, int T,
+                        int n_heads, int head_dim, int block, float rope_theta,
+                        void *pooled_k, void *pooled_v, nd_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* KV budget window (host only)                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * kv_budget_window and effective_kv_window of [N2] "Effective KV Window:
+ * Bounding the Cache Size" with the constants of [N1] "256 这个窗口宽度从哪来"
+ * (budget 11 MiB + 512 KiB, group 32, minimum window 160):
+ *   head_dim = (attn_dim or d_model) / num_heads     (attn_dim 0 = unset)
+ *   kv       = num_kv_heads * head_dim
+ *   per_pos  = num_layers * (2 kv + 2 (kv/32) * 4) + n_engram_sites * (d_model + 128)
+ *   budget   = max(160, min(((11.5 MiB / per_pos) / 32) * 32, max_seq_len))
+ *   effective = kv_window ? min(budget, kv_window) : budget
+ * Exact integer arithmetic on the host; no device is touched.
+ * Returns ND_ERR_INVALID_ARG for a NULL pointer, num_heads <= 0, negative
+ * fields, or per_pos == 0.
+ */
+typedef struct {
+  int d_model, attn_dim, num_heads, num_kv_heads, num_layers, n_engram_sites,
+      max_seq_len, kv_window;
+} nd_model_cfg;
+
+ND_API int nd_kv_budget_window(const nd_model_cfg *cfg, int *budget_out,
+                        int *effective_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ND_H_ */

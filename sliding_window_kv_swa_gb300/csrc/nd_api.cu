@@ -1,0 +1,313 @@
+// nd_api.cu -- the extern "C" entry points of libnd (see include/nd.h):
+// host-side argument validation, workspace carving and kernel dispatch.
+// Nothing here allocates memory; nothing here synchronises except
+// nd_device_errors().
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "nd.h"
+#include "nd_internal.h"
+
+namespace nd {
+
+// Device error word: kernels OR flags into it (bounded waits that gave up,
+// cache metadata out of range).  One copy per device the module is loaded on.
+__device__ int g_device_errors = 0;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_ptr[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = int(e);
+  return ND_ERR_CUDA;
+}
+
+// Returns ND_OK if the current device is an sm_103 part.
+int check_device(int *dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return ND_ERR_UNSUPPORTED;
+  if (dev_out) *dev_out = dev;
+  int ok = __atomic_load_n(&g_arch_ok[dev], __ATOMIC_ACQUIRE);
+  if (ok == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    ok = (major == 10 && minor == 3) ? 1 : -1;
+    __atomic_store_n(&g_arch_ok[dev], ok, __ATOMIC_RELEASE);
+  }
+  return ok == 1 ? ND_OK : ND_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int finish(cudaError_t e) { return e == cudaSuccess ? ND_OK : fail_cuda(e); }
+
+int validate_cache(const nd_kv_cache *c) {
+  if (!c) return ND_ERR_INVALID_ARG;
+  if (c->batch < 0 || c->n_kv_heads <= 0 || c->sink_cap < 0 || c->ring_cap < 0)
+    return ND_ERR_INVALID_ARG;
+  if (c->head_dim <= 0 || c->head_dim % 32) return ND_ERR_INVALID_ARG;
+  if (c->batch == 0) return ND_OK;
+  if (!c->k_codes || !c->v_codes || !c->k_scale || !c->v_scale || !c->sink_len ||
+      !c->ring_start || !c->ring_len || !c->seq_len)
+    return ND_ERR_INVALID_ARG;
+  if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_scale) ||
+      !aligned16(c->v_scale))
+    return ND_ERR_INVALID_ARG;
+  return ND_OK;
+}
+
+}  // namespace
+
+int *device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int *p = __atomic_load_n(&g_err_ptr[dev], __ATOMIC_ACQUIRE);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_errors) != cudaSuccess) return nullptr;
+    __atomic_store_n(&g_err_ptr[dev], static_cast<int *>(addr), __ATOMIC_RELEASE);
+  }
+  return g_err_ptr[dev];
+}
+
+}  // namespace nd
+
+using namespace nd;
+
+extern "C" {
+
+const char *nd_version(void) { return "nd 0.1.0 sm_103a"; }
+
+const char *nd_status_string(int status) {
+  switch (status) {
+    case ND_OK: return "ND_OK";
+    case ND_ERR_INVALID_ARG: return "ND_ERR_INVALID_ARG";
+    case ND_ERR_UNSUPPORTED: return "ND_ERR_UNSUPPORTED";
+    case ND_ERR_CUDA: return "ND_ERR_CUDA";
+    case ND_ERR_WORKSPACE: return "ND_ERR_WORKSPACE";
+    case ND_ERR_DEVICE: return "ND_ERR_DEVICE";
+    default: return "ND_ERR_UNKNOWN";
+  }
+}
+
+int nd_last_cuda_error(void) { return t_last_cuda_error; }
+
+int nd_device_errors(int *flags_out, int clear) {
+  if (!flags_out) return ND_ERR_INVALID_ARG;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e);
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_errors, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  *flags_out = v;
+  if (clear && v) {
+    int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_errors, &zero, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return ND_OK;
+}
+
+int nd_kv_append_quant(const nd_kv_cache *cache, const void *k_new, const void *v_new,
+                       int to_sink, nd_stream_t stream) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (cache->batch == 0) return ND_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ND_ERR_INVALID_ARG;
+  if (!to_sink && cache->ring_cap <= 0) return ND_ERR_INVALID_ARG;
+  if (to_sink && cache->sink_cap <= 0) return ND_ERR_INVALID_ARG;
+  const int d = cache->head_dim;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return ND_ERR_UNSUPPORTED;
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  return finish(launch_kv_append_quant(*cache, k_new, v_new, to_sink ? 1 : 0, device_error_word(),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim, int8_t *codes, float *scales,
+                     nd_stream_t stream) {
+  if (n_rows < 0) return ND_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return head_dim > 0 && head_dim % 32 == 0 ? ND_ERR_UNSUPPORTED : ND_ERR_INVALID_ARG;
+  if (n_rows == 0) return ND_OK;
+  if (!x || !codes || !scales || !aligned16(x) || !aligned16(codes) || !aligned16(scales))
+    return ND_ERR_INVALID_ARG;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  return finish(launch_kv_quant_rows(x, n_rows, head_dim, codes, scales,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t nd_swa_sink_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                         int max_slots) {
+  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || max_slots <= 0) return 0;
+  return decode_workspace_bytes(batch, n_q_heads, head_dim, max_slots, n_kv_heads);
+}
+
+int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, int window,
+                       void *out, float *lse, void *workspace, size_t workspace_bytes,
+                       nd_stream_t stream) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return ND_ERR_INVALID_ARG;
+  const int G = n_q_heads / cache->n_kv_heads;
+  if (G > 8) return ND_ERR_UNSUPPORTED;
+  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
+  if (cache->batch == 0) return ND_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  const int max_slots = cache->sink_cap + (cache->ring_cap < window ? cache->ring_cap : window);
+  if (max_slots <= 0) return ND_ERR_INVALID_ARG;
+  DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots);
+  if (pl.n_split > 1) {
+    size_t need = size_t(cache->batch) * n_q_heads * pl.n_split * (cache->head_dim + 2) * sizeof(float);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ND_ERR_WORKSPACE;
+  }
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  return finish(launch_decode(q, *cache, n_q_heads, window, out, lse, workspace, workspace_bytes,
+                              device_error_word(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,
+                                          int n_kv_heads, int head_dim, float rope_theta,
+                                          int block) {
+  if (batch <= 0 || T <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return 0;
+  const size_t esz = dtype == ND_F32 ? 4 : 2;
+  size_t bytes = 0;
+  if (rope_theta != 0.f) {
+    bytes += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
+    bytes += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
+  }
+  if (dtype == ND_BF16) bytes += round_up(prefill_plan_bytes(batch, T, block), 256);
+  return bytes;
+}
+
+int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dtype, int batch,
+                        int T, int n_q_heads, int n_kv_heads, int head_dim,
+                        const int32_t *seg_ids, const uint8_t *sink, int window, float rope_theta,
+                        const void *pooled_k, const void *pooled_v, int block, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+  if (dtype != ND_F32 && dtype != ND_BF16) return ND_ERR_INVALID_ARG;
+  if (batch < 0 || T < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || window < 0 || block < 0)
+    return ND_ERR_INVALID_ARG;
+  if (n_q_heads % n_kv_heads) return ND_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128)
+    return head_dim > 0 && head_dim % 2 == 0 ? ND_ERR_UNSUPPORTED : ND_ERR_INVALID_ARG;
+  if (size_t(batch) * T == 0) return ND_OK;
+  if (!q || !k || !v || !out) return ND_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  if (block > 0) {
+    if (dtype != ND_BF16) return ND_ERR_UNSUPPORTED;
+    if (seg_ids || sink || window < 1) return ND_ERR_INVALID_ARG;
+    if (!pooled_k || !pooled_v || !aligned16(pooled_k) || !aligned16(pooled_v))
+      return ND_ERR_INVALID_ARG;
+  }
+  const size_t need = nd_swa_sink_prefill_workspace_size(dtype, batch, T, n_q_heads, n_kv_heads,
+                                                         head_dim, rope_theta, block);
+  if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return ND_ERR_WORKSPACE;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dtype = dtype;
+  a.batch = batch;
+  a.T = T;
+  a.Hq = n_q_heads;
+  a.Hkv = n_kv_heads;
+  a.d = head_dim;
+  a.seg_ids = seg_ids;
+  a.sink = sink;
+  a.window = window;
+  a.pooled_k = block > 0 ? pooled_k : nullptr;
+  a.pooled_v = block > 0 ? pooled_v : nullptr;
+  a.block = block;
+  a.out = out;
+  a.lse = lse;
+
+  char *ws = static_cast<char *>(workspace);
+  const size_t esz = dtype == ND_F32 ? 4 : 2;
+  if (rope_theta != 0.f) {
+    void *qr = ws;
+    ws += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
+    void *kr = ws;
+    ws += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
+    cudaError_t e = launch_rope_qk(q, qr, n_q_heads, k, kr, n_kv_heads, batch, T, head_dim,
+                                   rope_theta, dtype == ND_F32, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    a.q = qr;
+    a.k = kr;
+  }
+  if (dtype == ND_F32) return finish(launch_prefill_f32(a, s));
+  return finish(launch_prefill_tc(a, ws, device_error_word(), s));
+}
+
+int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
+                  float rope_theta, nd_stream_t stream) {
+  if (batch < 0 || T < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2) return ND_ERR_INVALID_ARG;
+  if (head_dim > 256) return ND_ERR_UNSUPPORTED;
+  if (size_t(batch) * T == 0) return ND_OK;
+  if (!x || !y) return ND_ERR_INVALID_ARG;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  return finish(launch_rope(x, y, batch, T, n_heads, head_dim, rope_theta,
+                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nd_kv_compress_pool(const void *k, const void *v, int batch, int T, int n_heads, int head_dim,
+                        int block, float rope_theta, void *pooled_k, void *pooled_v,
+                        nd_stream_t stream) {
+  if (batch < 0 || T < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2 || block <= 0)
+    return ND_ERR_INVALID_ARG;
+  if (head_dim > 256) return ND_ERR_UNSUPPORTED;
+  if (size_t(batch) * (T / block) == 0) return ND_OK;
+  if (!k || !v || !pooled_k || !pooled_v) return ND_ERR_INVALID_ARG;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  return finish(launch_compress_pool(k, v, batch, T, n_heads, head_dim, block, rope_theta, pooled_k,
+                                     pooled_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int nd_kv_budget_window(const nd_model_cfg *cfg, int *budget_out, int *effective_out) {
+  if (!cfg || !budget_out) return ND_ERR_INVALID_ARG;
+  if (cfg->num_heads <= 0 || cfg->d_model < 0 || cfg->attn_dim < 0 || cfg->num_kv_heads < 0 ||
+      cfg->num_layers < 0 || cfg->n_engram_sites < 0 || cfg->max_seq_len < 0 || cfg->kv_window < 0)
+    return ND_ERR_INVALID_ARG;
+  const int64_t kBudgetBytes = 11LL * 1024 * 1024 + 512LL * 1024;
+  const int64_t kGroup = 32, kMin = 160;
+  const int64_t head_dim = int64_t(cfg->attn_dim ? cfg->attn_dim : cfg->d_model) / cfg->num_heads;
+  const int64_t kv = int64_t(cfg->num_kv_heads) * head_dim;
+  const int64_t per_pos = int64_t(cfg->num_layers) * (2 * kv + 2 * (kv / kGroup) * 4) +
+                          int64_t(cfg->n_engram_sites) * (cfg->d_model + kGroup * 4);
+  if (per_pos <= 0) return ND_ERR_INVALID_ARG;
+  int64_t w = (kBudgetBytes / per_pos) / kGroup * kGroup;
+  if (w > cfg->max_seq_len) w = cfg->max_seq_len;
+  if (w < kMin) w = kMin;
+  *budget_out = int(w);
+  if (effective_out)
+    *effective_out = cfg->kv_window ? int(w < cfg->kv_window ? w : cfg->kv_window) : int(w);
+  return ND_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// nd_common.cuh -- device helpers shared by the libnd kernels (sm_103a only).
+//
+// Bounded waits: every mbarrier wait in this library polls at most
+// ND_WAIT_LIMIT times and then records flag ND_DEVERR_TIMEOUT in the
+// device error word instead of spinning forever.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define ND_DEVERR_TIMEOUT 1
+#define ND_DEVERR_METADATA 2
+
+namespace nd {
+
+// Kernels OR flags into the device error word whose address the host passes
+// in (see nd_device_errors()).
+__device__ __forceinline__ void raise_device_error(int *err, int flag) {
+  if (err) atomicOr(err, flag);
+}
+
+constexpr uint32_t kWaitLimit = 1u << 24;  // polls of try_wait (each may sleep)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false (and raises the
+// timeout flag) if the phase did not complete within kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  raise_device_error(err, ND_DEVERR_TIMEOUT);
+  return false;
+}
+
+// ---------------------------------------------------------------- conversions
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Two int8 codes -> half2, exactly.  `w` holds four codes already biased to
+// unsigned (code + 128, i.e. xor 0x80 per byte).  Each selected byte u becomes
+// the low mantissa byte of an fp16 with exponent 2^10 (value 1024 + u); one
+// packed subtract of 1152 leaves the signed code (|code| <= 127 is exact).
+// sel_lo selects bytes (0,1), sel_hi bytes (2,3).
+__device__ __forceinline__ uint32_t codes_to_half2(uint32_t w_biased, uint32_t sel) {
+  uint32_t h = prmt(w_biased, 0x64646464u, sel);
+  uint32_t r;
+  const uint32_t bias = 0x64806480u;  // half2(1152, 1152)
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(bias));
+  return r;
+}
+constexpr uint32_t kSelBytes01 = 0x5140u;  // [b0, 0x64, b1, 0x64]
+constexpr uint32_t kSelBytes23 = 0x5342u;  // [b2, 0x64, b3, 0x64]
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- mma.sync
+// D = A * B + C, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float &d0, float &d1, float &d2, float &d3,
+                                              uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+}  // namespace nd

@@ -1,0 +1,63 @@
+// nd_internal.h -- launch functions behind the C ABI (host side, C++).
+// nd_api.cu validates arguments and then calls these; each enqueues kernels on
+// `stream` and returns the CUDA error of its launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "nd.h"
+
+namespace nd {
+
+// Address of the current device's error word (see nd_device_errors()).
+int *device_error_word();
+
+cudaError_t launch_kv_append_quant(const nd_kv_cache &c, const void *k_new, const void *v_new,
+                                   int to_sink, int *err, cudaStream_t stream);
+
+cudaError_t launch_kv_quant_rows(const void *x, int64_t n_rows, int head_dim, int8_t *codes,
+                                 float *scales, cudaStream_t stream);
+
+struct DecodePlan {
+  int n_split;        // CTAs per (sequence, kv head)
+  int slots_per_cta;  // multiple of 16
+  int max_slots;      // upper bound of visible slots per sequence
+};
+DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots);
+size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_slots,
+                              int n_kv_heads_hint);
+cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, int window,
+                          void *out, float *lse, void *ws, size_t ws_bytes, int *err,
+                          cudaStream_t stream);
+
+cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
+                        float theta, cudaStream_t stream);
+
+cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
+                           int batch, int T, int head_dim, float theta, bool f32,
+                           cudaStream_t stream);
+
+cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T, int n_heads,
+                                 int head_dim, int block, float theta, void *pk, void *pv,
+                                 cudaStream_t stream);
+
+struct PrefillArgs {
+  const void *q, *k, *v;  // after rotation, if any
+  nd_dtype dtype;
+  int batch, T, Hq, Hkv, d;
+  const int32_t *seg_ids;  // may be NULL
+  const uint8_t *sink;     // may be NULL
+  int window;
+  const void *pooled_k, *pooled_v;  // may be NULL
+  int block;                        // 0 = no pooled columns
+  void *out;
+  float *lse;  // may be NULL
+};
+
+size_t prefill_plan_bytes(int batch, int T, int block);
+cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream);
+
+}  // namespace nd

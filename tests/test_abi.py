@@ -1,0 +1,112 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every entry point
+nd.h declares, rejects bad arguments on the host, and its host-only budget
+window equals the oracle's bit for bit.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from conftest import ROOT
+from workloads import philox
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "nd.h")).read()
+    return sorted(set(re.findall(r"ND_API\s+[\w\s\*]*?\b(nd_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_entry_point():
+    import sliding_window_kv_swa_gb300 as nd
+    lib = ctypes.CDLL(nd.library_path())
+    names = declared_entry_points()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(nd.EXPORTED)
+
+
+def test_version_and_status_strings():
+    import sliding_window_kv_swa_gb300 as nd
+    assert "sm_103a" in nd.nd_version()
+    assert nd.nd_status_string(0) == "ND_OK"
+    assert nd.nd_status_string(1) == "ND_ERR_INVALID_ARG"
+
+
+def test_budget_window_matches_oracle():
+    import sliding_window_kv_swa_gb300 as nd
+    rng = philox(71)
+    for _ in range(500):
+        h = int(rng.choice([1, 2, 4, 8, 16, 32]))
+        kvh = int(rng.choice([x for x in (1, 2, 4, 8) if x <= h]))
+        d = int(rng.choice([64, 128, 256, 512, 1024, 4096]))
+        a = int(rng.choice([0, 0, 256, 512]))
+        L = int(rng.integers(0, 48))
+        sites = int(rng.integers(0, 3))
+        mx = int(rng.integers(1, 70000))
+        kvw = int(rng.choice([0, 128, 256, 4096]))
+        want = oracle.kv_budget_window(d, a, h, kvh, L, sites, mx)
+        if want < 0:
+            with pytest.raises(nd.NDError):
+                nd.nd_kv_budget_window(d, a, h, kvh, L, sites, mx, kvw)
+            continue
+        b, e = nd.nd_kv_budget_window(d, a, h, kvh, L, sites, mx, kvw)
+        assert b == want
+        assert e == oracle.effective_kv_window(want, kvw)
+
+
+def test_budget_window_rejects_bad_config():
+    import sliding_window_kv_swa_gb300 as nd
+    with pytest.raises(nd.NDError) as ei:
+        nd.nd_kv_budget_window(512, 0, 0, 2, 12, 2, 4096)
+    assert ei.value.status == 1
+    with pytest.raises(nd.NDError):
+        nd.nd_kv_budget_window(512, 0, 8, 2, 0, 0, 4096)   # per_pos == 0
+
+
+def test_host_validation_before_any_device_work():
+    import sliding_window_kv_swa_gb300 as nd
+    lib = ctypes.CDLL(nd.library_path())
+    lib.nd_swa_sink_prefill.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    # bad dtype, head_dim, GQA ratio, negative window: all rejected on the host
+    args = lambda dt, hq, hkv, d, w, blk=0, seg=None: (
+        P(16), P(16), P(16), dt, 1, 8, hq, hkv, d, seg, None, w, ctypes.c_float(0.0),
+        None, None, blk, P(16), None, None, ctypes.c_size_t(0), None)
+    assert lib.nd_swa_sink_prefill(*args(7, 4, 1, 64, 0)) == 1
+    assert lib.nd_swa_sink_prefill(*args(1, 4, 1, 96, 0)) == 2
+    assert lib.nd_swa_sink_prefill(*args(1, 6, 4, 64, 0)) == 1
+    assert lib.nd_swa_sink_prefill(*args(1, 4, 1, 64, -1)) == 1
+    # compressed variant needs bf16, no segments, window >= 1, pooled tensors
+    assert lib.nd_swa_sink_prefill(*args(0, 4, 1, 64, 8, blk=4)) == 2
+    assert lib.nd_swa_sink_prefill(*args(1, 4, 1, 64, 0, blk=4)) == 1
+    assert lib.nd_swa_sink_prefill(*args(1, 4, 1, 64, 8, blk=4, seg=P(16))) == 1
+    # misaligned pointer
+    bad = list(args(1, 4, 1, 64, 0))
+    bad[0] = P(18)
+    assert lib.nd_swa_sink_prefill(*bad) == 1
+    # decode: window < 1 and G > 8
+    cache = nd.nd._Cache(1, 1, 64, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
+    lib.nd_swa_sink_decode.restype = ctypes.c_int
+    assert lib.nd_swa_sink_decode(P(16), ctypes.byref(cache), 1, 0, P(16), None, None,
+                                  ctypes.c_size_t(0), None) == 1
+    assert lib.nd_swa_sink_decode(P(16), ctypes.byref(cache), 16, 8, P(16), None, None,
+                                  ctypes.c_size_t(0), None) == 2
+    # workspace required when the decode splits (1 sequence, 64 + 256 slots)
+    big = nd.nd._Cache(1, 1, 64, 64, 256, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert lib.nd_swa_sink_decode(P(16), ctypes.byref(big), 4, 256, P(16), None, None,
+                                  ctypes.c_size_t(0), None) == 4
+    # append: head_dim not a multiple of 32
+    c2 = nd.nd._Cache(1, 1, 48, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert lib.nd_kv_append_quant(ctypes.byref(c2), P(16), P(16), 0, None) == 1
+
+
+def test_workspace_sizes():
+    import sliding_window_kv_swa_gb300 as nd
+    # decode B64 Hq8 Hkv2 d64, 320 slots: five splits, (64+2) floats per partial
+    assert nd.nd_swa_sink_decode_workspace_size(64, 8, 2, 64, 320) == 64 * 8 * 5 * 66 * 4
+    assert nd.nd_swa_sink_decode_workspace_size(512, 32, 8, 128, 1280) == 0   # no split
+    # prefill with rotation keeps rotated copies of q and k
+    n = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, 1, 512, 4, 1, 64, 10000.0, 0)
+    assert n >= 512 * 4 * 64 * 4 + 512 * 1 * 64 * 4

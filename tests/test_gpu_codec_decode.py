@@ -1,0 +1,222 @@
+"""GPU parity: int8 group-32 codec, fused quantise-and-append, and decode,
+against the fp64 oracle (codes and cache metadata bit-exact; decode outputs
+within max-abs 2e-2 / mean-abs 2e-3, the bf16 tolerance)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close_bf16, dev, dev_bf16, host, need_gpu, no_device_errors
+from workloads import (bf16_bits_to_f32, decode_b64, decode_cache, decode_sweep, normal_bf16, philox,
+                       random_codes, to_bf16_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+    yield
+    no_device_errors()
+
+
+def nd():
+    import sliding_window_kv_swa_gb300 as m
+    return m
+
+
+# ---------------------------------------------------------------- codec
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+def test_quant_rows_bit_exact(d):
+    rng = philox(200 + d)
+    n = 3001
+    x = rng.standard_normal((n, d), dtype=np.float32) * rng.uniform(1e-3, 1e3, (n, 1)).astype(np.float32)
+    x[5] = 0.0                                    # zero group -> scale 0
+    x[6, :32] = 1e-30                             # tiny values (bf16 subnormal range)
+    bits = to_bf16_bits(x)
+    codes = torch.empty((n, d), dtype=torch.int8, device="cuda")
+    scales = torch.empty((n, d // 32), dtype=torch.float32, device="cuda")
+    nd().nd_kv_quant_rows(dev_bf16(bits), codes, scales)
+    wc, ws = oracle.quant_g32(bf16_bits_to_f32(bits))
+    np.testing.assert_array_equal(host(codes), wc)
+    np.testing.assert_array_equal(host(scales).view(np.uint32), ws.view(np.uint32))
+
+
+def test_quant_rows_golden_ties():
+    from test_oracle_attention import read_codec_fixture
+    groups = read_codec_fixture()
+    x = np.array([g["x"] for g in groups], np.float32).reshape(1, -1)
+    codes = torch.empty((1, 128), dtype=torch.int8, device="cuda")
+    scales = torch.empty((1, 4), dtype=torch.float32, device="cuda")
+    nd().nd_kv_quant_rows(dev_bf16(to_bf16_bits(x)), codes, scales)
+    np.testing.assert_array_equal(host(codes).reshape(-1), np.array([g["code"] for g in groups]).reshape(-1))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_append_sequence_matches_oracle(d):
+    """Sinks first, then the ring fills, wraps twice; every step bit-exact."""
+    B, Hkv, S, W = 5, 3, 4, 8
+    rng = philox(300 + d)
+    ref = oracle.Cache(B, Hkv, d, S, W)
+    cache = nd().KVCache.empty(B, Hkv, d, S, W)
+    for step in range(S + 2 * W + 3):
+        to_sink = step < S
+        kb, kf = normal_bf16(rng, (B, Hkv, d))
+        vb, vf = normal_bf16(rng, (B, Hkv, d))
+        nd().nd_kv_append_quant(cache, dev_bf16(kb), dev_bf16(vb), to_sink)
+        assert oracle.kv_append(ref, kf, vf, to_sink) == 0
+        for name in ("k_codes", "v_codes", "k_scale", "v_scale", "sink_len", "ring_start", "ring_len", "seq_len"):
+            np.testing.assert_array_equal(host(getattr(cache, name)), getattr(ref, name), err_msg=f"{name} step {step}")
+
+
+def test_rejected_sink_append_sets_flag_and_writes_nothing():
+    B, Hkv, d, S, W = 2, 1, 64, 2, 4
+    cache = nd().KVCache.empty(B, Hkv, d, S, W)
+    rng = philox(310)
+    kb, _ = normal_bf16(rng, (B, Hkv, d))
+    nd().nd_kv_append_quant(cache, dev_bf16(kb), dev_bf16(kb), False)   # ring token first
+    before = host(cache.k_codes).copy()
+    nd().nd_kv_append_quant(cache, dev_bf16(kb), dev_bf16(kb), True)    # then a sink: rejected
+    assert nd().nd_device_errors(clear=True) == 2
+    np.testing.assert_array_equal(host(cache.k_codes), before)
+    np.testing.assert_array_equal(host(cache.sink_len), [0, 0])
+    np.testing.assert_array_equal(host(cache.seq_len), [1, 1])
+
+
+# ---------------------------------------------------------------- decode
+
+def device_cache(ref: "oracle.Cache"):
+    c = nd().KVCache(dev(ref.k_codes), dev(ref.v_codes), dev(ref.k_scale), dev(ref.v_scale),
+                     dev(ref.sink_len), dev(ref.ring_start), dev(ref.ring_len), dev(ref.seq_len),
+                     ref.sink_cap, ref.ring_cap)
+    return c
+
+
+def oracle_cache(w, S, W):
+    B, Hkv, ns, d = w["k"].shape
+    ref = oracle.Cache(B, Hkv, d, S, W)
+    ref.k_codes[...], ref.k_scale[...] = oracle.quant_g32(w["k"])
+    ref.v_codes[...], ref.v_scale[...] = oracle.quant_g32(w["v"])
+    for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
+        getattr(ref, f)[...] = w[f]
+    return ref
+
+
+def run_decode(ref, q_bits, window, lse=True):
+    B, Hq, d = q_bits.shape
+    cache = device_cache(ref)
+    out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+    l = torch.empty((B, Hq), dtype=torch.float32, device="cuda") if lse else None
+    nd().nd_swa_sink_decode(dev_bf16(q_bits), cache, window, out=out, lse=l)
+    return host(out), (host(l) if lse else None)
+
+
+def test_decode_b64_matches_oracle():
+    w = decode_b64()
+    ref = oracle_cache(w, 64, 256)
+    got, lse = run_decode(ref, w["q_bits"], 256)
+    want, wlse = oracle.decode(w["q"], ref, 256)
+    assert_close_bf16(got, want, "decode B64")
+    np.testing.assert_allclose(lse, wlse, atol=2e-3, rtol=0)
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 1, 64), (8, 8, 128), (16, 2, 128), (6, 2, 64), (32, 8, 128)])
+def test_decode_partial_rings_and_windows(Hq, Hkv, d):
+    rng = philox(400 + Hq + d)
+    S, W, B = 24, 40, 7
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=401 + Hq, full=False)
+    ref = oracle_cache(w, S, W)
+    # per-sequence variety: fewer sinks, empty ring, wrapped ring
+    ref.sink_len[:] = [24, 0, 5, 24, 17, 1, 24]
+    ref.ring_len[:] = [40, 13, 0, 40, 1, 40, 27]
+    ref.ring_start[:] = [7, 0, 0, 39, 0, 0, 0]
+    ref.seq_len[:] = ref.sink_len + ref.ring_len + np.array([7, 0, 0, 39, 0, 0, 0])
+    for window in (W, 17, 1, 3 * W):
+        got, lse = run_decode(ref, w["q_bits"], window)
+        want, wlse = oracle.decode(w["q"], ref, window)
+        assert_close_bf16(got, want, f"decode window {window}")
+        np.testing.assert_allclose(lse, wlse, atol=2e-3, rtol=0)
+
+
+def test_decode_empty_cache_gives_zero_and_neg_inf():
+    B, Hq, Hkv, d, S, W = 3, 4, 1, 64, 8, 16
+    ref = oracle.Cache(B, Hkv, d, S, W)
+    q_bits, _ = normal_bf16(philox(410), (B, Hq, d))
+    got, lse = run_decode(ref, q_bits, W)
+    assert np.all(got == 0) and np.all(np.isneginf(lse))
+
+
+def test_decode_invariant_to_ring_rotation():
+    S, W, Hq, Hkv, d = 16, 64, 8, 2, 128
+    w = decode_cache(2, Hq, Hkv, d, S, W, seed=420, full=True)
+    ref = oracle_cache(w, S, W)
+    base, _ = run_decode(ref, w["q_bits"], W)
+    for shift in (1, 17, 63):
+        r2 = ref.copy()
+        for arr in (r2.k_codes, r2.v_codes, r2.k_scale, r2.v_scale):
+            arr[:, :, S:] = np.roll(arr[:, :, S:], shift, axis=2)
+        r2.ring_start[:] = (ref.ring_start + shift) % W
+        got, _ = run_decode(r2, w["q_bits"], W)
+        assert np.abs(got - base).max() <= 4e-3   # summation order only
+
+
+def test_decode_large_magnitudes_and_tiny_values():
+    """Power-of-two pre-scaling keeps fp16 operands exact at any magnitude."""
+    S, W, Hq, Hkv, d = 8, 32, 4, 1, 64
+    for mag in (1e-6, 1e-2, 1e3):
+        w = decode_cache(2, Hq, Hkv, d, S, W, seed=430, full=True)
+        w["k"] = bf16_bits_to_f32(to_bf16_bits(w["k"] * mag))
+        w["v"] = bf16_bits_to_f32(to_bf16_bits(w["v"] * mag))
+        q_bits = to_bf16_bits(w["q"] * (1.0 / max(mag, 1e-3)))
+        ref = oracle_cache(w, S, W)
+        got, _ = run_decode(ref, q_bits, W, lse=False)
+        want, _ = oracle.decode(bf16_bits_to_f32(q_bits), ref, W)
+        err = np.abs(got - want).max() / max(np.abs(want).max(), 1e-30)
+        assert err < 1e-2, (mag, err)
+
+
+@pytest.mark.parametrize("B", [32, 512])
+def test_decode_sweep_full_size_sampled(B):
+    """Configuration of the large-batch sweep (Hq32 Hkv8 d128, 1024 sinks + 256
+    ring) at full size, in the bench's launch configuration; sampled
+    sequences are checked against the oracle one by one."""
+    rng = philox(500 + B)
+    Hq, Hkv, d, S, W = 32, 8, 128, 1024, 256
+    kc, ks, vc, vs = random_codes(rng, B, Hkv, S + W, d)
+    ring_start = rng.integers(0, W, size=B).astype(np.int32)
+    meta = dict(sink_len=np.full(B, S, np.int32), ring_start=ring_start,
+                ring_len=np.full(B, W, np.int32), seq_len=(S + W + ring_start).astype(np.int32))
+    q_bits, q = normal_bf16(rng, (B, Hq, d))
+    cache = nd().KVCache(dev(kc), dev(vc), dev(ks), dev(vs), dev(meta["sink_len"]), dev(meta["ring_start"]),
+                         dev(meta["ring_len"]), dev(meta["seq_len"]), S, W)
+    out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+    nd().nd_swa_sink_decode(dev_bf16(q_bits), cache, W, out=out)
+    got = host(out)
+    for b in sorted(set([0, B - 1] + list(rng.integers(0, B, size=6)))):
+        ref = oracle.Cache(1, Hkv, d, S, W)
+        ref.k_codes[...], ref.k_scale[...] = kc[b:b + 1], ks[b:b + 1]
+        ref.v_codes[...], ref.v_scale[...] = vc[b:b + 1], vs[b:b + 1]
+        for f in meta:
+            getattr(ref, f)[...] = meta[f][b:b + 1]
+        want, _ = oracle.decode(q[b:b + 1], ref, W)
+        assert_close_bf16(got[b:b + 1], want, f"sequence {b}")
+
+
+def test_append_then_decode_step():
+    """The decode-sweep step: quantise-and-append one token, then attend."""
+    B, Hq, Hkv, d, S, W = 6, 32, 8, 128, 64, 32
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=600, full=True)
+    ref = oracle_cache(w, S, W)
+    cache = device_cache(ref)
+    rng = philox(601)
+    for step in range(3):
+        kb, kf = normal_bf16(rng, (B, Hkv, d))
+        vb, vf = normal_bf16(rng, (B, Hkv, d))
+        qb, qf = normal_bf16(rng, (B, Hq, d))
+        nd().nd_kv_append_quant(cache, dev_bf16(kb), dev_bf16(vb), False)
+        oracle.kv_append(ref, kf, vf, False)
+        out = nd().nd_swa_sink_decode(dev_bf16(qb), cache, W)
+        want, _ = oracle.decode(qf, ref, W)
+        assert_close_bf16(host(out), want, f"step {step}")
+    np.testing.assert_array_equal(host(cache.k_codes), ref.k_codes)

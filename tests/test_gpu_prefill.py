@@ -1,0 +1,200 @@
+"""GPU parity: prefill attention under make_causal_packing_mask, rotary
+embedding, block pooling with midpoint rotation and compressed attention,
+against the fp64 oracle.  fp32 paths within 1e-4; bf16 outputs within max-abs
+2e-2 / mean-abs 2e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (assert_close_bf16, assert_close_f32, dev, dev_bf16, host, need_gpu,
+                      no_device_errors)
+from workloads import (compressed, normal_bf16, packed_prefill, packed_segments, philox,
+                       tiny_prefill)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+    yield
+    no_device_errors()
+
+
+def nd():
+    import sliding_window_kv_swa_gb300 as m
+    return m
+
+
+def oracle_rows(q, k, v, seg, sink, window, theta, rows):
+    """Oracle prefill for sampled (b, t) rows: mask rows of one batch row at a
+    time, rotation of q at the sampled positions and of k at every position."""
+    out = np.empty((len(rows), q.shape[2], q.shape[3]))
+    lse = np.empty((len(rows), q.shape[2]))
+    for b in sorted(set(int(r[0]) for r in rows)):
+        idx = [i for i, r in enumerate(rows) if r[0] == b]
+        ts = np.array([rows[i][1] for i in idx])
+        T = q.shape[1]
+        qb = q[b, ts][None].astype(np.float64)
+        kb = k[b:b + 1].astype(np.float64)
+        if theta:
+            qb = oracle.rope(qb, ts.astype(np.int64), theta)
+            kb = oracle.rope(kb, np.arange(T), theta)
+        mask = oracle.causal_packing_mask(seg[b:b + 1], None if sink is None else sink[b:b + 1], window)
+        o, l = oracle.attention(qb, kb, v[b:b + 1], mask[:, ts])
+        out[idx], lse[idx] = o[0], l[0]
+    return out, lse
+
+
+# ---------------------------------------------------------------- fp32
+
+@pytest.mark.parametrize("single", [False, True])
+def test_tiny_prefill_fp32(single):
+    w = tiny_prefill(single_segment=single)
+    lse = torch.empty((1, 4, 512), dtype=torch.float32, device="cuda")
+    out = nd().nd_swa_sink_prefill(dev(w["q"]), dev(w["k"]), dev(w["v"]), dev(w["seg_ids"]), dev(w["sink"]),
+                                   w["window"], lse=lse)
+    want, wlse = oracle.swa_sink_prefill(w["q"], w["k"], w["v"], w["seg_ids"], w["sink"], w["window"])
+    assert_close_f32(host(out), want, "tiny prefill")
+    np.testing.assert_allclose(host(lse).transpose(0, 2, 1), wlse, atol=1e-4, rtol=0)
+
+
+def test_fp32_variants():
+    rng = philox(700)
+    B, T, Hq, Hkv, d = 2, 333, 6, 2, 128
+    q, k, v = (rng.standard_normal((B, T, H, d), dtype=np.float32) for H in (Hq, Hkv, Hkv))
+    seg, sink = packed_segments(rng, B, T, 2, 3, 40, 5, 30)
+    seg[1, 300:] = 0                                  # padding tail
+    for window, theta, use_sink in ((0, 0.0, False), (17, 0.0, True), (64, 10000.0, True)):
+        s = sink if use_sink else None
+        out = nd().nd_swa_sink_prefill(dev(q), dev(k), dev(v), dev(seg), None if s is None else dev(s),
+                                       window, rope_theta=theta)
+        want, _ = oracle.swa_sink_prefill(q, k, v, seg, s, window, theta)
+        assert_close_f32(host(out), want, f"fp32 W={window} theta={theta}")
+
+
+# ---------------------------------------------------------------- bf16
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T,Hq,Hkv,window", [(1, 2, 1, 256), (200, 4, 4, 32), (517, 8, 2, 100),
+                                             (1000, 4, 1, 256), (700, 3, 1, 0)])
+def test_bf16_packed_small(d, T, Hq, Hkv, window):
+    rng = philox(800 + T + d)
+    B = 2
+    qb, q = normal_bf16(rng, (B, T, Hq, d))
+    kb, k = normal_bf16(rng, (B, T, Hkv, d))
+    vb, v = normal_bf16(rng, (B, T, Hkv, d))
+    if T >= 200:
+        seg, sink = packed_segments(rng, B, T, 2, 3, T // 4, 3, T // 8)
+    else:
+        seg = np.ones((B, T), np.int32)
+        sink = np.zeros((B, T), np.uint8)
+        sink[:, :3] = 1
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
+    out = nd().nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), dev(sink), window,
+                                   rope_theta=10000.0, lse=lse)
+    want, wlse = oracle.swa_sink_prefill(q, k, v, seg, sink, window, 10000.0)
+    assert_close_bf16(host(out), want, f"bf16 T={T}")
+    np.testing.assert_allclose(host(lse).transpose(0, 2, 1), wlse, atol=2e-2, rtol=0)
+
+
+def test_bf16_padding_rows_are_zero():
+    rng = philox(900)
+    B, T, Hq, Hkv, d = 1, 300, 4, 2, 64
+    qb, q = normal_bf16(rng, (B, T, Hq, d))
+    kb, k = normal_bf16(rng, (B, T, Hkv, d))
+    vb, v = normal_bf16(rng, (B, T, Hkv, d))
+    seg = np.ones((B, T), np.int32)
+    seg[0, 100:180] = 0
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
+    out = host(nd().nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), None, 64, lse=lse))
+    assert np.all(out[0, 100:180] == 0)
+    assert np.all(np.isneginf(host(lse)[0, :, 100:180]))
+    want, _ = oracle.swa_sink_prefill(q, k, v, seg, None, 64)
+    assert_close_bf16(out, want, "padding")
+
+
+def test_packed_prefill_full_size_sampled():
+    """Packed-segment prefill at full size (B8 T4096 Hq32 Hkv8 d128, W256,
+    RoPE) in the bench's launch configuration; sampled rows vs the oracle."""
+    w = packed_prefill()
+    B, T, Hq, d = w["q"].shape
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
+    out = nd().nd_swa_sink_prefill(dev_bf16(w["q_bits"]), dev_bf16(w["k_bits"]), dev_bf16(w["v_bits"]),
+                                   dev(w["seg_ids"]), dev(w["sink"]), w["window"], rope_theta=w["rope_theta"],
+                                   lse=lse)
+    got = host(out)
+    rng = philox(901)
+    rows = [(b, t) for b in range(B) for t in (0, T - 1)]
+    rows += [(int(rng.integers(0, B)), int(rng.integers(0, T))) for _ in range(48)]
+    # rows at segment and sink boundaries
+    for b in (0, B - 1):
+        starts = np.nonzero(np.diff(w["seg_ids"][b]))[0] + 1
+        for s in starts[:3]:
+            rows += [(b, int(s)), (b, int(s) - 1), (b, int(s) + 300)]
+    rows = [(b, min(t, T - 1)) for b, t in rows]
+    want, wlse = oracle_rows(w["q"], w["k"], w["v"], w["seg_ids"], w["sink"], w["window"], w["rope_theta"], rows)
+    gr = np.stack([got[b, t] for b, t in rows])
+    assert_close_bf16(gr, want, "packed prefill sampled rows")
+    gl = np.stack([host(lse)[b, :, t] for b, t in rows])
+    np.testing.assert_allclose(gl, wlse, atol=2e-2, rtol=0)
+
+
+# ---------------------------------------------------------------- rope / pool / compressed
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_rope_matches_oracle(d):
+    rng = philox(1000 + d)
+    B, T, H = 2, 4096, 3
+    xb, x = normal_bf16(rng, (B, T, H, d))
+    y = host(nd().nd_rope_apply(dev_bf16(xb), rope_theta=10000.0))
+    want = oracle.rope(x, np.arange(T), 10000.0)
+    err = np.abs(y - want)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3      # bf16 output rounding
+    assert np.all(err <= np.abs(want) * 2 ** -8 + 1e-6)   # one bf16 rounding per element
+
+
+@pytest.mark.parametrize("block,T", [(4, 4096), (1, 100), (3, 101), (8, 64)])
+def test_compress_pool_matches_oracle(block, T):
+    rng = philox(1100 + block)
+    B, H, d = 2, 4, 64
+    kb, k = normal_bf16(rng, (B, T, H, d))
+    vb, v = normal_bf16(rng, (B, T, H, d))
+    pk, pv = nd().nd_kv_compress_pool(dev_bf16(kb), dev_bf16(vb), block, 10000.0)
+    _, kk, vv = oracle.compress(k, k, v, block, 10000.0)
+    nb = T // block
+    for got, want, name in ((host(pk), kk[:, :nb], "pooled k"), (host(pv), vv[:, :nb], "pooled v")):
+        err = np.abs(got - want)
+        assert np.all(err <= np.abs(want) * 2 ** -8 + 1e-6), name
+
+
+def test_compressed_prefill_full_size():
+    """Compressed-attention configuration at full size (B4 T4096 H16 d64, W256,
+    b4, RoPE): pool (GPU) + rotation + attention, every row vs the oracle."""
+    w = compressed()
+    B, T, H, d = w["q"].shape
+    pk, pv = nd().nd_kv_compress_pool(dev_bf16(w["k_bits"]), dev_bf16(w["v_bits"]), w["block"], w["rope_theta"])
+    out = nd().nd_swa_sink_prefill(dev_bf16(w["q_bits"]), dev_bf16(w["k_bits"]), dev_bf16(w["v_bits"]),
+                                   None, None, w["window"], rope_theta=w["rope_theta"], pooled_k=pk,
+                                   pooled_v=pv, block=w["block"])
+    got = host(out)
+    rng = philox(1200)
+    rows = np.array([(b, t) for b in range(B) for t in (0, 255, 256, 258, 259, 262, 263, 1000, T - 1)]
+                    + [(int(rng.integers(0, B)), int(rng.integers(0, T))) for _ in range(64)])
+    want, _ = oracle.compressed_prefill(w["q"], w["k"], w["v"], w["window"], w["block"], w["rope_theta"], rows=rows)
+    assert_close_bf16(np.stack([got[b, t] for b, t in rows]), want, "compressed sampled rows")
+
+
+@pytest.mark.parametrize("T,W,block", [(300, 16, 4), (129, 1, 2), (513, 64, 8), (64, 8, 1)])
+def test_compressed_prefill_small_all_rows(T, W, block):
+    rng = philox(1300 + T)
+    B, H, d = 2, 4, 64
+    qb, q = normal_bf16(rng, (B, T, H, d))
+    kb, k = normal_bf16(rng, (B, T, H, d))
+    vb, v = normal_bf16(rng, (B, T, H, d))
+    pk, pv = nd().nd_kv_compress_pool(dev_bf16(kb), dev_bf16(vb), block, 10000.0)
+    out = nd().nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), None, None, W, rope_theta=10000.0,
+                                   pooled_k=pk, pooled_v=pv, block=block)
+    want, _ = oracle.compressed_prefill(q, k, v, W, block, 10000.0)
+    assert_close_bf16(host(out), want, f"compressed T={T}")
