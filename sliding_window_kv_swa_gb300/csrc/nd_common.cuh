@@ -21,7 +21,7 @@ __device__ __forceinline__ void raise_device_error(int *err, int flag) {
   if (err) atomicOr(err, flag);
 }
 
-constexpr uint32_t kWaitLimit = 1u << 24;  // polls of try_wait (each may sleep)
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls of try_wait (each may sleep)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
