@@ -165,6 +165,35 @@ ND_API int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_h
                        int window, void *out, float *lse, void *workspace,
                        size_t workspace_bytes, nd_stream_t stream);
 
+/*
+ * nd_swa_sink_decode without a workspace argument.  The pages have no
+ * counterpart: this is a library convenience for callers that cannot
+ * allocate device memory -- a thread recording a CUDA graph with a frozen
+ * memory plan, a serving loop that must never call cudaMalloc (it may
+ * synchronise the device), or a host runtime that owns all device memory and
+ * passes a plugin only its inputs and outputs.
+ *
+ * Computes exactly what nd_swa_sink_decode computes, with the same arguments
+ * and results.  Its split-K scratch is one fixed device array of
+ * ND_NOALLOC_SCRATCH_BYTES inside libnd, present on every device that loads
+ * the library until the process exits.  The call allocates nothing and calls
+ * no allocating routine.
+ *  - Returns ND_ERR_WORKSPACE when the decode would need more scratch than
+ *    ND_NOALLOC_SCRATCH_BYTES (nd_swa_sink_decode_workspace_size tells how
+ *    much a shape needs); use nd_swa_sink_decode with a caller workspace then.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture
+ *    on that device.
+ *  - All calls on a device share the one array and each overwrites it, so
+ *    calls whose kernels may overlap on the GPU (different streams without
+ *    ordering between them) race; order them on one stream or use
+ *    nd_swa_sink_decode with separate workspaces.
+ */
+#define ND_NOALLOC_SCRATCH_BYTES (2u << 20)
+ND_API int nd_swa_sink_decode_noalloc(const void *q, const nd_kv_cache *cache,
+                                      int n_q_heads, int window, void *out,
+                                      float *lse, nd_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Prefill                                                                   */
 /* ------------------------------------------------------------------------ */

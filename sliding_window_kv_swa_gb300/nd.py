@@ -69,6 +69,7 @@ def _lib():
             "nd_kv_quant_rows": (I, [P, L, I, P, P, P]),
             "nd_swa_sink_decode_workspace_size": (S, [I, I, I, I, I]),
             "nd_swa_sink_decode": (I, [P, P, I, I, P, P, P, S, P]),
+            "nd_swa_sink_decode_noalloc": (I, [P, P, I, I, P, P, P]),
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
@@ -90,7 +91,8 @@ def library_path() -> str:
 
 EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_errors",
             "nd_kv_append_quant", "nd_kv_quant_rows", "nd_swa_sink_decode_workspace_size",
-            "nd_swa_sink_decode", "nd_swa_sink_prefill_workspace_size", "nd_swa_sink_prefill",
+            "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_prefill_workspace_size",
+            "nd_swa_sink_prefill",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
 
 
@@ -218,6 +220,21 @@ def nd_swa_sink_decode(q: torch.Tensor, cache: KVCache, window: int, out: Option
     _check("nd_swa_sink_decode", _lib().nd_swa_sink_decode(
         _ptr(q), ctypes.byref(s), Hq, int(window), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 2 << 20   # ND_NOALLOC_SCRATCH_BYTES in nd.h
+
+
+def nd_swa_sink_decode_noalloc(q: torch.Tensor, cache: KVCache, window: int, out: torch.Tensor,
+                               lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory).  `out` must be given:
+    this entry point allocates nothing.  Calls overlapping on the GPU race."""
+    B, Hq, d = q.shape
+    s = cache.struct()
+    _check("nd_swa_sink_decode_noalloc", _lib().nd_swa_sink_decode_noalloc(
+        _ptr(q), ctypes.byref(s), Hq, int(window), _ptr(out), _ptr(lse), _stream(stream)))
     return out
 
 

@@ -1,0 +1,70 @@
+"""nd_swa_sink_decode_noalloc: the decode entry point for callers that cannot
+allocate device memory (a thread recording a CUDA graph with a frozen memory
+plan, a serving loop that must not call cudaMalloc, a host runtime that owns
+all device memory).  Its split-K scratch is a fixed device array inside the
+library; these tests call it through the C ABI and check it against
+nd_swa_sink_decode with a caller workspace, on two calls in a row (the second
+call reuses the scratch the first one left behind), and check that shapes
+needing more scratch than the array holds are refused.
+
+This file is named to be collected last, so a run that stops at the first
+failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close_bf16, dev, dev_bf16, host, need_gpu
+from workloads import decode_b64, normal_bf16, philox
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_cache(nd, w, S, W):
+    ref = oracle.Cache(*w["k"].shape[:2], w["k"].shape[3], S, W)
+    ref.k_codes[...], ref.k_scale[...] = oracle.quant_g32(w["k"])
+    ref.v_codes[...], ref.v_scale[...] = oracle.quant_g32(w["v"])
+    for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
+        getattr(ref, f)[...] = w[f]
+    return nd.KVCache(dev(ref.k_codes), dev(ref.v_codes), dev(ref.k_scale), dev(ref.v_scale),
+                      dev(ref.sink_len), dev(ref.ring_start), dev(ref.ring_len), dev(ref.seq_len), S, W)
+
+
+def test_noalloc_decode_matches_workspace_decode_on_two_calls():
+    need_gpu()
+    import sliding_window_kv_swa_gb300 as nd
+    S, W = 64, 256
+    w = decode_b64()                               # B64 Hq8 Hkv2 d64: the decode splits
+    B, Hq, d = w["q"].shape
+    cache = _device_cache(nd, w, S, W)
+    need = nd.nd_swa_sink_decode_workspace_size(B, Hq, cache.n_kv_heads, d, S + W)
+    assert 0 < need <= nd.nd.NOALLOC_SCRATCH_BYTES
+    rng = philox(2024)
+    queries = [w["q_bits"], normal_bf16(rng, (B, Hq, d))[0]]
+    for call, q_bits in enumerate(queries):
+        q = dev_bf16(q_bits)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        want = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+        want_lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        nd.nd_swa_sink_decode(q, cache, W, out=want, lse=want_lse, workspace=ws)
+        got = torch.empty_like(want)
+        got_lse = torch.empty_like(want_lse)
+        nd.nd_swa_sink_decode_noalloc(q, cache, W, out=got, lse=got_lse)
+        torch.cuda.synchronize()
+        assert_close_bf16(host(got), host(want), f"noalloc call {call}")
+        np.testing.assert_allclose(host(got_lse), host(want_lse), atol=2e-3, rtol=0)
+    assert nd.nd_device_errors(clear=True) == 0
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch():
+    need_gpu()
+    import sliding_window_kv_swa_gb300 as nd
+    B, Hq, Hkv, d, S, W = 8, 64, 8, 128, 1024, 256
+    need = nd.nd_swa_sink_decode_workspace_size(B, Hq, Hkv, d, S + W)
+    assert need > nd.nd.NOALLOC_SCRATCH_BYTES
+    cache = nd.KVCache.empty(B, Hkv, d, S, W)
+    q = torch.zeros((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(nd.NDError) as ei:
+        nd.nd_swa_sink_decode_noalloc(q, cache, W, out=out)
+    assert ei.value.status == nd.nd.ND_ERR_WORKSPACE
