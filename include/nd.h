@@ -189,7 +189,7 @@ ND_API int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_h
  *    ordering between them) race; order them on one stream or use
  *    nd_swa_sink_decode with separate workspaces.
  */
-#define ND_NOALLOC_SCRATCH_BYTES (2u << 20)
+#define ND_NOALLOC_SCRATCH_BYTES (512u << 10)
 ND_API int nd_swa_sink_decode_noalloc(const void *q, const nd_kv_cache *cache,
                                       int n_q_heads, int window, void *out,
                                       float *lse, nd_stream_t stream);

@@ -1,5 +1,5 @@
 // decode.cu -- one decode step over the bounded int8 cache (sink slots + ring
-// window), split-K over slots, with a combine kernel for the splits.
+// window), with an optional split-K over slots and a combine kernel.
 //
 // What is computed: the decode mask of "256-token滑动窗口+KV sink：Needle 2工具钉住
 // 机制源码分析", section "256-token 滑动窗口：源码走读": the query at position
@@ -8,20 +8,28 @@
 // scale per 32 channels ("How the 256-Token Sliding Window Works with Tools as
 // KV Sinks in Needle", section "Effective KV Window").
 //
-// How: HBM-bound (about 7 flop per byte at G = 4).  Each CTA streams a slice of
-// the visible slots of one (sequence, KV head) straight from global memory
-// (8-byte and 4-byte loads that fill whole 32-byte sectors), converts codes to
-// fp16 in registers with byte permutes (exact for |code| <= 127), and lets
-// warp-level m16n8k16 tensor-core MMAs do the dot products, so the per-byte
-// ALU work is the conversion alone:
-//   QK : D[head][slot]   = q(fp16, rows = heads) x codes^T, one MMA pair per
-//        32-channel group so each group's partial is scaled by its own fp32
-//        scale; q is pre-scaled by a power of two so its fp16 copy is exact.
-//   PV : D[chan][head]   = codes^T(rows = channels) x P'^T, P' = p * v_scale,
-//        also pre-scaled by a per-group power of two (no fp16 subnormals).
-// The QK accumulator layout equals the PV B-operand layout, so
-// probabilities never leave registers.  Online softmax per head uses quad
-// shuffles; the four warps of a CTA are merged through shared memory.
+// How: HBM-bound (about 7 flop per byte at G = 4).  A CTA owns one (sequence,
+// KV head) -- or a slice of its visible slots when there are too few sequences
+// to fill the GPU -- and each warp walks 16-slot steps of it:
+//   copy : every lane issues 16-byte cp.async copies of K codes, V codes and
+//          scales for the step three steps ahead into the warp's own shared
+//          stages (XOR-swizzled 16-byte chunks, so the fragment reads below
+//          are bank-conflict free); no registers are tied up by loads in
+//          flight, and the warp never waits on other warps.
+//   math : codes become fp16 with byte permutes (exact for |code| <= 127) and
+//          warp-level m16n8k16 tensor-core MMAs do the dot products, so the
+//          per-byte ALU work is the conversion alone.
+//          QK : D[head][slot] = q(fp16, rows = heads) x codes^T, one MMA pair
+//               per 32-channel group so each group's fp32 scale multiplies its
+//               own partial; q is pre-scaled by a power of two (exact).
+//          PV : D[chan][head] = codes^T(rows = channels) x P'^T with
+//               P' = p * v_scale, pre-scaled per group by a power of two that
+//               only ever decreases (no fp16 overflow or subnormals).
+//          The QK accumulator layout equals the PV B-operand layout, so
+//          probabilities never leave registers; the online softmax uses quad
+//          shuffles.
+//   merge: the warps of a CTA merge through shared memory; split CTAs write
+//          (max, sum, O) partials that a combine kernel merges.
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -29,10 +37,9 @@ namespace nd {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
-constexpr int kStep = 16;            // slots per warp iteration (one MMA k-step)
-constexpr int kTargetCtas = 152 * 4;  // enough CTAs to fill every SM
+constexpr int kStep = 16;    // slots per warp step (one MMA k-step)
+constexpr int kStages = 4;   // copies in flight per warp: kStages - 1 steps ahead
+constexpr int kTargetCtas = 152;
 
 struct DecodeParams {
   const uint16_t *q;
@@ -46,11 +53,16 @@ struct DecodeParams {
   int *err;
 };
 
+template <int D>
+struct Stage {
+  static constexpr int kCodes = kStep * D;              // bytes of K (or V) codes per step
+  static constexpr int kScales = kStep * (D / 32) * 4;  // bytes of K (or V) scales per step
+  static constexpr int kBytes = 2 * kCodes + 2 * kScales;
+};
+
 __device__ __forceinline__ int ilog2_floor(float x) {  // x > 0, finite
   int e = int((__float_as_uint(x) >> 23) & 0xff) - 127;
-  if (e == -127) {  // subnormal
-    e = -127 + (31 - __clz(__float_as_uint(x) & 0x7fffff)) - 22;
-  }
+  if (e == -127) e = -127 + (31 - __clz(__float_as_uint(x) & 0x7fffff)) - 22;  // subnormal
   return e;
 }
 
@@ -60,9 +72,45 @@ __device__ __forceinline__ float exp2i(int e) {
   return __uint_as_float(uint32_t(e + 127) << 23);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(const DecodeParams p) {
+// Byte offset inside a stage: 16-byte chunks XOR-swizzled by the 128-byte
+// line index, a bijection inside every 128-byte line.
+__device__ __forceinline__ uint32_t swz(uint32_t a) { return a ^ (((a >> 7) & 7u) << 4); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ldsf(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const DecodeParams p) {
   constexpr int NG = D / 32;  // scale groups per row
+  using S = Stage<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ int s_meta[4];
+
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -71,23 +119,17 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(cons
   const int nslot = c.sink_cap + c.ring_cap;
   const size_t pair = size_t(b) * c.n_kv_heads + hkv;
 
-  __shared__ int s_meta[4];
-  __shared__ unsigned s_vmax[NG];
-  __shared__ float s_m[kWarps][8], s_l[kWarps][8];
-  __shared__ float s_o[kWarps][8][D];
-  __shared__ float s_qmax[8];
-
   if (threadIdx.x == 0) {
     int sl = c.sink_len[b], rs = c.ring_start[b], rl = c.ring_len[b];
-    bool sane = sl >= 0 && sl <= c.sink_cap && rl >= 0 && rl <= c.ring_cap && rs >= 0 &&
-                (c.ring_cap == 0 || rs < c.ring_cap);
+    const bool sane = sl >= 0 && sl <= c.sink_cap && rl >= 0 && rl <= c.ring_cap && rs >= 0 &&
+                      (c.ring_cap == 0 || rs < c.ring_cap);
     int total = 0, rs_eff = 0;
     if (!sane) {
       raise_device_error(p.err, ND_DEVERR_METADATA);
       sl = 0;
     } else {
-      int n_vis = rl < p.window ? rl : p.window;
-      int i0 = rl - n_vis;  // oldest visible ring entry (logical)
+      const int n_vis = rl < p.window ? rl : p.window;
+      const int i0 = rl - n_vis;  // oldest visible ring entry (logical)
       rs_eff = c.ring_cap ? (rs + i0) % c.ring_cap : 0;
       total = sl + n_vis;
     }
@@ -95,8 +137,38 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(cons
     s_meta[1] = rs_eff;
     s_meta[2] = total;
   }
-  if (threadIdx.x < NG) s_vmax[threadIdx.x] = 0u;
-  if (threadIdx.x < 8) s_qmax[threadIdx.x] = 0.f;
+
+  // ---- q fragments while the metadata read is in flight.  Thread t owns
+  //      channels 32*grp + 8t .. +7 of head g; k-step s uses 4s .. 4s+3.
+  uint32_t qa[NG][2][2];
+  float head_coef;  // 2^-Eq * log2(e) / sqrt(D), for head g
+  {
+    const bool row_ok = g < G;
+    const uint16_t *qh = p.q + (size_t(b) * p.Hq + hkv * G + (row_ok ? g : 0)) * D;
+    uint4 w[NG];
+    float qm = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp) {
+      w[grp] = row_ok ? *reinterpret_cast<const uint4 *>(qh + 32 * grp + 8 * t) : make_uint4(0, 0, 0, 0);
+      const uint32_t ws[4] = {w[grp].x, w[grp].y, w[grp].z, w[grp].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(ws[i])), fabsf(bf16_hi(ws[i]))));
+    }
+    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
+    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
+    const int eq = qm > 0.f ? 14 - ilog2_floor(qm) : 0;
+    const float up = exp2i(eq);
+    head_coef = exp2i(-eq) * (1.4426950408889634f * rsqrtf(float(D)));
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp) {
+      const uint32_t ws[4] = {w[grp].x, w[grp].y, w[grp].z, w[grp].w};
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        qa[grp][s][0] = pack_half2(bf16_lo(ws[2 * s]) * up, bf16_hi(ws[2 * s]) * up);
+        qa[grp][s][1] = pack_half2(bf16_lo(ws[2 * s + 1]) * up, bf16_hi(ws[2 * s + 1]) * up);
+      }
+    }
+  }
   __syncthreads();
   const int sink_len = s_meta[0], rs_eff = s_meta[1], total = s_meta[2];
   const int v_begin = split * p.slots_per_cta;
@@ -115,68 +187,45 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(cons
   const float *ks = c.k_scale + pair * nslot * NG;
   const float *vs = c.v_scale + pair * nslot * NG;
 
-  // ---- per-group max of the value scales over this CTA's slots (for the
-  //      power-of-two pre-scale of P'), and per-head max |q|.
-  {
-    float vmax[NG];
-#pragma unroll
-    for (int i = 0; i < NG; ++i) vmax[i] = 0.f;
-    for (int v = v_begin + threadIdx.x; v < v_end; v += kThreads) {
-      const float *row = vs + size_t(phys(v)) * NG;
-#pragma unroll
-      for (int i = 0; i < NG; ++i) vmax[i] = fmaxf(vmax[i], row[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < NG; ++i) {
-      float m = vmax[i];
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) atomicMax(&s_vmax[i], __float_as_uint(m));
-    }
-    // |q| max per head: warp w handles heads w, w + 4
-    for (int h = warp; h < G; h += kWarps) {
-      const uint16_t *qh = p.q + (size_t(b) * p.Hq + hkv * G + h) * D;
-      float m = 0.f;
-      for (int ch = lane; ch < D; ch += 32) m = fmaxf(m, fabsf(__uint_as_float(uint32_t(qh[ch]) << 16)));
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) s_qmax[h] = m;
-    }
-  }
-  __syncthreads();
+  const uint32_t my_stages = smem_u32(smem) + warp * kStages * S::kBytes;
+  // step n of this warp covers virtual slots base(n) .. base(n)+15
+  const int first = v_begin + warp * kStep;
+  const int n_steps = v_end > first ? (v_end - first + NW * kStep - 1) / (NW * kStep) : 0;
+  auto base_of = [&](int n) { return first + n * NW * kStep; };
 
-  // ---- q fragments (A operand of QK), channel permutation per group:
-  //      thread t owns channels 32*grp + 8t .. +7; k-step s uses 4s .. 4s+3.
-  uint32_t qa[NG][2][2];
-  float head_coef = 0.f;  // 2^-Eq * log2(e) / sqrt(D), for head g
-  {
-    const bool row_ok = g < G;
-    float qm = row_ok ? s_qmax[g] : 0.f;
-    int eq = qm > 0.f ? 14 - ilog2_floor(qm) : 0;
-    float up = exp2i(eq);
-    head_coef = exp2i(-eq) * (1.4426950408889634f * rsqrtf(float(D)));
-    const uint16_t *qh = p.q + (size_t(b) * p.Hq + hkv * G + (row_ok ? g : 0)) * D;
+  // Every lane copies its share of one step: 16-byte chunks of K and V codes
+  // and one scale row (K or V) of one slot.  One commit group per step
+  // (empty past the end) keeps the group count uniform.
+  auto issue = [&](int n) {
+    if (n < n_steps) {
+      const int base = base_of(n);
+      const uint32_t st = my_stages + (n % kStages) * S::kBytes;
+      constexpr int kChunks = kStep * D / 16;
 #pragma unroll
-    for (int grp = 0; grp < NG; ++grp) {
-      uint4 w = row_ok ? *reinterpret_cast<const uint4 *>(qh + 32 * grp + 8 * t) : make_uint4(0, 0, 0, 0);
-      uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        qa[grp][s][0] = pack_half2(bf16_lo(ws[2 * s]) * up, bf16_hi(ws[2 * s]) * up);
-        qa[grp][s][1] = pack_half2(bf16_lo(ws[2 * s + 1]) * up, bf16_hi(ws[2 * s + 1]) * up);
+      for (int i = lane; i < kChunks; i += 32) {
+        const int row = i / (D / 16), ch = i % (D / 16);
+        const int v = base + row;
+        const int ps = phys(v < v_end ? v : base);
+        const uint32_t off = swz(uint32_t(row * D + ch * 16));
+        cp_async16(st + off, kc + size_t(ps) * D + ch * 16);
+        cp_async16(st + S::kCodes + off, vc + size_t(ps) * D + ch * 16);
+      }
+      {
+        const int row = lane & 15, which = lane >> 4;
+        const int v = base + row;
+        const int ps = phys(v < v_end ? v : base);
+        const uint32_t dst = st + 2 * S::kCodes + which * S::kScales + row * NG * 4;
+        const float *src = (which ? vs : ks) + size_t(ps) * NG;
+        if constexpr (NG == 4) cp_async16(dst, src);
+        else cp_async8(dst, src);
       }
     }
-  }
-  float vup[NG], vdown[NG];
-#pragma unroll
-  for (int grp = 0; grp < NG; ++grp) {
-    float vm = __uint_as_float(s_vmax[grp]);
-    int ev = vm > 0.f ? 14 - ilog2_floor(vm) : 0;
-    vup[grp] = exp2i(ev);
-    vdown[grp] = exp2i(-ev);
-  }
+    cp_async_commit();
+  };
 
-  // ---- main loop: warp w takes k-steps w, w+4, ...
+#pragma unroll
+  for (int n = 0; n < kStages - 1; ++n) issue(n);
+
   float o[NG][2][4];
 #pragma unroll
   for (int grp = 0; grp < NG; ++grp)
@@ -185,67 +234,42 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(cons
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[grp][tt][i] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;
+  int e_acc[NG];  // power-of-two pre-scale of P' per group (never increases; 127 = unset)
+#pragma unroll
+  for (int grp = 0; grp < NG; ++grp) e_acc[grp] = 127;
 
-  for (int base = v_begin + warp * kStep; base < v_end; base += kWarps * kStep) {
-    // slots this thread touches: K rows (tile j, slot g) and the score / V
-    // columns 2t, 2t+1, 8+2t, 9+2t.
-    const int vk0 = base + g, vk1 = base + 8 + g;
-    const int vcol[4] = {base + 2 * t, base + 2 * t + 1, base + 8 + 2 * t, base + 9 + 2 * t};
-    const int pk0 = phys(vk0 < v_end ? vk0 : base), pk1 = phys(vk1 < v_end ? vk1 : base);
-    int pc[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) pc[i] = phys(vcol[i] < v_end ? vcol[i] : base);
-
-    uint2 kw[2][NG];
-#pragma unroll
-    for (int grp = 0; grp < NG; ++grp) {
-      kw[0][grp] = *reinterpret_cast<const uint2 *>(kc + size_t(pk0) * D + 32 * grp + 8 * t);
-      kw[1][grp] = *reinterpret_cast<const uint2 *>(kc + size_t(pk1) * D + 32 * grp + 8 * t);
-    }
-    uint32_t vw[4][NG];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int grp = 0; grp < NG; ++grp)
-        vw[i][grp] = *reinterpret_cast<const uint32_t *>(vc + size_t(pc[i]) * D + 32 * grp + 4 * g);
-    float ksc[4][NG], vsc[4][NG];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if constexpr (NG == 4) {
-        float4 a = *reinterpret_cast<const float4 *>(ks + size_t(pc[i]) * NG);
-        float4 bb = *reinterpret_cast<const float4 *>(vs + size_t(pc[i]) * NG);
-        ksc[i][0] = a.x; ksc[i][1] = a.y; ksc[i][2] = a.z; ksc[i][3] = a.w;
-        vsc[i][0] = bb.x; vsc[i][1] = bb.y; vsc[i][2] = bb.z; vsc[i][3] = bb.w;
-      } else {
-#pragma unroll
-        for (int grp = 0; grp < NG; ++grp) {
-          ksc[i][grp] = ks[size_t(pc[i]) * NG + grp];
-          vsc[i][grp] = vs[size_t(pc[i]) * NG + grp];
-        }
-      }
-    }
+  for (int n = 0; n < n_steps; ++n) {
+    issue(n + kStages - 1);
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int base = base_of(n);
+    const uint32_t st = my_stages + (n % kStages) * S::kBytes;
+    const int col[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
 
     // ---- QK: scores for head g at columns 2t, 2t+1 of tiles 0 and 1
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
+      const int row = 8 * j + g;
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
+        const uint2 kw = lds64(st + swz(uint32_t(row * D + 32 * grp + 8 * t)));
         float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-        const uint32_t w0 = kw[j][grp].x ^ 0x80808080u, w1 = kw[j][grp].y ^ 0x80808080u;
+        const uint32_t w0 = kw.x ^ 0x80808080u, w1 = kw.y ^ 0x80808080u;
         mma_f16_16816(d0, d1, d2, d3, qa[grp][0][0], 0u, qa[grp][0][1], 0u,
                       codes_to_half2(w0, kSelBytes01), codes_to_half2(w0, kSelBytes23));
         mma_f16_16816(d0, d1, d2, d3, qa[grp][1][0], 0u, qa[grp][1][1], 0u,
                       codes_to_half2(w1, kSelBytes01), codes_to_half2(w1, kSelBytes23));
-        sc[2 * j] = fmaf(ksc[2 * j][grp], d0, sc[2 * j]);
-        sc[2 * j + 1] = fmaf(ksc[2 * j + 1][grp], d1, sc[2 * j + 1]);
+        const uint32_t ksc = st + 2 * S::kCodes + (8 * j + 2 * t) * NG * 4 + grp * 4;
+        sc[2 * j] = fmaf(ldsf(ksc), d0, sc[2 * j]);
+        sc[2 * j + 1] = fmaf(ldsf(ksc + NG * 4), d1, sc[2 * j + 1]);
       }
     }
     // ---- online softmax for head g (log2 domain)
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      sc[i] = (vcol[i] < v_end && g < G) ? sc[i] * head_coef : -INFINITY;
+      sc[i] = (base + col[i] < v_end && g < G) ? sc[i] * head_coef : -INFINITY;
       mx = fmaxf(mx, sc[i]);
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -257,28 +281,49 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(cons
     for (int i = 0; i < 4; ++i) pr[i] = (m_new == -INFINITY) ? 0.f : ex2(sc[i] - m_new);
     l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
     m_run = m_new;
-    // rescale O: this thread's O columns are heads 2t and 2t+1
+    // this thread's O columns are heads 2t and 2t+1
     const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
     const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
-#pragma unroll
-    for (int grp = 0; grp < NG; ++grp)
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        o[grp][tt][0] *= a_lo;
-        o[grp][tt][1] *= a_hi;
-        o[grp][tt][2] *= a_lo;
-        o[grp][tt][3] *= a_hi;
-      }
-    // ---- PV: per group, B = P'^T (slot x head), A = V^T (channel x slot)
+    // ---- PV per group: B = P'^T (slot x head), A = V^T (channel x slot)
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
-      const float u = vup[grp];
-      const uint32_t b0 = pack_half2(pr[0] * (vsc[0][grp] * u), pr[1] * (vsc[1][grp] * u));
-      const uint32_t b1 = pack_half2(pr[2] * (vsc[2][grp] * u), pr[3] * (vsc[3][grp] * u));
-      const uint32_t x01 = prmt(vw[0][grp], vw[1][grp], 0x5140u) ^ 0x80808080u;
-      const uint32_t x23 = prmt(vw[0][grp], vw[1][grp], 0x7362u) ^ 0x80808080u;
-      const uint32_t y01 = prmt(vw[2][grp], vw[3][grp], 0x5140u) ^ 0x80808080u;
-      const uint32_t y23 = prmt(vw[2][grp], vw[3][grp], 0x7362u) ^ 0x80808080u;
+      float vsc[4];
+      float vm = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        vsc[i] = ldsf(st + 2 * S::kCodes + S::kScales + col[i] * NG * 4 + grp * 4);
+        vm = fmaxf(vm, base + col[i] < v_end ? vsc[i] : 0.f);
+      }
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
+      // exponent that keeps p * v_scale * 2^e below 2^15 for this step; the
+      // accumulator keeps the smallest exponent seen so far (warp-uniform)
+      const int e_step = vm > 0.f ? 14 - ilog2_floor(vm) : 127;
+      float f_lo = a_lo, f_hi = a_hi;
+      if (e_step < e_acc[grp]) {
+        const float shrink = e_acc[grp] == 127 ? 0.f : exp2i(e_step - e_acc[grp]);
+        f_lo *= shrink;
+        f_hi *= shrink;
+        e_acc[grp] = e_step;
+      }
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        o[grp][tt][0] *= f_lo;
+        o[grp][tt][1] *= f_hi;
+        o[grp][tt][2] *= f_lo;
+        o[grp][tt][3] *= f_hi;
+      }
+      const float u = exp2i(e_acc[grp]);
+      const uint32_t b0 = pack_half2(pr[0] * (vsc[0] * u), pr[1] * (vsc[1] * u));
+      const uint32_t b1 = pack_half2(pr[2] * (vsc[2] * u), pr[3] * (vsc[3] * u));
+      uint32_t vw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        vw[i] = lds32(st + S::kCodes + swz(uint32_t(col[i] * D + 32 * grp + 4 * g)));
+      const uint32_t x01 = prmt(vw[0], vw[1], 0x5140u) ^ 0x80808080u;
+      const uint32_t x23 = prmt(vw[0], vw[1], 0x7362u) ^ 0x80808080u;
+      const uint32_t y01 = prmt(vw[2], vw[3], 0x5140u) ^ 0x80808080u;
+      const uint32_t y23 = prmt(vw[2], vw[3], 0x7362u) ^ 0x80808080u;
       // tile 0: rows g <-> channel 4g, rows g+8 <-> channel 4g+1
       mma_f16_16816(o[grp][0][0], o[grp][0][1], o[grp][0][2], o[grp][0][3],
                     codes_to_half2(x01, kSelBytes01), codes_to_half2(x01, kSelBytes23),
@@ -288,38 +333,47 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 4) decode_kernel(cons
                     codes_to_half2(x23, kSelBytes01), codes_to_half2(x23, kSelBytes23),
                     codes_to_half2(y23, kSelBytes01), codes_to_half2(y23, kSelBytes23), b0, b1);
     }
+    __syncwarp();  // every lane is done with this stage before it is refilled
   }
+  cp_async_wait<0>();
 
-  // ---- merge: quad-sum l, then the four warps through shared memory
+  // ---- merge: quad-sum l, then the warps through shared memory (the stage
+  //      buffers are free once every warp is past its loop)
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  if (t == 0 && g < 8) {
-    s_m[warp][g] = m_run;
-    s_l[warp][g] = l_run;
+  __syncthreads();
+  float *s_o = reinterpret_cast<float *>(smem);  // [NW][8][D]
+  float *s_m = s_o + NW * 8 * D;                 // [NW][8]
+  float *s_l = s_m + NW * 8;                     // [NW][8]
+  if (t == 0) {
+    s_m[warp * 8 + g] = m_run;
+    s_l[warp * 8 + g] = l_run;
   }
 #pragma unroll
-  for (int grp = 0; grp < NG; ++grp)
+  for (int grp = 0; grp < NG; ++grp) {
+    const float down = e_acc[grp] == 127 ? 0.f : exp2i(-e_acc[grp]);
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
       const int ch0 = 32 * grp + 4 * g + 2 * tt;  // row g; row g+8 is ch0 + 1
-      s_o[warp][2 * t][ch0] = o[grp][tt][0] * vdown[grp];
-      s_o[warp][2 * t + 1][ch0] = o[grp][tt][1] * vdown[grp];
-      s_o[warp][2 * t][ch0 + 1] = o[grp][tt][2] * vdown[grp];
-      s_o[warp][2 * t + 1][ch0 + 1] = o[grp][tt][3] * vdown[grp];
+      float *w0 = s_o + (warp * 8 + 2 * t) * D;
+      float *w1 = s_o + (warp * 8 + 2 * t + 1) * D;
+      w0[ch0] = o[grp][tt][0] * down;
+      w1[ch0] = o[grp][tt][1] * down;
+      w0[ch0 + 1] = o[grp][tt][2] * down;
+      w1[ch0 + 1] = o[grp][tt][3] * down;
     }
+  }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
     const int h = idx / D, ch = idx % D;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w * 8 + h]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = ex2(s_m[w][h] - M);
-        L += f * s_l[w][h];
-        O += f * s_o[w][h][ch];
+      for (int w = 0; w < NW; ++w) {
+        const float f = ex2(s_m[w * 8 + h] - M);
+        L += f * s_l[w * 8 + h];
+        O += f * s_o[(w * 8 + h) * D + ch];
       }
     }
     if (p.n_split == 1) {
@@ -364,26 +418,54 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
   if (ch == 0 && p.lse) p.lse[row] = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
+// Warps per CTA: 16 at head_dim 64 (one CTA per SM covers a whole short
+// sequence in one or two steps per warp), 4 at head_dim 128 (three CTAs per SM).
+constexpr int warps_for(int D) { return D == 64 ? 16 : 4; }
+
+template <int D, int NW>
+size_t decode_smem_bytes() {
+  const size_t stages = size_t(NW) * kStages * Stage<D>::kBytes;
+  const size_t merge = size_t(NW) * 8 * D * 4 + 2 * size_t(NW) * 8 * 4;
+  return stages > merge ? stages : merge;
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+  constexpr int NW = warps_for(D);
+  const size_t smem = decode_smem_bytes<D, NW>();
+  auto kern = decode_kernel<D, NW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NW * 32, smem, stream>>>(p);
+  if (p.n_split > 1) decode_combine_kernel<D><<<p.c.batch * p.Hq, D, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots) {
+DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots, int head_dim) {
   DecodePlan pl;
   const long pairs = long(batch) * n_kv_heads;
-  const int ksteps = (max_slots + kStep - 1) / kStep;
-  long want = pairs > 0 ? (kTargetCtas + pairs - 1) / pairs : 1;
-  long cap = (ksteps + kWarps - 1) / kWarps;  // at least one k-step per warp
-  long ns = want < cap ? want : cap;
-  if (ns < 1) ns = 1;
+  const int steps = (max_slots + kStep - 1) / kStep;
+  const int nw = warps_for(head_dim);
+  long ns = 1;
+  // One CTA per (sequence, KV head) while that fills at least half the SMs;
+  // otherwise split the slots so every SM gets work (at least one step per warp).
+  if (pairs * 2 < kTargetCtas) {
+    const long want = (kTargetCtas + pairs - 1) / (pairs > 0 ? pairs : 1);
+    const long cap = (steps + nw - 1) / nw;
+    ns = want < cap ? want : cap;
+    if (ns < 1) ns = 1;
+  }
   pl.n_split = int(ns);
-  pl.slots_per_cta = int((ksteps + ns - 1) / ns) * kStep;
+  pl.slots_per_cta = int((steps + ns - 1) / ns) * kStep;
   if (pl.slots_per_cta == 0) pl.slots_per_cta = kStep;
   pl.max_slots = max_slots;
   return pl;
 }
 
-size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_slots,
-                              int n_kv_heads_hint) {
-  DecodePlan pl = plan_decode(batch, n_kv_heads_hint, max_slots);
+size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_slots, int n_kv_heads) {
+  DecodePlan pl = plan_decode(batch, n_kv_heads, max_slots, head_dim);
   if (pl.n_split <= 1) return 0;
   return size_t(batch) * n_q_heads * pl.n_split * (head_dim + 2) * sizeof(float);
 }
@@ -392,7 +474,7 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
                           void *out, float *lse, void *ws, size_t ws_bytes, int *err,
                           cudaStream_t stream) {
   const int max_slots = c.sink_cap + (c.ring_cap < window ? c.ring_cap : window);
-  DecodePlan pl = plan_decode(c.batch, c.n_kv_heads, max_slots);
+  DecodePlan pl = plan_decode(c.batch, c.n_kv_heads, max_slots, c.head_dim);
   DecodeParams p;
   p.q = static_cast<const uint16_t *>(q);
   p.c = c;
@@ -414,16 +496,9 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
     p.ws_ml = p.ws_o + parts * c.head_dim;
   }
   dim3 grid(pl.n_split, c.n_kv_heads, c.batch);
-  if (c.head_dim == 128) {
-    decode_kernel<128><<<grid, kThreads, 0, stream>>>(p);
-    if (pl.n_split > 1) decode_combine_kernel<128><<<c.batch * n_q_heads, 128, 0, stream>>>(p);
-  } else if (c.head_dim == 64) {
-    decode_kernel<64><<<grid, kThreads, 0, stream>>>(p);
-    if (pl.n_split > 1) decode_combine_kernel<64><<<c.batch * n_q_heads, 64, 0, stream>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (c.head_dim == 128) return launch_d<128>(p, grid, stream);
+  if (c.head_dim == 64) return launch_d<64>(p, grid, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace nd

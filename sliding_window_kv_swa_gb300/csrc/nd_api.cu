@@ -175,7 +175,7 @@ int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, i
   if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
   const int max_slots = cache->sink_cap + (cache->ring_cap < window ? cache->ring_cap : window);
   if (max_slots <= 0) return ND_ERR_INVALID_ARG;
-  DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots);
+  DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim);
   if (pl.n_split > 1) {
     size_t need = size_t(cache->batch) * n_q_heads * pl.n_split * (cache->head_dim + 2) * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ND_ERR_WORKSPACE;

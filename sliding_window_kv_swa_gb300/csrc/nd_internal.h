@@ -25,7 +25,7 @@ struct DecodePlan {
   int slots_per_cta;  // multiple of 16
   int max_slots;      // upper bound of visible slots per sequence
 };
-DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots);
+DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots, int head_dim);
 size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_slots,
                               int n_kv_heads_hint);
 cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, int window,

@@ -223,7 +223,7 @@ def nd_swa_sink_decode(q: torch.Tensor, cache: KVCache, window: int, out: Option
     return out
 
 
-NOALLOC_SCRATCH_BYTES = 2 << 20   # ND_NOALLOC_SCRATCH_BYTES in nd.h
+NOALLOC_SCRATCH_BYTES = 512 << 10   # ND_NOALLOC_SCRATCH_BYTES in nd.h
 
 
 def nd_swa_sink_decode_noalloc(q: torch.Tensor, cache: KVCache, window: int, out: torch.Tensor,

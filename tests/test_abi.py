@@ -104,9 +104,11 @@ def test_host_validation_before_any_device_work():
 
 def test_workspace_sizes():
     import sliding_window_kv_swa_gb300 as nd
-    # decode B64 Hq8 Hkv2 d64, 320 slots: five splits, (64+2) floats per partial
-    assert nd.nd_swa_sink_decode_workspace_size(64, 8, 2, 64, 320) == 64 * 8 * 5 * 66 * 4
-    assert nd.nd_swa_sink_decode_workspace_size(512, 32, 8, 128, 1280) == 0   # no split
+    # one CTA per (sequence, KV head) once that fills half the GPU: no split
+    assert nd.nd_swa_sink_decode_workspace_size(64, 8, 2, 64, 320) == 0
+    assert nd.nd_swa_sink_decode_workspace_size(512, 32, 8, 128, 1280) == 0
+    # 8 sequences x 2 KV heads: two-way split, (64+2) floats per partial
+    assert nd.nd_swa_sink_decode_workspace_size(8, 8, 2, 64, 320) == 8 * 8 * 2 * 66 * 4
     # prefill with rotation keeps rotated copies of q and k
     n = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, 1, 512, 4, 1, 64, 10000.0, 0)
     assert n >= 512 * 4 * 64 * 4 + 512 * 1 * 64 * 4

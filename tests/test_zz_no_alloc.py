@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from gpu_util import assert_close_bf16, dev, dev_bf16, host, need_gpu
-from workloads import decode_b64, normal_bf16, philox
+from workloads import decode_cache, normal_bf16, philox
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,9 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
     need_gpu()
     import sliding_window_kv_swa_gb300 as nd
     S, W = 64, 256
-    w = decode_b64()                               # B64 Hq8 Hkv2 d64: the decode splits
+    # 8 sequences x 2 KV heads are too few to fill the GPU, so the decode
+    # splits each sequence's slots and needs scratch for the partials
+    w = decode_cache(8, 8, 2, 64, S, W, seed=2023, full=True)
     B, Hq, d = w["q"].shape
     cache = _device_cache(nd, w, S, W)
     need = nd.nd_swa_sink_decode_workspace_size(B, Hq, cache.n_kv_heads, d, S + W)
@@ -59,7 +61,7 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
 def test_noalloc_refuses_shapes_beyond_its_scratch():
     need_gpu()
     import sliding_window_kv_swa_gb300 as nd
-    B, Hq, Hkv, d, S, W = 8, 64, 8, 128, 1024, 256
+    B, Hq, Hkv, d, S, W = 2, 64, 8, 128, 1024, 256   # ten-way split of 1280 slots
     need = nd.nd_swa_sink_decode_workspace_size(B, Hq, Hkv, d, S + W)
     assert need > nd.nd.NOALLOC_SCRATCH_BYTES
     cache = nd.KVCache.empty(B, Hkv, d, S, W)
