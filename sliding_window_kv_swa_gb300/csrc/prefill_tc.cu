@@ -6,22 +6,28 @@
 // "Two kinds of columns" (pooled block j visible iff (j+1)*block <= q-W+1,
 // then the exact sliding window).
 //
-// Work split.  A small plan pass lists, for every (sequence, 128-row query
-// tile), the 64-key tiles that can hold a visible key (segment-id ranges,
-// causal bound, window bound, sink presence; pooled tiles below the threshold),
-// so the cost follows window + sink rather than T^2.  One CTA (4 warps) then
-// runs one (sequence, query tile, query head):
-//   TMA   : Q tile [128 x d] once; K and V tiles [64 x d] double-buffered,
-//           128-byte swizzled, issued by one thread on mbarriers.
-//   MMA   : S = Q K^T (M=128, N=64) into TMEM; O_tile = P V (M=128, N=d) into
-//           TMEM, P read from shared memory (K-major), V as an MN-major
-//           operand straight from its TMA tile.  One thread issues, commits
-//           to an mbarrier.
-//   softmax: thread i owns query row i = TMEM lane i: loads its S row,
-//           applies the exact mask, online softmax in the log2 domain,
-//           writes bf16 P, and accumulates O = O*alpha + O_tile in registers.
-// Every mbarrier wait is bounded; on timeout the CTA raises the device error
-// flag, stops issuing work and frees its TMEM.
+// Work split.  A plan pass lists, for every (sequence, row span), the 64-key
+// tiles that can hold a visible key (segment-id ranges, causal bound, window
+// bound, sink presence; pooled tiles below the threshold), so the cost follows
+// window + sink rather than T^2.
+//
+// One CTA runs two 128-row blocks that share their K/V tiles: two query heads
+// of one GQA group (same rows), or, when the group size is odd, two
+// consecutive row blocks of one head.  Its ten warps specialise:
+//   warps 0-3, 4-7 : one softmax warpgroup per row block; thread i owns row i
+//                    (= TMEM lane i): exact mask, online softmax in the log2
+//                    domain, bf16 P into a 128-byte-swizzled shared tile.
+//   warp 8         : TMA loader -- Q once, then K/V tiles (double-buffered) and
+//                    the tiles' segment / sink metadata.
+//   warp 9         : MMA issuer -- S = Q K^T (M128 N64) and O += P V (M128, N=d,
+//                    V as an MN-major operand) for both blocks, interleaved so
+//                    the tensor core computes S(j+1) while the softmax warps
+//                    work on tile j.
+// O accumulates in TMEM; a row's O is rescaled (TMEM load / multiply / store)
+// only when its running max grows by more than 2^8, so most tiles touch O
+// only through the MMA.  P is double-buffered per block.  Every mbarrier wait
+// is bounded; a wait that gives up raises the device error flag and a shared
+// abort flag, and all roles then run to the common exit, which frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -34,16 +40,19 @@ namespace nd {
 
 namespace {
 
-constexpr int BM = 128;  // query rows per CTA = TMEM lanes
+constexpr int BM = 128;  // rows per block = TMEM lanes
 constexpr int BN = 64;   // keys per tile
-constexpr int kThreads = 128;
+constexpr int NS = 3;    // K/V stages
+constexpr int kWarpLoad = 8, kWarpMma = 9;
+constexpr int kThreads = 10 * 32;
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 
 struct TileSummary {
   int seg_lo, seg_hi, any_sink;
 };
 
 struct TcParams {
-  int B, T, Hq, Hkv, G, W, block, nb, n_qt, n_kt, n_pt, plan_stride;
+  int B, T, Hq, Hkv, G, W, block, nb, n_span, span, n_kt, plan_stride, pair_heads;
   const int32_t *seg;
   const uint8_t *sink;
   const int32_t *plan;
@@ -71,23 +80,23 @@ __global__ void tile_summary_kernel(const int32_t *seg, const uint8_t *sink, int
   sum[i] = {lo, hi, any};
 }
 
-__global__ void tile_plan_kernel(const int32_t *seg, const TileSummary *sum, TcParams p,
-                                 int32_t *plan) {
+// One thread per (sequence, row span): the key tiles any row of the span may
+// see, pooled tiles first (entry bit 20 set), then exact tiles, ascending.
+__global__ void tile_plan_kernel(const TileSummary *sum, TcParams p, int32_t *plan) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= p.B * p.n_qt) return;
-  const int b = i / p.n_qt, qt = i % p.n_qt;
-  const int q0 = qt * BM, q1 = min(p.T, q0 + BM) - 1;
+  if (i >= p.B * p.n_span) return;
+  const int b = i / p.n_span, sp = i % p.n_span;
+  const int q0 = sp * p.span, q1 = min(p.T, q0 + p.span) - 1;
   int32_t *out = plan + size_t(i) * p.plan_stride;
   int n = 0;
   if (p.block > 0) {
-    // pooled columns j < nb visible from some row iff (j+1)*block <= q1 - W + 1
-    const int lim = q1 - p.W + 1;
+    const int lim = q1 - p.W + 1;  // pooled column j visible iff (j+1)*block <= q - W + 1
     const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
     for (int j = 0; j * BN < ncol; ++j) out[1 + n++] = (1 << 20) | j;
   }
   int qlo = INT_MAX, qhi = INT_MIN;
   for (int q = q0; q <= q1; ++q) {
-    const int s = seg ? seg[size_t(b) * p.T + q] : 1;
+    const int s = p.seg ? p.seg[size_t(b) * p.T + q] : 1;
     if (s > 0) {
       qlo = min(qlo, s);
       qhi = max(qhi, s);
@@ -154,8 +163,7 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
-  uint32_t r[32];
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
       "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -165,9 +173,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
         "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -181,57 +203,88 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Bounded wait that also gives up at once when another role already did.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
+                                              volatile int *abort_flag) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  raise_device_error(err, ND_DEVERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int D>
-struct Smem {
-  static constexpr int kBoxes = D / 64;                // 64-column swizzle atoms per row
-  static constexpr int kQ = kBoxes * BM * 128;         // Q tile bytes
-  static constexpr int kKV = kBoxes * BN * 128;        // one K (or V) tile
-  static constexpr int kP = BM * BN * 2;               // P tile (one atom column)
-  static constexpr bool kAliasP = (kKV == kP);         // P reuses the consumed K stage
-  static constexpr int kBytes = kQ + 4 * kKV + (kAliasP ? 0 : kP) + 1024;  // + alignment slack
-  static constexpr int kTmemCols = (BN + D) <= 128 ? 128 : 256;
+struct Lay {
+  static constexpr int kBoxes = D / 64;            // 64-column swizzle atoms per row
+  static constexpr int kQ = kBoxes * BM * 128;     // one block's Q tile
+  static constexpr int kKV = kBoxes * BN * 128;    // one K (or V) tile
+  static constexpr int kP = BM * BN * 2;           // one P tile
+  static constexpr int oQ = 0;                     // Q[2 blocks]
+  static constexpr int oKV = 2 * kQ;               // {K, V}[NS stages]
+  static constexpr int oP = oKV + NS * 2 * kKV;    // P[2 blocks]
+  static constexpr int kBytes = oP + 2 * kP + 1024;  // + alignment slack
+  // TMEM columns: S[block][2 buffers] (BN each), then O[block] (D each)
+  static constexpr int kCols = 4 * BN + 2 * D;
+  static constexpr int kTmemCols = kCols <= 256 ? 256 : 512;
+};
+
+// Per-stage key-tile facts the loader publishes with the metadata.
+struct TileFlags {
+  int seg_lo, seg_hi, all_sink;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_pk,
                       const __grid_constant__ CUtensorMap tm_pv, const TcParams p) {
-  using L = Smem<D>;
+  using L = Lay<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_kv[2], bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_q, kv_full[NS], kv_empty[NS], s_full[2][2], p_full[2],
+      pv_done[2];
   __shared__ uint32_t s_tmem;
-  bool fail = false, aborted = false;  // this thread saw a wait time out; the CTA did
-  __shared__ int s_seg[2][BN];
-  __shared__ unsigned char s_sink[2][BN];
+  __shared__ int s_abort;
+  __shared__ int s_seg[NS][BN];
+  __shared__ unsigned char s_sink[NS][BN];
+  __shared__ TileFlags s_flags[NS];
 
-  const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int hk = hq / p.G;
-  const int q0 = qt * BM;
-  const int q = q0 + tid;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z;
+  const int head0 = p.pair_heads ? 2 * blockIdx.y : blockIdx.y;
+  const int head1 = p.pair_heads ? head0 + 1 : head0;
+  const int row00 = p.pair_heads ? blockIdx.x * BM : blockIdx.x * 2 * BM;
+  const int row01 = p.pair_heads ? row00 : row00 + BM;
+  const int hk = head0 / p.G;
+  const int32_t *plan = p.plan + (size_t(b) * p.n_span + blockIdx.x) * p.plan_stride;
+  const int n = plan[0];
+  volatile int *abort_flag = &s_abort;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = base;
-  const uint32_t sK[2] = {base + L::kQ, base + L::kQ + L::kKV};
-  const uint32_t sV[2] = {base + L::kQ + 2 * L::kKV, base + L::kQ + 3 * L::kKV};
-  const uint32_t sPsep = base + L::kQ + 4 * L::kKV;
-
-  const int32_t *plan = p.plan + (size_t(b) * p.n_qt + qt) * p.plan_stride;
-  const int n_tiles = plan[0];
+  auto sQ = [&](int rb) { return base + L::oQ + rb * L::kQ; };
+  auto sK = [&](int st) { return base + L::oKV + st * 2 * L::kKV; };
+  auto sV = [&](int st) { return base + L::oKV + st * 2 * L::kKV + L::kKV; };
+  auto sP = [&](int rb) { return base + L::oP + rb * L::kP; };
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
-    mbar_init(&bar_kv[0], 1);
-    mbar_init(&bar_kv[1], 1);
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_o, 1);
-
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&kv_full[s], 2);  // expect_tx arrival + metadata arrival
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&s_full[r][0], 1);
+      mbar_init(&s_full[r][1], 1);
+      mbar_init(&p_full[r], BM);
+      mbar_init(&pv_done[r], 1);
+    }
+    s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&s_tmem)),
                  "r"(L::kTmemCols)
@@ -242,182 +295,258 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t tS = tmem, tO = tmem + BN;
-  const uint32_t lane_base = uint32_t(warp * 32) << 16;
+  auto tS = [&](int rb, int buf) { return tmem + (rb * 2 + buf) * BN; };
+  auto tO = [&](int rb) { return tmem + 4 * BN + rb * D; };
+  bool fail = false;
 
-  auto issue_kv = [&](int it) {
-    const int e = plan[1 + it];
-    const bool pooled = (e >> 20) & 1;
-    const int j = e & 0xFFFFF;
-    const int st = it & 1;
-    mbar_arrive_expect_tx(&bar_kv[st], 2 * L::kKV);
-    const CUtensorMap *mk = pooled ? &tm_pk : &tm_k;
-    const CUtensorMap *mv = pooled ? &tm_pv : &tm_v;
-#pragma unroll
-    for (int x = 0; x < L::kBoxes; ++x) {
-      tma_load_4d(sK[st] + x * BN * 128, mk, 64 * x, hk, j * BN, b, &bar_kv[st]);
-      tma_load_4d(sV[st] + x * BN * 128, mv, 64 * x, hk, j * BN, b, &bar_kv[st]);
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------ TMA loader
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(&bar_q, 2 * L::kQ);
+      for (int x = 0; x < L::kBoxes; ++x) {
+        tma_load_4d(sQ(0) + x * BM * 128, &tm_q, 64 * x, head0, row00, b, &bar_q);
+        tma_load_4d(sQ(1) + x * BM * 128, &tm_q, 64 * x, head1, row01, b, &bar_q);
+      }
     }
-  };
-  auto load_meta = [&](int it) {  // key metadata of tile `it` into buffer it & 1
-    if (it >= n_tiles || tid >= BN) return;
-    const int e = plan[1 + it];
-    const int k = (e & 0xFFFFF) * BN + tid;
-    if ((e >> 20) & 1) {
-      s_seg[it & 1][tid] = k;  // pooled: column index
-      s_sink[it & 1][tid] = 0;
-    } else {
-      s_seg[it & 1][tid] = k < p.T ? (p.seg ? p.seg[size_t(b) * p.T + k] : 1) : 0;
-      s_sink[it & 1][tid] = (k < p.T && p.sink) ? p.sink[size_t(b) * p.T + k] : 0;
+    for (int j = 0; j < n; ++j) {
+      const int st = j % NS;
+      if (j >= NS && !wait_or_abort(&kv_empty[st], ((j / NS) - 1) & 1, p.err, abort_flag)) fail = true;
+      fail = __any_sync(0xffffffffu, fail);  // the warp leaves the loop together
+      if (fail) break;
+      const int e = plan[1 + j];
+      const bool pooled = (e >> 20) & 1;
+      const int jt = e & 0xFFFFF;
+      int lo = INT_MAX, hi = INT_MIN, all_sink = 1;
+      for (int kk = lane; kk < BN; kk += 32) {
+        const int k = jt * BN + kk;
+        int sg = k, sk = 0;
+        if (!pooled) {
+          sg = k < p.T ? (p.seg ? p.seg[size_t(b) * p.T + k] : 1) : 0;
+          sk = (k < p.T && p.sink) ? p.sink[size_t(b) * p.T + k] : 0;
+          lo = min(lo, sg);
+          hi = max(hi, sg);
+          all_sink &= sk != 0;
+        }
+        s_seg[st][kk] = sg;  // pooled tile: the column index
+        s_sink[st][kk] = (unsigned char)sk;
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+        all_sink &= __shfl_xor_sync(0xffffffffu, all_sink, off);
+      }
+      if (lane == 0) s_flags[st] = {lo, hi, all_sink};
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kKV);
+        const CUtensorMap *mk = pooled ? &tm_pk : &tm_k;
+        const CUtensorMap *mv = pooled ? &tm_pv : &tm_v;
+        for (int x = 0; x < L::kBoxes; ++x) {
+          tma_load_4d(sK(st) + x * BN * 128, mk, 64 * x, hk, jt * BN, b, &kv_full[st]);
+          tma_load_4d(sV(st) + x * BN * 128, mv, 64 * x, hk, jt * BN, b, &kv_full[st]);
+        }
+        mbar_arrive(&kv_full[st]);  // metadata written by the whole warp (ordered by __syncwarp)
+      }
     }
-  };
-
-  if (tid == 0 && n_tiles > 0) {
-    mbar_arrive_expect_tx(&bar_q, L::kQ);
-#pragma unroll
-    for (int x = 0; x < L::kBoxes; ++x) tma_load_4d(sQ + x * BM * 128, &tm_q, 64 * x, hq, q0, b, &bar_q);
-    issue_kv(0);
-  }
-  load_meta(0);
-
-  const int myseg = q < p.T ? (p.seg ? p.seg[size_t(b) * p.T + q] : 1) : 0;
-  const int W = p.W == 0 ? INT_MAX : p.W;
-  const float c = 1.4426950408889634f * rsqrtf(float(D));  // log2(e) / sqrt(d), applied to scores
-  float o[D];
-#pragma unroll
-  for (int i = 0; i < D; ++i) o[i] = 0.f;
-  float m = -INFINITY, l = 0.f;
-  __syncthreads();
-
-  constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
-  constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
-
-  for (int it = 0; it < n_tiles; ++it) {
-    const int st = it & 1;
-    const int e = plan[1 + it];
-    const bool pooled = (e >> 20) & 1;
-    const int j = e & 0xFFFFF;
-    // ---- issue S = Q K^T
-    if (tid == 0 && !fail) {
-      if (it + 1 < n_tiles) issue_kv(it + 1);  // stage st^1 is free: tile it-1 finished
-      bool ok = true;
-      if (it == 0) ok = mbar_wait(&bar_q, 0, p.err);
-      ok = ok && mbar_wait(&bar_kv[st], (it >> 1) & 1, p.err);
-      if (!ok) {
-        fail = true;
-      } else {
-        tc_fence_after();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------ MMA issuer
+    //   S(0), S(1) for both blocks, then per tile j: O += P V for both blocks
+    //   (each waits for its block's P), then S(j+2) into the S buffer tile j
+    //   just freed, once tile j+2's K/V have landed.
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
+      constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
+      auto issue_s = [&](int rb, int j) {
+        const int st = j % NS;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes inside the atom
-          const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * BM * 128 + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK[st] + (kk >> 2) * BN * 128 + off, 16, 1024);
-          mma_bf16(tS, a, bd, kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t a = sdesc_sw128(sQ(rb) + (kk >> 2) * BM * 128 + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
+          mma_bf16(tS(rb, j & 1), a, bd, kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_s);
+        mma_commit(&s_full[rb][j & 1]);
+      };
+      bool ok = wait_or_abort(&bar_q, 0, p.err, abort_flag);
+      for (int j = 0; j < 2 && j < n && ok; ++j) {
+        ok = wait_or_abort(&kv_full[j % NS], (j / NS) & 1, p.err, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, j);
+          issue_s(1, j);
+        }
       }
-    }
-    // ---- softmax on row `tid`
-    if (!mbar_wait(&bar_s, it & 1, p.err)) fail = true;
-    __syncwarp();
-    tc_fence_after();
-    float s[BN];
-    tmem_ld32(tS + lane_base, s);
-    tmem_ld32(tS + lane_base + 32, s + 32);
-    const int *ks = s_seg[st];
-    const unsigned char *kn = s_sink[st];
-    float mx = -INFINITY;
+      for (int j = 0; j < n && ok; ++j) {
+        const int st = j % NS;
+        for (int rb = 0; rb < 2 && ok; ++rb) {
+          ok = wait_or_abort(&p_full[rb], j & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-    for (int x = 0; x < BN; ++x) {
-      bool vis;
-      if (pooled) {
-        const int jp = ks[x];
-        vis = myseg > 0 && jp < p.nb && (jp + 1) * p.block <= q - p.W + 1;
-      } else {
-        const int k = j * BN + x;
-        vis = myseg > 0 && k <= q && ks[x] == myseg && (q - k < W || kn[x]);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(sP(rb) + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
+            mma_bf16(tO(rb), a, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&pv_done[rb]);
+        }
+        if (!ok) break;
+        mma_commit(&kv_empty[st]);
+        if (j + 2 < n) {
+          ok = wait_or_abort(&kv_full[(j + 2) % NS], ((j + 2) / NS) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, j + 2);
+          issue_s(1, j + 2);
+        }
       }
-      s[x] = vis ? s[x] : -INFINITY;
-      mx = fmaxf(mx, s[x]);
+      fail = !ok;
     }
-    const float m_new = fmaxf(m, mx);
-    const float alpha = (m_new == -INFINITY) ? 1.f : ex2((m - m_new) * c);
-    const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
-    float rs = 0.f;
-    // P row -> shared memory, K-major 128B-swizzled (16-byte chunk ch of row r
-    // lands at chunk ch ^ (r & 7)), 8 probabilities per chunk
-    const uint32_t sP = L::kAliasP ? sK[st] : sPsep;
-#pragma unroll
-    for (int ch = 0; ch < BN / 8; ++ch) {
-      uint32_t w[4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float p0 = ex2(fmaf(s[8 * ch + 2 * x], c, -mc));
-        const float p1 = ex2(fmaf(s[8 * ch + 2 * x + 1], c, -mc));
-        rs += p0 + p1;
-        w[x] = pack_bf16x2(p0, p1);
-      }
-      st_shared_v4(sP + tid * 128 + ((ch ^ (tid & 7)) << 4), w[0], w[1], w[2], w[3]);
-    }
-    l = l * alpha + rs;
-    m = m_new;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- issue O_tile = P V
-    if (tid == 0 && !fail) {
+  } else {
+    // ------------------------------------------------ softmax warpgroups
+    const int rb = warp >> 2;
+    const int r = tid & (BM - 1);
+    const int q = (rb ? row01 : row00) + r;
+    const int head = rb ? head1 : head0;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const int myseg = q < p.T ? (p.seg ? p.seg[size_t(b) * p.T + q] : 1) : 0;
+    const int W = p.W == 0 ? INT_MAX : p.W;
+    const float c = 1.4426950408889634f * rsqrtf(float(D));  // log2(e) / sqrt(d)
+    float m_used = -INFINITY, l = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int st = j % NS;
+      const int e = plan[1 + j];
+      const bool pooled = (e >> 20) & 1;
+      const int k0 = (e & 0xFFFFF) * BN;
+      if (!fail && !(wait_or_abort(&s_full[rb][j & 1], (j >> 1) & 1, p.err, abort_flag) &&
+                     wait_or_abort(&kv_full[st], (j / NS) & 1, p.err, abort_flag)))
+        fail = true;
+      __syncwarp();
       tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t a = sdesc_sw128(sP + kk * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(sV[st] + kk * 16 * 128, BN * 128, 1024);
-        mma_bf16(tO, a, bd, kIdPV, kk > 0 ? 1u : 0u);
+      uint32_t sr[BN];
+      tmem_ld32(tS(rb, j & 1) + lane_base, sr);
+      tmem_ld32(tS(rb, j & 1) + lane_base + 32, sr + 32);
+      tmem_ld_wait();
+      // every key of the tile visible for this row?  (warp-uniform fast path)
+      bool full;
+      if (pooled) {
+        full = myseg > 0 && k0 + BN - 1 < p.nb && (k0 + BN) * p.block <= q - p.W + 1;
+      } else {
+        const TileFlags f = s_flags[st];
+        full = myseg > 0 && f.seg_lo == myseg && f.seg_hi == myseg && k0 + BN - 1 <= q &&
+               (q - k0 < W || f.all_sink);
       }
-      mma_commit(&bar_o);
+      float s[BN];
+      if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+        for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
+      } else if (pooled) {
+#pragma unroll
+        for (int x = 0; x < BN; ++x) {
+          const int jp = k0 + x;
+          const bool vis = myseg > 0 && jp < p.nb && (jp + 1) * p.block <= q - p.W + 1;
+          s[x] = vis ? __uint_as_float(sr[x]) : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int x = 0; x < BN; ++x) {
+          const int k = k0 + x;
+          const bool vis = myseg > 0 && k <= q && s_seg[st][x] == myseg && (q - k < W || s_sink[st][x]);
+          s[x] = vis ? __uint_as_float(sr[x]) : -INFINITY;
+        }
+      }
+      float mxp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mxp[i] = s[i];
+#pragma unroll
+      for (int x = 8; x < BN; ++x) mxp[x & 7] = fmaxf(mxp[x & 7], s[x]);
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      if (m_used == -INFINITY) m_used = mx;  // nothing accumulated yet: no rescale
+      const bool need = mx > m_used && (mx - m_used) * c > kRescaleLog2;
+      const float alpha = need ? ex2((m_used - mx) * c) : 1.f;
+      if (need) {
+        l *= alpha;
+        m_used = mx;
+      }
+      const float mc = m_used == -INFINITY ? 0.f : m_used * c;
+      uint32_t pk[BN / 2];
+      float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int x = 0; x < BN; x += 2) {
+        const float p0 = ex2(fmaf(s[x], c, -mc));
+        const float p1 = ex2(fmaf(s[x + 1], c, -mc));
+        rsp[(x >> 1) & 3] += p0 + p1;
+        pk[x >> 1] = pack_bf16x2(p0, p1);
+      }
+      l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
+      // PV(j-1) must have landed before O is rescaled or P is overwritten
+      if (j >= 1 && !fail && !wait_or_abort(&pv_done[rb], (j - 1) & 1, p.err, abort_flag)) fail = true;
+      __syncwarp();
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, need) && j >= 1) {
+#pragma unroll 1
+        for (int x = 0; x < D; x += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO(rb) + lane_base + x, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tO(rb) + lane_base + x, ov);
+        }
+        tmem_st_wait();
+      }
+      const uint32_t prow = sP(rb) + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < BN / 8; ++ch)
+        st_shared_v4(prow + ((ch ^ (r & 7)) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                     pk[4 * ch + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[rb]);
     }
-    load_meta(it + 1);
-    if (!mbar_wait(&bar_o, it & 1, p.err)) fail = true;
+    // ---- epilogue: O / l from TMEM
+    if (n > 0 && !fail && !wait_or_abort(&pv_done[rb], (n - 1) & 1, p.err, abort_flag)) fail = true;
     __syncwarp();
     tc_fence_after();
-#pragma unroll
+    const bool store = q < p.T;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint16_t *dst = p.out + ((size_t(b) * p.T + (store ? q : 0)) * p.Hq + head) * D;
+#pragma unroll 1
     for (int x = 0; x < D; x += 32) {
-      float ot[32];
-      tmem_ld32(tO + lane_base + x, ot);
+      uint32_t ov[32];
+      if (n > 0) {
+        tmem_ld32(tO(rb) + lane_base + x, ov);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[x + i] = fmaf(o[x + i], alpha, ot[i]);
+        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+      }
+      if (store && !fail && !*abort_flag) {
+#pragma unroll
+        for (int y = 0; y < 32; y += 8) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(ov[y]) * inv, __uint_as_float(ov[y + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(ov[y + 2]) * inv, __uint_as_float(ov[y + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(ov[y + 4]) * inv, __uint_as_float(ov[y + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(ov[y + 6]) * inv, __uint_as_float(ov[y + 7]) * inv);
+          *reinterpret_cast<uint4 *>(dst + x + y) = v;
+        }
+      }
     }
-    tc_fence_before();
-    if (__syncthreads_or(fail)) {
-      aborted = true;
-      break;
-    }
+    if (store && p.lse && !fail)
+      p.lse[(size_t(b) * p.Hq + head) * p.T + q] =
+          l > 0.f ? (m_used * c + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
 
-  // ---- error path: give copies and MMAs that may still be in flight a
-  //      bounded time (about 2 ms) to land before the CTA releases its shared
-  //      memory and TMEM
-  if (aborted)
-    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
-  // ---- epilogue
-  if (q < p.T && !aborted) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint16_t *dst = p.out + ((size_t(b) * p.T + q) * p.Hq + hq) * D;
-#pragma unroll
-    for (int x = 0; x < D; x += 8) {
-      uint4 v;
-      v.x = pack_bf16x2(o[x] * inv, o[x + 1] * inv);
-      v.y = pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv);
-      v.z = pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv);
-      v.w = pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv);
-      *reinterpret_cast<uint4 *>(dst + x) = v;
-    }
-    if (p.lse)
-      p.lse[(size_t(b) * p.Hq + hq) * p.T + q] =
-          l > 0.f ? (m * c + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-  }
+  // ---- common exit: on the error path give copies and MMAs still in flight a
+  //      bounded time (about 2 ms) to land before shared memory and TMEM go
   tc_fence_before();
+  if (__syncthreads_or(fail || *abort_flag))
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(L::kTmemCols)
@@ -454,25 +583,31 @@ bool make_map(CUtensorMap *map, const void *ptr, int B, int rows, int H, int D, 
 }
 
 struct PlanDims {
-  int n_qt, n_kt, n_pt, stride;
+  int span, n_span, n_kt, n_pt, stride;
   size_t sum_bytes, plan_bytes;
 };
 
-PlanDims plan_dims(int B, int T, int block) {
+// span = rows one CTA covers: 128 (two heads of a GQA pair) or 256 (two
+// consecutive row blocks of one head).  The workspace is sized for the larger
+// of the two so the query does not depend on the head layout.
+PlanDims plan_dims(int B, int T, int block, int span) {
   PlanDims d;
-  d.n_qt = (T + BM - 1) / BM;
+  d.span = span;
+  d.n_span = (T + span - 1) / span;
   d.n_kt = (T + BN - 1) / BN;
   const int nb = block > 0 ? T / block : 0;
   d.n_pt = (nb + BN - 1) / BN;
   d.stride = 1 + d.n_kt + d.n_pt;
   d.sum_bytes = (size_t(B) * d.n_kt * sizeof(TileSummary) + 255) / 256 * 256;
-  d.plan_bytes = size_t(B) * d.n_qt * d.stride * sizeof(int32_t);
+  d.plan_bytes = size_t(B) * ((T + BM - 1) / BM) * d.stride * sizeof(int32_t);
   return d;
 }
 
 template <int D>
 cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t stream) {
-  PlanDims pd = plan_dims(a.batch, a.T, a.block);
+  const int G = a.Hq / a.Hkv;
+  const bool pair_heads = G % 2 == 0;
+  PlanDims pd = plan_dims(a.batch, a.T, a.block, pair_heads ? BM : 2 * BM);
   TileSummary *sum = static_cast<TileSummary *>(ws);
   int32_t *plan = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pd.sum_bytes);
   TcParams p;
@@ -480,14 +615,15 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.T = a.T;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.G = a.Hq / a.Hkv;
+  p.G = G;
   p.W = a.window;
   p.block = a.block;
   p.nb = a.block > 0 ? a.T / a.block : 0;
-  p.n_qt = pd.n_qt;
+  p.n_span = pd.n_span;
+  p.span = pd.span;
   p.n_kt = pd.n_kt;
-  p.n_pt = pd.n_pt;
   p.plan_stride = pd.stride;
+  p.pair_heads = pair_heads ? 1 : 0;
   p.seg = a.seg_ids;
   p.sink = a.sink;
   p.plan = plan;
@@ -509,20 +645,20 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   }
   const int ns = a.batch * pd.n_kt;
   tile_summary_kernel<<<(ns + 127) / 128, 128, 0, stream>>>(a.seg_ids, a.sink, a.T, pd.n_kt, sum, a.batch);
-  const int nq = a.batch * pd.n_qt;
-  tile_plan_kernel<<<(nq + 127) / 128, 128, 0, stream>>>(a.seg_ids, sum, p, plan);
+  const int nq = a.batch * pd.n_span;
+  tile_plan_kernel<<<(nq + 127) / 128, 128, 0, stream>>>(sum, p, plan);
   auto kern = prefill_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(pd.n_qt, a.Hq, a.batch);
-  kern<<<grid, kThreads, Smem<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, p);
+  dim3 grid(pd.n_span, pair_heads ? a.Hq / 2 : a.Hq, a.batch);
+  kern<<<grid, kThreads, Lay<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t prefill_plan_bytes(int batch, int T, int block) {
-  PlanDims pd = plan_dims(batch, T, block);
+  PlanDims pd = plan_dims(batch, T, block, BM);  // the 128-row span has the most plan rows
   return pd.sum_bytes + pd.plan_bytes;
 }
 
