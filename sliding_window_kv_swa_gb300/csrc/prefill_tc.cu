@@ -17,15 +17,16 @@
 //   warps 0-3, 4-7 : one softmax warpgroup per row block; thread i owns row i
 //                    (= TMEM lane i): exact mask, online softmax in the log2
 //                    domain, bf16 P into a 128-byte-swizzled shared tile.
-//   warp 8         : TMA loader -- Q once, then K/V tiles (double-buffered) and
-//                    the tiles' segment / sink metadata.
-//   warp 9         : MMA issuer -- S = Q K^T (M128 N64) and O += P V (M128, N=d,
-//                    V as an MN-major operand) for both blocks, interleaved so
-//                    the tensor core computes S(j+1) while the softmax warps
-//                    work on tile j.
+//   warp 8         : TMA loader -- Q once, then K/V tiles over three stages,
+//                    with each tile's segment / sink record (cp.async).
+//   warp 9         : MMA issuer -- S = Q K^T (M128 N64, double-buffered in
+//                    TMEM, issued two tiles ahead) and O += P V (M128, N=d, V as
+//                    an MN-major operand) for both blocks, so the tensor core
+//                    works ahead while the softmax warps handle a tile.
 // O accumulates in TMEM; a row's O is rescaled (TMEM load / multiply / store)
 // only when its running max grows by more than 2^8, so most tiles touch O
-// only through the MMA.  P is double-buffered per block.  Every mbarrier wait
+// only through the MMA.  Tiles every row of a warp fully sees skip the
+// per-element mask.  Every mbarrier wait
 // is bounded; a wait that gives up raises the device error flag and a shared
 // abort flag, and all roles then run to the common exit, which frees TMEM.
 #include <cuda.h>
@@ -47,15 +48,24 @@ constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kThreads = 10 * 32;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 
-struct TileSummary {
-  int seg_lo, seg_hi, any_sink;
+// Per (sequence, 64-key tile) metadata record, written once per call by
+// tile_meta_kernel and copied asynchronously into shared memory by the loader
+// next to the tile's K/V: segment ids, sink flags and summary flags.
+struct alignas(128) TileMeta {
+  int seg[BN];                 // 0 for keys past T
+  unsigned char sink[BN];
+  int seg_lo, seg_hi;          // over keys with a positive id (lo > hi: none)
+  int all_sink, any_sink;
+  int pad[12];
 };
+static_assert(sizeof(TileMeta) == 384, "16-byte chunks for cp.async");
 
 struct TcParams {
   int B, T, Hq, Hkv, G, W, block, nb, n_span, span, n_kt, plan_stride, pair_heads;
   const int32_t *seg;
   const uint8_t *sink;
   const int32_t *plan;
+  const TileMeta *meta;  // [B][n_kt]
   uint16_t *out;
   float *lse;
   int *err;
@@ -63,26 +73,45 @@ struct TcParams {
 
 // ------------------------------------------------------------------ plan
 
-__global__ void tile_summary_kernel(const int32_t *seg, const uint8_t *sink, int T, int n_kt,
-                                    TileSummary *sum, int B) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= B * n_kt) return;
-  const int b = i / n_kt, j = i % n_kt;
-  int lo = INT_MAX, hi = INT_MIN, any = 0;
-  for (int k = j * BN; k < min(T, (j + 1) * BN); ++k) {
-    const int s = seg ? seg[size_t(b) * T + k] : 1;
+// One warp per (sequence, key tile); lane l handles keys l and l + 32.
+__global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T, int n_kt,
+                                 TileMeta *meta, int B) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= B * n_kt) return;
+  const int b = w / n_kt, j = w % n_kt;
+  TileMeta &m = meta[w];
+  int lo = INT_MAX, hi = INT_MIN, all = 1, any = 0;
+  for (int kk = lane; kk < BN; kk += 32) {
+    const int k = j * BN + kk;
+    const int s = k < T ? (seg ? seg[size_t(b) * T + k] : 1) : 0;
+    const int sk = (k < T && sink) ? (sink[size_t(b) * T + k] != 0) : 0;
+    m.seg[kk] = s;
+    m.sink[kk] = (unsigned char)sk;
     if (s > 0) {
       lo = min(lo, s);
       hi = max(hi, s);
     }
-    if (sink) any |= sink[size_t(b) * T + k] != 0;
+    all &= sk;
+    any |= sk;
   }
-  sum[i] = {lo, hi, any};
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    all &= __shfl_xor_sync(0xffffffffu, all, off);
+    any |= __shfl_xor_sync(0xffffffffu, any, off);
+  }
+  if (lane == 0) {
+    m.seg_lo = lo;
+    m.seg_hi = hi;
+    m.all_sink = all;
+    m.any_sink = any;
+  }
 }
 
 // One thread per (sequence, row span): the key tiles any row of the span may
 // see, pooled tiles first (entry bit 20 set), then exact tiles, ascending.
-__global__ void tile_plan_kernel(const TileSummary *sum, TcParams p, int32_t *plan) {
+__global__ void tile_plan_kernel(const TileMeta *meta, TcParams p, int32_t *plan) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= p.B * p.n_span) return;
   const int b = i / p.n_span, sp = i % p.n_span;
@@ -104,7 +133,7 @@ __global__ void tile_plan_kernel(const TileSummary *sum, TcParams p, int32_t *pl
   }
   if (qlo <= qhi) {
     for (int j = 0; j * BN <= q1; ++j) {
-      const TileSummary t = sum[size_t(b) * p.n_kt + j];
+      const TileMeta &t = meta[size_t(b) * p.n_kt + j];
       if (t.seg_lo > t.seg_hi || t.seg_lo > qhi || t.seg_hi < qlo) continue;
       const bool in_window = p.W == 0 || (j + 1) * BN - 1 >= q0 - p.W + 1;
       if (!in_window && !t.any_sink) continue;
@@ -226,16 +255,20 @@ struct Lay {
   static constexpr int oQ = 0;                     // Q[2 blocks]
   static constexpr int oKV = 2 * kQ;               // {K, V}[NS stages]
   static constexpr int oP = oKV + NS * 2 * kKV;    // P[2 blocks]
-  static constexpr int kBytes = oP + 2 * kP + 1024;  // + alignment slack
+  static constexpr int oM = oP + 2 * kP;           // TileMeta[NS stages]
+  static constexpr int kBytes = oM + NS * int(sizeof(TileMeta)) + 1024;  // + alignment slack
   // TMEM columns: S[block][2 buffers] (BN each), then O[block] (D each)
   static constexpr int kCols = 4 * BN + 2 * D;
   static constexpr int kTmemCols = kCols <= 256 ? 256 : 512;
 };
 
-// Per-stage key-tile facts the loader publishes with the metadata.
-struct TileFlags {
-  int seg_lo, seg_hi, all_sink;
-};
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -248,9 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       pv_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_seg[NS][BN];
-  __shared__ unsigned char s_sink[NS][BN];
-  __shared__ TileFlags s_flags[NS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z;
@@ -268,11 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sK = [&](int st) { return base + L::oKV + st * 2 * L::kKV; };
   auto sV = [&](int st) { return base + L::oKV + st * 2 * L::kKV + L::kKV; };
   auto sP = [&](int rb) { return base + L::oP + rb * L::kP; };
+  auto sM = [&](int st) { return base + L::oM + st * uint32_t(sizeof(TileMeta)); };
+  auto meta_at = [&](int st) {  // generic pointer to a stage's metadata record
+    return reinterpret_cast<const TileMeta *>(smem_raw + (sM(st) - smem_u32(smem_raw)));
+  };
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&kv_full[s], 2);  // expect_tx arrival + metadata arrival
+      mbar_init(&kv_full[s], 1 + 32);  // expect_tx arrival + one metadata arrival per loader lane
       mbar_init(&kv_empty[s], 1);
     }
     for (int r = 0; r < 2; ++r) {
@@ -316,28 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = plan[1 + j];
       const bool pooled = (e >> 20) & 1;
       const int jt = e & 0xFFFFF;
-      int lo = INT_MAX, hi = INT_MIN, all_sink = 1;
-      for (int kk = lane; kk < BN; kk += 32) {
-        const int k = jt * BN + kk;
-        int sg = k, sk = 0;
-        if (!pooled) {
-          sg = k < p.T ? (p.seg ? p.seg[size_t(b) * p.T + k] : 1) : 0;
-          sk = (k < p.T && p.sink) ? p.sink[size_t(b) * p.T + k] : 0;
-          lo = min(lo, sg);
-          hi = max(hi, sg);
-          all_sink &= sk != 0;
-        }
-        s_seg[st][kk] = sg;  // pooled tile: the column index
-        s_sink[st][kk] = (unsigned char)sk;
-      }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-        all_sink &= __shfl_xor_sync(0xffffffffu, all_sink, off);
-      }
-      if (lane == 0) s_flags[st] = {lo, hi, all_sink};
-      __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&kv_full[st], 2 * L::kKV);
         const CUtensorMap *mk = pooled ? &tm_pk : &tm_k;
@@ -346,8 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sK(st) + x * BN * 128, mk, 64 * x, hk, jt * BN, b, &kv_full[st]);
           tma_load_4d(sV(st) + x * BN * 128, mv, 64 * x, hk, jt * BN, b, &kv_full[st]);
         }
-        mbar_arrive(&kv_full[st]);  // metadata written by the whole warp (ordered by __syncwarp)
       }
+      // the exact tile's metadata record (384 bytes) rides along asynchronously;
+      // pooled tiles need none
+      constexpr int kChunks = int(sizeof(TileMeta)) / 16;
+      if (!pooled && lane < kChunks)
+        cp_async16(sM(st) + lane * 16,
+                   reinterpret_cast<const char *>(p.meta + size_t(b) * p.n_kt + jt) + lane * 16);
+      cp_async_arrive(&kv_full[st]);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer
@@ -433,9 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pooled) {
         full = myseg > 0 && k0 + BN - 1 < p.nb && (k0 + BN) * p.block <= q - p.W + 1;
       } else {
-        const TileFlags f = s_flags[st];
-        full = myseg > 0 && f.seg_lo == myseg && f.seg_hi == myseg && k0 + BN - 1 <= q &&
-               (q - k0 < W || f.all_sink);
+        const TileMeta *f = meta_at(st);
+        full = myseg > 0 && f->seg_lo == myseg && f->seg_hi == myseg && k0 + BN - 1 <= q &&
+               (q - k0 < W || f->all_sink);
       }
       float s[BN];
       if (__all_sync(0xffffffffu, full)) {
@@ -445,15 +463,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < BN; ++x) {
           const int jp = k0 + x;
-          const bool vis = myseg > 0 && jp < p.nb && (jp + 1) * p.block <= q - p.W + 1;
+          const bool vis = (myseg > 0) & (jp < p.nb) & ((jp + 1) * p.block <= q - p.W + 1);
           s[x] = vis ? __uint_as_float(sr[x]) : -INFINITY;
         }
       } else {
+        // Branch-free: every key's segment id and sink flag is loaded (4 at a
+        // time) and combined with bitwise operators, so no per-key branch or
+        // guarded load serialises the warp.
+        const uint32_t mseg = sM(st), msink = sM(st) + BN * 4;
 #pragma unroll
-        for (int x = 0; x < BN; ++x) {
-          const int k = k0 + x;
-          const bool vis = myseg > 0 && k <= q && s_seg[st][x] == myseg && (q - k < W || s_sink[st][x]);
-          s[x] = vis ? __uint_as_float(sr[x]) : -INFINITY;
+        for (int x = 0; x < BN; x += 4) {
+          int sg[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(sg[0]), "=r"(sg[1]), "=r"(sg[2]), "=r"(sg[3])
+                       : "r"(mseg + x * 4));
+          uint32_t sk;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sk) : "r"(msink + x));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int k = k0 + x + i;
+            const bool vis = (myseg > 0) & (k <= q) & (sg[i] == myseg) &
+                             ((q - k < W) | (((sk >> (8 * i)) & 0xffu) != 0u));
+            s[x + i] = vis ? __uint_as_float(sr[x + i]) : -INFINITY;
+          }
         }
       }
       float mxp[8];
@@ -598,7 +630,7 @@ PlanDims plan_dims(int B, int T, int block, int span) {
   const int nb = block > 0 ? T / block : 0;
   d.n_pt = (nb + BN - 1) / BN;
   d.stride = 1 + d.n_kt + d.n_pt;
-  d.sum_bytes = (size_t(B) * d.n_kt * sizeof(TileSummary) + 255) / 256 * 256;
+  d.sum_bytes = (size_t(B) * d.n_kt * sizeof(TileMeta) + 255) / 256 * 256;
   d.plan_bytes = size_t(B) * ((T + BM - 1) / BM) * d.stride * sizeof(int32_t);
   return d;
 }
@@ -608,7 +640,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   const int G = a.Hq / a.Hkv;
   const bool pair_heads = G % 2 == 0;
   PlanDims pd = plan_dims(a.batch, a.T, a.block, pair_heads ? BM : 2 * BM);
-  TileSummary *sum = static_cast<TileSummary *>(ws);
+  TileMeta *meta = static_cast<TileMeta *>(ws);
   int32_t *plan = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pd.sum_bytes);
   TcParams p;
   p.B = a.batch;
@@ -627,6 +659,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.seg = a.seg_ids;
   p.sink = a.sink;
   p.plan = plan;
+  p.meta = meta;
   p.out = static_cast<uint16_t *>(a.out);
   p.lse = a.lse;
   p.err = err;
@@ -644,9 +677,9 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
     tpv = tv;
   }
   const int ns = a.batch * pd.n_kt;
-  tile_summary_kernel<<<(ns + 127) / 128, 128, 0, stream>>>(a.seg_ids, a.sink, a.T, pd.n_kt, sum, a.batch);
+  tile_meta_kernel<<<(ns + 3) / 4, 128, 0, stream>>>(a.seg_ids, a.sink, a.T, pd.n_kt, meta, a.batch);
   const int nq = a.batch * pd.n_span;
-  tile_plan_kernel<<<(nq + 127) / 128, 128, 0, stream>>>(sum, p, plan);
+  tile_plan_kernel<<<(nq + 127) / 128, 128, 0, stream>>>(meta, p, plan);
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
