@@ -47,6 +47,7 @@ constexpr int NS = 3;    // K/V stages
 constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kThreads = 10 * 32;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
+constexpr int kMaxPlan = 1024;      // tile-list entries staged in shared memory
 
 // Per (sequence, 64-key tile) metadata record, written once per call by
 // tile_meta_kernel and copied asynchronously into shared memory by the loader
@@ -56,7 +57,9 @@ struct alignas(128) TileMeta {
   unsigned char sink[BN];
   int seg_lo, seg_hi;          // over keys with a positive id (lo > hi: none)
   int all_sink, any_sink;
-  int pad[12];
+  unsigned long long sink_bits;  // bit x = key x is a sink
+  int uniform_seg;             // the one id every key < T carries (> 0), else 0
+  int pad[9];
 };
 static_assert(sizeof(TileMeta) == 384, "16-byte chunks for cp.async");
 
@@ -80,8 +83,9 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
   if (w >= B * n_kt) return;
   const int b = w / n_kt, j = w % n_kt;
   TileMeta &m = meta[w];
-  int lo = INT_MAX, hi = INT_MIN, all = 1, any = 0;
-  for (int kk = lane; kk < BN; kk += 32) {
+  int lo = INT_MAX, hi = INT_MIN, all = 1, any = 0, padding = 0;
+  uint32_t sink_word[2];
+  for (int kk = lane, half = 0; kk < BN; kk += 32, ++half) {
     const int k = j * BN + kk;
     const int s = k < T ? (seg ? seg[size_t(b) * T + k] : 1) : 0;
     const int sk = (k < T && sink) ? (sink[size_t(b) * T + k] != 0) : 0;
@@ -91,8 +95,10 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
       lo = min(lo, s);
       hi = max(hi, s);
     }
+    padding |= (k < T) & (s <= 0);
     all &= sk;
     any |= sk;
+    sink_word[half] = __ballot_sync(0xffffffffu, sk != 0);
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) {
@@ -100,12 +106,15 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
     hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
     all &= __shfl_xor_sync(0xffffffffu, all, off);
     any |= __shfl_xor_sync(0xffffffffu, any, off);
+    padding |= __shfl_xor_sync(0xffffffffu, padding, off);
   }
   if (lane == 0) {
     m.seg_lo = lo;
     m.seg_hi = hi;
     m.all_sink = all;
     m.any_sink = any;
+    m.sink_bits = (unsigned long long)sink_word[0] | ((unsigned long long)sink_word[1] << 32);
+    m.uniform_seg = (lo == hi && !padding) ? lo : 0;
   }
 }
 
@@ -281,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pv_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_plan[kMaxPlan];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z;
@@ -292,6 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t *plan = p.plan + (size_t(b) * p.n_span + blockIdx.x) * p.plan_stride;
   const int n = plan[0];
   volatile int *abort_flag = &s_abort;
+  // the tile list, staged once in shared memory (read by every role each tile)
+  for (int i = tid; i < n && i < kMaxPlan; i += kThreads) s_plan[i] = plan[1 + i];
+  const int32_t *tiles = n <= kMaxPlan ? s_plan : plan + 1;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   auto sQ = [&](int rb) { return base + L::oQ + rb * L::kQ; };
@@ -347,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j >= NS && !wait_or_abort(&kv_empty[st], ((j / NS) - 1) & 1, p.err, abort_flag)) fail = true;
       fail = __any_sync(0xffffffffu, fail);  // the warp leaves the loop together
       if (fail) break;
-      const int e = plan[1 + j];
+      const int e = tiles[j];
       const bool pooled = (e >> 20) & 1;
       const int jt = e & 0xFFFFF;
       if (lane == 0) {
@@ -369,9 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer
-    //   S(0), S(1) for both blocks, then per tile j: O += P V for both blocks
-    //   (each waits for its block's P), then S(j+2) into the S buffer tile j
-    //   just freed, once tile j+2's K/V have landed.
+    //   An event loop serves each block on its own: S(s) into S buffer s&1 as
+    //   soon as that buffer is free (the block wrote P(s-2)) and tile s's K/V
+    //   have landed; O += P V as soon as the block's P is written.  A K/V
+    //   stage is released once both blocks' PV of its tile are issued, so the
+    //   blocks drift apart by at most the stage ring.
     if (lane == 0 && n > 0) {
       constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
@@ -387,36 +402,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_full[rb][j & 1]);
       };
       bool ok = wait_or_abort(&bar_q, 0, p.err, abort_flag);
-      for (int j = 0; j < 2 && j < n && ok; ++j) {
-        ok = wait_or_abort(&kv_full[j % NS], (j / NS) & 1, p.err, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, j);
-          issue_s(1, j);
-        }
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        const int st = j % NS;
-        for (int rb = 0; rb < 2 && ok; ++rb) {
-          ok = wait_or_abort(&p_full[rb], j & 1, p.err, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
+      int js[2] = {0, 0};   // next tile whose S each block needs
+      int jpv[2] = {0, 0};  // next tile whose PV each block awaits
+      int released = 0;     // tiles whose K/V stage went back to the loader
+      uint32_t idle = 0;
+      while (ok && (jpv[0] < n || jpv[1] < n)) {
+        bool progress = false;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sP(rb) + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
-            mma_bf16(tO(rb), a, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int rb = 0; rb < 2; ++rb) {
+          const int s = js[rb];
+          if (s < n && s <= jpv[rb] + 1 && mbar_test_wait(&kv_full[s % NS], (s / NS) & 1)) {
+            tc_fence_after();
+            issue_s(rb, s);
+            js[rb] = s + 1;
+            progress = true;
           }
-          mma_commit(&pv_done[rb]);
+          const int j = jpv[rb];
+          if (j < n && j < js[rb] && mbar_test_wait(&p_full[rb], j & 1)) {
+            tc_fence_after();
+            const int st = j % NS;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t a = sdesc_sw128(sP(rb) + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
+              mma_bf16(tO(rb), a, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&pv_done[rb]);
+            jpv[rb] = j + 1;
+            progress = true;
+          }
         }
-        if (!ok) break;
-        mma_commit(&kv_empty[st]);
-        if (j + 2 < n) {
-          ok = wait_or_abort(&kv_full[(j + 2) % NS], ((j + 2) / NS) & 1, p.err, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(0, j + 2);
-          issue_s(1, j + 2);
+        while (released < min(jpv[0], jpv[1])) {
+          mma_commit(&kv_empty[released % NS]);  // both blocks' PV of that tile issued
+          ++released;
+        }
+        if (progress) {
+          idle = 0;
+        } else if (__nanosleep(32), ++idle > kWaitLimit) {  // idle: yield the issue slot
+          raise_device_error(p.err, ND_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+        } else if ((idle & 255u) == 255u && *abort_flag) {
+          ok = false;
         }
       }
       fail = !ok;
@@ -434,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n; ++j) {
       const int st = j % NS;
-      const int e = plan[1 + j];
+      const int e = tiles[j];
       const bool pooled = (e >> 20) & 1;
       const int k0 = (e & 0xFFFFF) * BN;
       if (!fail && !(wait_or_abort(&s_full[rb][j & 1], (j >> 1) & 1, p.err, abort_flag) &&
@@ -442,10 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail = true;
       __syncwarp();
       tc_fence_after();
-      uint32_t sr[BN];
-      tmem_ld32(tS(rb, j & 1) + lane_base, sr);
-      tmem_ld32(tS(rb, j & 1) + lane_base + 32, sr + 32);
+      // one 64-register row buffer: raw scores, then masked scores, then p
+      uint32_t v[BN];
+      tmem_ld32(tS(rb, j & 1) + lane_base, v);
+      tmem_ld32(tS(rb, j & 1) + lane_base + 32, v + 32);
       tmem_ld_wait();
+      constexpr uint32_t kNegInf = 0xff800000u;
       // every key of the tile visible for this row?  (warp-uniform fast path)
       bool full;
       if (pooled) {
@@ -455,44 +484,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         full = myseg > 0 && f->seg_lo == myseg && f->seg_hi == myseg && k0 + BN - 1 <= q &&
                (q - k0 < W || f->all_sink);
       }
-      float s[BN];
       if (__all_sync(0xffffffffu, full)) {
-#pragma unroll
-        for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
+        // nothing to mask
       } else if (pooled) {
 #pragma unroll
         for (int x = 0; x < BN; ++x) {
           const int jp = k0 + x;
           const bool vis = (myseg > 0) & (jp < p.nb) & ((jp + 1) * p.block <= q - p.W + 1);
-          s[x] = vis ? __uint_as_float(sr[x]) : -INFINITY;
+          v[x] = vis ? v[x] : kNegInf;
         }
       } else {
-        // Branch-free: every key's segment id and sink flag is loaded (4 at a
-        // time) and combined with bitwise operators, so no per-key branch or
-        // guarded load serialises the warp.
-        const uint32_t mseg = sM(st), msink = sM(st) + BN * 4;
+        // A 64-bit visibility mask for this row, then one bit test and a
+        // select per key.
+        const TileMeta *f = meta_at(st);
+        uint32_t v0 = 0u, v1 = 0u;
+        if (f->uniform_seg != 0) {
+          // every key in one segment: (causal bound) and (window range or
+          // sink), built from shifts
+          const int hi = q - k0;                             // last causal key (tile-relative)
+          const int lo = W == INT_MAX ? 0 : q - W + 1 - k0;  // first key inside the window
+          const unsigned long long all1 = ~0ull;
+          const unsigned long long causal = hi < 0 ? 0ull : (hi >= 63 ? all1 : (all1 >> (63 - hi)));
+          const unsigned long long window = lo <= 0 ? all1 : (lo > 63 ? 0ull : (all1 << lo));
+          const unsigned long long vis =
+              (f->uniform_seg == myseg && myseg > 0) ? (causal & (window | f->sink_bits)) : 0ull;
+          v0 = uint32_t(vis);
+          v1 = uint32_t(vis >> 32);
+        } else {
+          // keys from several segments (or padding): compare every key's
+          // segment id and sink flag, four at a time, branch-free; the loop
+          // stays rolled so the loads do not pile up in registers
+          const uint32_t mseg = sM(st), msink = sM(st) + BN * 4;
+#pragma unroll 1
+          for (int x = 0; x < BN; x += 4) {
+            int sg[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(sg[0]), "=r"(sg[1]), "=r"(sg[2]), "=r"(sg[3])
+                         : "r"(mseg + x * 4));
+            uint32_t sk;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sk) : "r"(msink + x));
+            uint32_t bits = 0u;
 #pragma unroll
-        for (int x = 0; x < BN; x += 4) {
-          int sg[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(sg[0]), "=r"(sg[1]), "=r"(sg[2]), "=r"(sg[3])
-                       : "r"(mseg + x * 4));
-          uint32_t sk;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sk) : "r"(msink + x));
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int k = k0 + x + i;
-            const bool vis = (myseg > 0) & (k <= q) & (sg[i] == myseg) &
-                             ((q - k < W) | (((sk >> (8 * i)) & 0xffu) != 0u));
-            s[x + i] = vis ? __uint_as_float(sr[x + i]) : -INFINITY;
+            for (int i = 0; i < 4; ++i) {
+              const int k = k0 + x + i;
+              const bool vis = (myseg > 0) & (k <= q) & (sg[i] == myseg) &
+                               ((q - k < W) | (((sk >> (8 * i)) & 0xffu) != 0u));
+              bits |= uint32_t(vis) << i;
+            }
+            if (x < 32) v0 |= bits << x;
+            else v1 |= bits << (x - 32);
           }
+        }
+#pragma unroll
+        for (int x = 0; x < BN; ++x) {
+          const uint32_t bit = x < 32 ? (v0 >> x) & 1u : (v1 >> (x - 32)) & 1u;
+          v[x] = bit ? v[x] : kNegInf;
         }
       }
       float mxp[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mxp[i] = s[i];
+      for (int i = 0; i < 8; ++i) mxp[i] = __uint_as_float(v[i]);
 #pragma unroll
-      for (int x = 8; x < BN; ++x) mxp[x & 7] = fmaxf(mxp[x & 7], s[x]);
+      for (int x = 8; x < BN; ++x) mxp[x & 7] = fmaxf(mxp[x & 7], __uint_as_float(v[x]));
       const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                              fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       if (m_used == -INFINITY) m_used = mx;  // nothing accumulated yet: no rescale
@@ -503,14 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mx;
       }
       const float mc = m_used == -INFINITY ? 0.f : m_used * c;
-      uint32_t pk[BN / 2];
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int x = 0; x < BN; x += 2) {
-        const float p0 = ex2(fmaf(s[x], c, -mc));
-        const float p1 = ex2(fmaf(s[x + 1], c, -mc));
-        rsp[(x >> 1) & 3] += p0 + p1;
-        pk[x >> 1] = pack_bf16x2(p0, p1);
+      for (int x = 0; x < BN; ++x) {
+        const float pv = ex2(fmaf(__uint_as_float(v[x]), c, -mc));
+        rsp[x & 3] += pv;
+        v[x] = __float_as_uint(pv);
       }
       l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       // PV(j-1) must have landed before O is rescaled or P is overwritten
@@ -531,9 +582,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t prow = sP(rb) + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch)
-        st_shared_v4(prow + ((ch ^ (r & 7)) << 4), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                     pk[4 * ch + 3]);
+      for (int ch = 0; ch < BN / 8; ++ch) {
+        st_shared_v4(prow + ((ch ^ (r & 7)) << 4),
+                     pack_bf16x2(__uint_as_float(v[8 * ch]), __uint_as_float(v[8 * ch + 1])),
+                     pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
+                     pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
+                     pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[rb]);
