@@ -275,9 +275,9 @@ def bench_decode(torch, nd, B, Hq, Hkv, d, S, W, steps, warmup, seed, pk, dist=N
         _state=(reps, ws))
 
 
-def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None):
+def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
     from workloads import packed_prefill
-    w = packed_prefill()
+    w = packed_prefill(B=batch)
     B, T, Hq, d = w["q"].shape
     Hkv = w["k"].shape[2]
     q, k, v = dev_bf16(torch, w["q_bits"]), dev_bf16(torch, w["k_bits"]), dev_bf16(torch, w["v_bits"])
@@ -294,7 +294,7 @@ def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None):
     pairs = int(visible_pairs_packed(w["seg_ids"], w["sink"], w["window"]).sum())
     flops = 4.0 * d * pairs * Hq
     t = ms / steps * 1e-3
-    return dict(config="packed prefill B8 T4096 Hq32 Hkv8 d128 W256 RoPE, 3-6 segments with 64-512 sink prefixes",
+    return dict(config=f"packed prefill B{B} T{T} Hq{Hq} Hkv{Hkv} d{d} W256 RoPE, 3-6 segments with 64-512 sink prefixes",
                 ms_per_step=ms / steps, tok_s=B * T / t, tflops=flops / t / 1e12,
                 frac=flops / t / 1e12 / pk["bf16"], visible_pairs=pairs, flops_per_step=flops,
                 launches=2 * steps)
@@ -404,6 +404,8 @@ def main():
     ap.add_argument("--impl", default="nd", choices=["nd", "reference"])
     ap.add_argument("--rows", default="all", help="comma list of extra rows: sweep,packed,compressed or none")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--packed-batch", type=int, default=8,
+                    help="sequences in the packed-prefill row (8 = the measured configuration; smaller for profiling)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
@@ -470,7 +472,8 @@ def main():
             torch.cuda.empty_cache()
         rows["decode_sweep"] = dict(config="decode + fused append, Hq32 Hkv8 d128, 1024 sinks + 256 ring", **sweep)
     if "packed" in want:
-        rows["packed_prefill"] = bench_packed_prefill(torch, nd, max(10, steps // 10), warmup, pk, dist)
+        rows["packed_prefill"] = bench_packed_prefill(torch, nd, max(10, steps // 10), warmup, pk, dist,
+                                                      batch=args.packed_batch)
         torch.cuda.empty_cache()
     if "compressed" in want:
         rows["compressed_prefill"] = bench_compressed(torch, nd, max(10, steps // 10), warmup, pk, dist)

@@ -13,22 +13,26 @@
 //
 // One CTA runs two 128-row blocks that share their K/V tiles: two query heads
 // of one GQA group (same rows), or, when the group size is odd, two
-// consecutive row blocks of one head.  Its ten warps specialise:
+// consecutive row blocks of one head.  Its eleven warps specialise:
 //   warps 0-3, 4-7 : one softmax warpgroup per row block; thread i owns row i
 //                    (= TMEM lane i): exact mask, online softmax in the log2
-//                    domain, bf16 P into a 128-byte-swizzled shared tile.
-//   warp 8         : TMA loader -- Q once, then K/V tiles over three stages,
-//                    with each tile's segment / sink record (cp.async).
-//   warp 9         : MMA issuer -- S = Q K^T (M128 N64, double-buffered in
-//                    TMEM, issued two tiles ahead) and O += P V (M128, N=d, V as
-//                    an MN-major operand) for both blocks, so the tensor core
-//                    works ahead while the softmax warps handle a tile.
+//                    domain; bf16 P goes back into TMEM over the S columns
+//                    it came from.
+//   warp 8         : TMA loader over three rings: K tiles
+//                    (freed as soon as both blocks' S MMAs have read them),
+//                    V tiles (freed after both blocks' PV) and the exact
+//                    tiles' segment / sink records (cp.async, freed once the
+//                    softmax warps have built their masks).
+//   warps 9, 10    : one MMA issuer per row block -- S = Q K^T (M128 N64,
+//                    double-buffered in TMEM, two tiles ahead) and O += P V
+//                    (M128, N=d, P read from TMEM, V an MN-major shared
+//                    operand) -- so neither block waits behind the other's.
 // O accumulates in TMEM; a row's O is rescaled (TMEM load / multiply / store)
 // only when its running max grows by more than 2^8, so most tiles touch O
 // only through the MMA.  Tiles every row of a warp fully sees skip the
-// per-element mask.  Every mbarrier wait
-// is bounded; a wait that gives up raises the device error flag and a shared
-// abort flag, and all roles then run to the common exit, which frees TMEM.
+// per-element mask.  Every mbarrier wait is bounded; a wait that gives up
+// raises the device error flag and a shared abort flag, and all roles then run
+// to the common exit, which frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,9 +47,9 @@ namespace {
 
 constexpr int BM = 128;  // rows per block = TMEM lanes
 constexpr int BN = 64;   // keys per tile
-constexpr int NS = 3;    // K/V stages
-constexpr int kWarpLoad = 8, kWarpMma = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int NM = 8;    // tile-record stages
+constexpr int kWarpLoad = 8, kWarpMma0 = 9, kWarpMma1 = 10;
+constexpr int kThreads = 11 * 32;
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 constexpr int kMaxPlan = 1024;      // tile-list entries staged in shared memory
 
@@ -178,6 +182,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// Same with the A operand (M x K, K-major) read from TMEM.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -199,6 +212,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       "%3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+
+// TMA tile store from shared memory (rows past the tensor's extent are not
+// written), then wait until the copy has read its shared-memory source.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(BM) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
@@ -257,15 +288,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
 
 template <int D>
 struct Lay {
+  static constexpr int NK = D == 64 ? 6 : 4;       // K stages
+  static constexpr int NV = D == 64 ? 5 : 3;       // V stages
   static constexpr int kBoxes = D / 64;            // 64-column swizzle atoms per row
   static constexpr int kQ = kBoxes * BM * 128;     // one block's Q tile
   static constexpr int kKV = kBoxes * BN * 128;    // one K (or V) tile
-  static constexpr int kP = BM * BN * 2;           // one P tile
+  static constexpr int kP = BM * 64 * 2;           // one 64-column bf16 O slab
   static constexpr int oQ = 0;                     // Q[2 blocks]
-  static constexpr int oKV = 2 * kQ;               // {K, V}[NS stages]
-  static constexpr int oP = oKV + NS * 2 * kKV;    // P[2 blocks]
-  static constexpr int oM = oP + 2 * kP;           // TileMeta[NS stages]
-  static constexpr int kBytes = oM + NS * int(sizeof(TileMeta)) + 1024;  // + alignment slack
+  static constexpr int oK = 2 * kQ;                // K[NK stages]
+  static constexpr int oV = oK + NK * kKV;         // V[NV stages]
+  static constexpr int oP = oV + NV * kKV;         // O staging slab[2 blocks]
+  static constexpr int oM = oP + 2 * kP;           // TileMeta[NM stages]
+  static constexpr int kBytes = oM + NM * int(sizeof(TileMeta)) + 1024;  // + alignment slack
   // TMEM columns: S[block][2 buffers] (BN each), then O[block] (D each)
   static constexpr int kCols = 4 * BN + 2 * D;
   static constexpr int kTmemCols = kCols <= 256 ? 256 : 512;
@@ -283,11 +317,13 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_pk,
-                      const __grid_constant__ CUtensorMap tm_pv, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_pv, const __grid_constant__ CUtensorMap tm_o,
+                      const TcParams p) {
   using L = Lay<D>;
+  constexpr int NK = L::NK, NV = L::NV;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, kv_full[NS], kv_empty[NS], s_full[2][2], p_full[2],
-      pv_done[2];
+  __shared__ __align__(8) uint64_t bar_q, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+      m_full[NM], m_empty[NM], s_full[2][2], p_full[2], pv_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_plan[kMaxPlan];
@@ -308,19 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   auto sQ = [&](int rb) { return base + L::oQ + rb * L::kQ; };
-  auto sK = [&](int st) { return base + L::oKV + st * 2 * L::kKV; };
-  auto sV = [&](int st) { return base + L::oKV + st * 2 * L::kKV + L::kKV; };
+  auto sK = [&](int st) { return base + L::oK + st * L::kKV; };
+  auto sV = [&](int st) { return base + L::oV + st * L::kKV; };
   auto sP = [&](int rb) { return base + L::oP + rb * L::kP; };
   auto sM = [&](int st) { return base + L::oM + st * uint32_t(sizeof(TileMeta)); };
-  auto meta_at = [&](int st) {  // generic pointer to a stage's metadata record
+  auto meta_at = [&](int st) {  // generic pointer to a stage's tile record
     return reinterpret_cast<const TileMeta *>(smem_raw + (sM(st) - smem_u32(smem_raw)));
   };
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&kv_full[s], 1 + 32);  // expect_tx arrival + one metadata arrival per loader lane
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 2);  // one commit from each block's issuer
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 2);
+    }
+    for (int s = 0; s < NM; ++s) {
+      mbar_init(&m_full[s], 32);   // one cp.async arrival per loader lane
+      mbar_init(&m_empty[s], 8);   // one arrival per softmax warp
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r][0], 1);
@@ -331,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&s_tmem)),
                  "r"(L::kTmemCols)
@@ -348,6 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------ TMA loader
+    //   Rings: K tiles (NK stages, freed once both blocks' S MMAs read them),
+    //   V tiles (NV stages, freed after both blocks' PV) and tile records
+    //   (NM stages, freed once all eight softmax warps built their masks).
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(&bar_q, 2 * L::kQ);
       for (int x = 0; x < L::kBoxes; ++x) {
@@ -355,43 +402,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sQ(1) + x * BM * 128, &tm_q, 64 * x, head1, row01, b, &bar_q);
       }
     }
-    for (int j = 0; j < n; ++j) {
-      const int st = j % NS;
-      if (j >= NS && !wait_or_abort(&kv_empty[st], ((j / NS) - 1) & 1, p.err, abort_flag)) fail = true;
-      fail = __any_sync(0xffffffffu, fail);  // the warp leaves the loop together
-      if (fail) break;
+    // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...  Every
+    // wait blocks in hardware (no polling loop competing for issue slots).
+    auto load_k = [&](int j) {
       const int e = tiles[j];
       const bool pooled = (e >> 20) & 1;
       const int jt = e & 0xFFFFF;
+      const int st = j % NK, sm = j % NM;
+      bool ok = true;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kKV);
-        const CUtensorMap *mk = pooled ? &tm_pk : &tm_k;
-        const CUtensorMap *mv = pooled ? &tm_pv : &tm_v;
-        for (int x = 0; x < L::kBoxes; ++x) {
-          tma_load_4d(sK(st) + x * BN * 128, mk, 64 * x, hk, jt * BN, b, &kv_full[st]);
-          tma_load_4d(sV(st) + x * BN * 128, mv, 64 * x, hk, jt * BN, b, &kv_full[st]);
+        ok = (j < NK || wait_or_abort(&k_empty[st], ((j / NK) - 1) & 1, p.err, abort_flag)) &&
+             (j < NM || wait_or_abort(&m_empty[sm], ((j / NM) - 1) & 1, p.err, abort_flag));
+        if (ok) {
+          mbar_arrive_expect_tx(&k_full[st], L::kKV);
+          for (int x = 0; x < L::kBoxes; ++x)
+            tma_load_4d(sK(st) + x * BN * 128, pooled ? &tm_pk : &tm_k, 64 * x, hk, jt * BN, b, &k_full[st]);
         }
       }
-      // the exact tile's metadata record (384 bytes) rides along asynchronously;
-      // pooled tiles need none
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return false;
+      // the exact tile's record (384 bytes) rides along asynchronously;
+      // pooled tiles need none, but every lane still arrives
       constexpr int kChunks = int(sizeof(TileMeta)) / 16;
       if (!pooled && lane < kChunks)
-        cp_async16(sM(st) + lane * 16,
-                   reinterpret_cast<const char *>(p.meta + size_t(b) * p.n_kt + jt) + lane * 16);
-      cp_async_arrive(&kv_full[st]);
+        cp_async16(sM(sm) + lane * 16, reinterpret_cast<const char *>(p.meta + size_t(b) * p.n_kt + jt) + lane * 16);
+      cp_async_arrive(&m_full[sm]);
+      return true;
+    };
+    auto load_v = [&](int j) {
+      const int e = tiles[j];
+      const bool pooled = (e >> 20) & 1;
+      const int jt = e & 0xFFFFF;
+      const int st = j % NV;
+      bool ok = true;
+      if (lane == 0) {
+        ok = j < NV || wait_or_abort(&v_empty[st], ((j / NV) - 1) & 1, p.err, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(&v_full[st], L::kKV);
+          for (int x = 0; x < L::kBoxes; ++x)
+            tma_load_4d(sV(st) + x * BN * 128, pooled ? &tm_pv : &tm_v, 64 * x, hk, jt * BN, b, &v_full[st]);
+        }
+      }
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
+    for (int j = 0; j <= n && !fail; ++j) {
+      if (j < n && !load_k(j)) fail = true;
+      if (!fail && j >= 1 && !load_v(j - 1)) fail = true;
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------ MMA issuer
-    //   An event loop serves each block on its own: S(s) into S buffer s&1 as
-    //   soon as that buffer is free (the block wrote P(s-2)) and tile s's K/V
-    //   have landed; O += P V as soon as the block's P is written.  A K/V
-    //   stage is released once both blocks' PV of its tile are issued, so the
-    //   blocks drift apart by at most the stage ring.
+  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+    // ------------------------------------------------ MMA issuers, one per block
+    //   S(0), S(1); then per tile j, once this block's P(j) is written: O += P V,
+    //   and S(j+2) into the same TMEM buffer once that PV has read P(j).
+    const int rb = warp - kWarpMma0;
     if (lane == 0 && n > 0) {
       constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
-      auto issue_s = [&](int rb, int j) {
-        const int st = j % NS;
+      auto issue_s = [&](int j) {
+        const int st = j % NK;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes inside the atom
@@ -400,50 +467,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tS(rb, j & 1), a, bd, kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[rb][j & 1]);
+        mma_commit(&k_empty[st]);
       };
       bool ok = wait_or_abort(&bar_q, 0, p.err, abort_flag);
-      int js[2] = {0, 0};   // next tile whose S each block needs
-      int jpv[2] = {0, 0};  // next tile whose PV each block awaits
-      int released = 0;     // tiles whose K/V stage went back to the loader
-      uint32_t idle = 0;
-      while (ok && (jpv[0] < n || jpv[1] < n)) {
-        bool progress = false;
-#pragma unroll
-        for (int rb = 0; rb < 2; ++rb) {
-          const int s = js[rb];
-          if (s < n && s <= jpv[rb] + 1 && mbar_test_wait(&kv_full[s % NS], (s / NS) & 1)) {
-            tc_fence_after();
-            issue_s(rb, s);
-            js[rb] = s + 1;
-            progress = true;
-          }
-          const int j = jpv[rb];
-          if (j < n && j < js[rb] && mbar_test_wait(&p_full[rb], j & 1)) {
-            tc_fence_after();
-            const int st = j % NS;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t a = sdesc_sw128(sP(rb) + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sV(st) + kk * 16 * 128, BN * 128, 1024);
-              mma_bf16(tO(rb), a, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&pv_done[rb]);
-            jpv[rb] = j + 1;
-            progress = true;
-          }
+      for (int j = 0; j < 2 && j < n && ok; ++j) {
+        ok = wait_or_abort(&k_full[j % NK], (j / NK) & 1, p.err, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_s(j);
         }
-        while (released < min(jpv[0], jpv[1])) {
-          mma_commit(&kv_empty[released % NS]);  // both blocks' PV of that tile issued
-          ++released;
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int sv = j % NV;
+        ok = wait_or_abort(&p_full[rb], j & 1, p.err, abort_flag) &&
+             wait_or_abort(&v_full[sv], (j / NV) & 1, p.err, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys = 8 TMEM columns of bf16 pairs
+          const uint64_t bd = sdesc_sw128(sV(sv) + kk * 16 * 128, BN * 128, 1024);
+          mma_bf16_ts(tO(rb), tS(rb, j & 1) + kk * 8, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        if (progress) {
-          idle = 0;
-        } else if (__nanosleep(32), ++idle > kWaitLimit) {  // idle: yield the issue slot
-          raise_device_error(p.err, ND_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          ok = false;
-        } else if ((idle & 255u) == 255u && *abort_flag) {
-          ok = false;
+        mma_commit(&pv_done[rb]);
+        mma_commit(&v_empty[sv]);
+        if (j + 2 < n) {
+          // S(j+2) overwrites the columns PV(j) reads P(j) from: wait for it
+          ok = wait_or_abort(&pv_done[rb], j & 1, p.err, abort_flag) &&
+               wait_or_abort(&k_full[(j + 2) % NK], ((j + 2) / NK) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(j + 2);
         }
       }
       fail = !ok;
@@ -460,12 +513,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = 1.4426950408889634f * rsqrtf(float(D));  // log2(e) / sqrt(d)
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n; ++j) {
-      const int st = j % NS;
+      const int sm = j % NM;
       const int e = tiles[j];
       const bool pooled = (e >> 20) & 1;
       const int k0 = (e & 0xFFFFF) * BN;
       if (!fail && !(wait_or_abort(&s_full[rb][j & 1], (j >> 1) & 1, p.err, abort_flag) &&
-                     wait_or_abort(&kv_full[st], (j / NS) & 1, p.err, abort_flag)))
+                     wait_or_abort(&m_full[sm], (j / NM) & 1, p.err, abort_flag)))
         fail = true;
       __syncwarp();
       tc_fence_after();
@@ -480,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pooled) {
         full = myseg > 0 && k0 + BN - 1 < p.nb && (k0 + BN) * p.block <= q - p.W + 1;
       } else {
-        const TileMeta *f = meta_at(st);
+        const TileMeta *f = meta_at(sm);
         full = myseg > 0 && f->seg_lo == myseg && f->seg_hi == myseg && k0 + BN - 1 <= q &&
                (q - k0 < W || f->all_sink);
       }
@@ -496,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // A 64-bit visibility mask for this row, then one bit test and a
         // select per key.
-        const TileMeta *f = meta_at(st);
+        const TileMeta *f = meta_at(sm);
         uint32_t v0 = 0u, v1 = 0u;
         if (f->uniform_seg != 0) {
           // every key in one segment: (causal bound) and (window range or
@@ -514,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keys from several segments (or padding): compare every key's
           // segment id and sink flag, four at a time, branch-free; the loop
           // stays rolled so the loads do not pile up in registers
-          const uint32_t mseg = sM(st), msink = sM(st) + BN * 4;
+          const uint32_t mseg = sM(sm), msink = sM(sm) + BN * 4;
 #pragma unroll 1
           for (int x = 0; x < BN; x += 4) {
             int sg[4];
@@ -541,6 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[x] = bit ? v[x] : kNegInf;
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m_empty[sm]);  // this warp is done with the tile record
       float mxp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mxp[i] = __uint_as_float(v[i]);
@@ -564,11 +619,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[x] = __float_as_uint(pv);
       }
       l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
-      // PV(j-1) must have landed before O is rescaled or P is overwritten
-      if (j >= 1 && !fail && !wait_or_abort(&pv_done[rb], (j - 1) & 1, p.err, abort_flag)) fail = true;
-      __syncwarp();
-      tc_fence_after();
+      // O is rescaled only after PV(j-1) has landed (rare: the max grew by
+      // more than 2^8); otherwise nothing here waits for the tensor core
       if (__any_sync(0xffffffffu, need) && j >= 1) {
+        if (!fail && !wait_or_abort(&pv_done[rb], (j - 1) & 1, p.err, abort_flag)) fail = true;
+        __syncwarp();
+        tc_fence_after();
 #pragma unroll 1
         for (int x = 0; x < D; x += 32) {
           uint32_t ov[32];
@@ -578,18 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st32(tO(rb) + lane_base + x, ov);
         }
-        tmem_st_wait();
       }
-      const uint32_t prow = sP(rb) + r * 128;
+      // P(j) as bf16 pairs over the first 32 columns of S(j)'s TMEM buffer
+      // (already read), where the PV MMA takes it as its A operand
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        st_shared_v4(prow + ((ch ^ (r & 7)) << 4),
-                     pack_bf16x2(__uint_as_float(v[8 * ch]), __uint_as_float(v[8 * ch + 1])),
-                     pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
-                     pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
-                     pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
-      }
-      fence_proxy_async_smem();
+      for (int i = 0; i < BN / 2; ++i)
+        v[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      tmem_st32(tS(rb, j & 1) + lane_base, v);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[rb]);
     }
@@ -597,30 +649,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n > 0 && !fail && !wait_or_abort(&pv_done[rb], (n - 1) & 1, p.err, abort_flag)) fail = true;
     __syncwarp();
     tc_fence_after();
+    // O / l, staged through this block's slab buffer as 64-column swizzled
+    // slabs and written by TMA
     const bool store = q < p.T;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint16_t *dst = p.out + ((size_t(b) * p.T + (store ? q : 0)) * p.Hq + head) * D;
+    const int row0 = rb ? row01 : row00;
+    const uint32_t prow = sP(rb) + r * 128;
 #pragma unroll 1
-    for (int x = 0; x < D; x += 32) {
-      uint32_t ov[32];
-      if (n > 0) {
-        tmem_ld32(tO(rb) + lane_base + x, ov);
-        tmem_ld_wait();
-      } else {
+    for (int x0 = 0; x0 < D; x0 += 64) {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t ov[32];
+        if (n > 0) {
+          tmem_ld32(tO(rb) + lane_base + x0 + 32 * h, ov);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = 0u;
-      }
-      if (store && !fail && !*abort_flag) {
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
 #pragma unroll
-        for (int y = 0; y < 32; y += 8) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(ov[y]) * inv, __uint_as_float(ov[y + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(ov[y + 2]) * inv, __uint_as_float(ov[y + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(ov[y + 4]) * inv, __uint_as_float(ov[y + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(ov[y + 6]) * inv, __uint_as_float(ov[y + 7]) * inv);
-          *reinterpret_cast<uint4 *>(dst + x + y) = v;
+        for (int y = 0; y < 4; ++y) {
+          const int ch = 4 * h + y;
+          st_shared_v4(prow + ((ch ^ (r & 7)) << 4),
+                       pack_bf16x2(__uint_as_float(ov[8 * y]) * inv, __uint_as_float(ov[8 * y + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(ov[8 * y + 2]) * inv, __uint_as_float(ov[8 * y + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(ov[8 * y + 4]) * inv, __uint_as_float(ov[8 * y + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(ov[8 * y + 6]) * inv, __uint_as_float(ov[8 * y + 7]) * inv));
         }
       }
+      fence_proxy_async_smem();
+      group_sync(1 + rb);
+      if (r == 0 && row0 < p.T && !fail && !*abort_flag) tma_store_4d(&tm_o, sP(rb), x0, head, row0, b);
+      group_sync(1 + rb);  // the slab buffer is free again
     }
     if (store && p.lse && !fail)
       p.lse[(size_t(b) * p.Hq + head) * p.T + q] =
@@ -633,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (__syncthreads_or(fail || *abort_flag))
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(L::kTmemCols)
@@ -719,9 +779,9 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.lse = a.lse;
   p.err = err;
 
-  CUtensorMap tq, tk, tv, tpk, tpv;
+  CUtensorMap tq, tk, tv, tpk, tpv, to;
   if (!make_map(&tq, a.q, a.batch, a.T, a.Hq, D, BM) || !make_map(&tk, a.k, a.batch, a.T, a.Hkv, D, BN) ||
-      !make_map(&tv, a.v, a.batch, a.T, a.Hkv, D, BN))
+      !make_map(&tv, a.v, a.batch, a.T, a.Hkv, D, BN) || !make_map(&to, a.out, a.batch, a.T, a.Hq, D, BM))
     return cudaErrorInvalidValue;
   if (a.block > 0 && p.nb > 0) {
     if (!make_map(&tpk, a.pooled_k, a.batch, p.nb, a.Hkv, D, BN) ||
@@ -739,7 +799,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(pd.n_span, pair_heads ? a.Hq / 2 : a.Hq, a.batch);
-  kern<<<grid, kThreads, Lay<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, p);
+  kern<<<grid, kThreads, Lay<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, to, p);
   return cudaGetLastError();
 }
 
