@@ -194,6 +194,7 @@ size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int 
   if (rope_theta != 0.f) {
     bytes += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
     bytes += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
+    bytes += round_up(rope_table_bytes(T, head_dim), 256);
   }
   if (dtype == ND_BF16) bytes += round_up(prefill_plan_bytes(batch, T, block), 256);
   return bytes;
@@ -253,8 +254,10 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
     ws += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
     void *kr = ws;
     ws += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
+    void *table = ws;
+    ws += round_up(rope_table_bytes(T, head_dim), 256);
     cudaError_t e = launch_rope_qk(q, qr, n_q_heads, k, kr, n_kv_heads, batch, T, head_dim,
-                                   rope_theta, dtype == ND_F32, s);
+                                   rope_theta, dtype == ND_F32, table, s);
     if (e != cudaSuccess) return fail_cuda(e);
     a.q = qr;
     a.k = kr;

@@ -35,8 +35,9 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
 cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                         float theta, cudaStream_t stream);
 
+size_t rope_table_bytes(int T, int head_dim);
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
-                           int batch, int T, int head_dim, float theta, bool f32,
+                           int batch, int T, int head_dim, float theta, bool f32, void *table,
                            cudaStream_t stream);
 
 cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T, int n_heads,

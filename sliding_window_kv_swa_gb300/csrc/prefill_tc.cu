@@ -122,38 +122,50 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
   }
 }
 
-// One thread per (sequence, row span): the key tiles any row of the span may
+// One warp per (sequence, row span): the key tiles any row of the span may
 // see, pooled tiles first (entry bit 20 set), then exact tiles, ascending.
 __global__ void tile_plan_kernel(const TileMeta *meta, TcParams p, int32_t *plan) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= p.B * p.n_span) return;
-  const int b = i / p.n_span, sp = i % p.n_span;
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= p.B * p.n_span) return;  // whole warps only
+  const int b = w / p.n_span, sp = w % p.n_span;
   const int q0 = sp * p.span, q1 = min(p.T, q0 + p.span) - 1;
-  int32_t *out = plan + size_t(i) * p.plan_stride;
+  int32_t *out = plan + size_t(w) * p.plan_stride;
   int n = 0;
   if (p.block > 0) {
     const int lim = q1 - p.W + 1;  // pooled column j visible iff (j+1)*block <= q - W + 1
     const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
-    for (int j = 0; j * BN < ncol; ++j) out[1 + n++] = (1 << 20) | j;
+    n = (ncol + BN - 1) / BN;
+    for (int j = lane; j < n; j += 32) out[1 + j] = (1 << 20) | j;
   }
   int qlo = INT_MAX, qhi = INT_MIN;
-  for (int q = q0; q <= q1; ++q) {
+  for (int q = q0 + lane; q <= q1; q += 32) {
     const int s = p.seg ? p.seg[size_t(b) * p.T + q] : 1;
     if (s > 0) {
       qlo = min(qlo, s);
       qhi = max(qhi, s);
     }
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    qlo = min(qlo, __shfl_xor_sync(0xffffffffu, qlo, off));
+    qhi = max(qhi, __shfl_xor_sync(0xffffffffu, qhi, off));
+  }
   if (qlo <= qhi) {
-    for (int j = 0; j * BN <= q1; ++j) {
-      const TileMeta &t = meta[size_t(b) * p.n_kt + j];
-      if (t.seg_lo > t.seg_hi || t.seg_lo > qhi || t.seg_hi < qlo) continue;
-      const bool in_window = p.W == 0 || (j + 1) * BN - 1 >= q0 - p.W + 1;
-      if (!in_window && !t.any_sink) continue;
-      out[1 + n++] = j;
+    const int jmax = q1 / BN;
+    for (int j0 = 0; j0 <= jmax; j0 += 32) {
+      const int j = j0 + lane;
+      bool keep = false;
+      if (j <= jmax) {
+        const TileMeta &t = meta[size_t(b) * p.n_kt + j];
+        const bool in_window = p.W == 0 || (j + 1) * BN - 1 >= q0 - p.W + 1;
+        keep = t.seg_lo <= t.seg_hi && t.seg_lo <= qhi && t.seg_hi >= qlo && (in_window || t.any_sink);
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (keep) out[1 + n + __popc(m & ((1u << lane) - 1u))] = j;
+      n += __popc(m);
     }
   }
-  out[0] = n;
+  if (lane == 0) out[0] = n;
 }
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -794,7 +806,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   const int ns = a.batch * pd.n_kt;
   tile_meta_kernel<<<(ns + 3) / 4, 128, 0, stream>>>(a.seg_ids, a.sink, a.T, pd.n_kt, meta, a.batch);
   const int nq = a.batch * pd.n_span;
-  tile_plan_kernel<<<(nq + 127) / 128, 128, 0, stream>>>(meta, p, plan);
+  tile_plan_kernel<<<(nq + 3) / 4, 128, 0, stream>>>(meta, p, plan);
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;

@@ -78,6 +78,79 @@ __global__ void __launch_bounds__(128) rope_kernel(const E *x1, E *y1, int H1, c
   }
 }
 
+// Prefill path: the (cos, sin) table of every position and channel pair is
+// built once per call (double-precision reduction as above), then one thread
+// rotates 8 channel pairs of one (b, t, head) with 16-byte loads and stores.
+__global__ void rope_table_kernel(float2 *cs, int T, int half, Freqs fr) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= T * half) return;
+  cs[idx] = rot_cs(double(idx / half), fr.f[idx % half]);
+}
+
+__device__ __forceinline__ void ld8(const uint16_t *p, float *x) {
+  const uint4 w = *reinterpret_cast<const uint4 *>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16_lo(u[i]);
+    x[2 * i + 1] = bf16_hi(u[i]);
+  }
+}
+__device__ __forceinline__ void st8(uint16_t *p, const float *x) {
+  uint4 w;
+  w.x = pack_bf16x2(x[0], x[1]);
+  w.y = pack_bf16x2(x[2], x[3]);
+  w.z = pack_bf16x2(x[4], x[5]);
+  w.w = pack_bf16x2(x[6], x[7]);
+  *reinterpret_cast<uint4 *>(p) = w;
+}
+__device__ __forceinline__ void ld8(const float *p, float *x) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+  x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+__device__ __forceinline__ void st8(float *p, const float *x) {
+  reinterpret_cast<float4 *>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4 *>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+// item = ((b*T + t) * (H1 + H2) + head) * (D / 16) + group of 8 pairs; heads
+// below H1 come from x1 / y1, the rest from x2 / y2.
+template <typename E>
+__global__ void __launch_bounds__(256) rope_vec_kernel(const E *x1, E *y1, int H1, const E *x2, E *y2,
+                                                       int H2, int T, int D, const float2 *cs,
+                                                       size_t n_items) {
+  const size_t item = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (item >= n_items) return;
+  const int half = D / 2, groups = half / 8;
+  const int i0 = int(item % groups) * 8;
+  const size_t rest = item / groups;
+  const int hh = int(rest % (H1 + H2));
+  const size_t bt = rest / (H1 + H2);
+  const int t = int(bt % T);
+  const bool second = hh >= H1;
+  const E *x = second ? x2 : x1;
+  E *y = second ? y2 : y1;
+  const int H = second ? H2 : H1, h = second ? hh - H1 : hh;
+  const size_t row = (bt * H + h) * D;
+  float a[8], b[8], c[8], s_[8];
+  ld8(x + row + i0, a);
+  ld8(x + row + i0 + half, b);
+  const float4 *t4 = reinterpret_cast<const float4 *>(cs + size_t(t) * half + i0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 w = t4[i];
+    c[2 * i] = w.x, s_[2 * i] = w.y, c[2 * i + 1] = w.z, s_[2 * i + 1] = w.w;
+  }
+  float ya[8], yb[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ya[i] = a[i] * c[i] - b[i] * s_[i];
+    yb[i] = b[i] * c[i] + a[i] * s_[i];
+  }
+  st8(y + row + i0, ya);
+  st8(y + row + i0 + half, yb);
+}
+
 // One CTA per (b, pooled block j): mean of `block` consecutive positions for
 // every head and channel, K rotated at the block midpoint.
 __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint16_t *v,
@@ -139,20 +212,29 @@ cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, i
   return cudaGetLastError();
 }
 
-// Rotate q and k of a prefill into separate output buffers in one launch.
+size_t rope_table_bytes(int T, int head_dim) { return size_t(T) * (head_dim / 2) * sizeof(float2); }
+
+// Rotate q and k of a prefill into separate output buffers: the angle table
+// into `table` (rope_table_bytes), then one vectorised pass over q and k.
+// head_dim must be a multiple of 16.
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
-                           int batch, int T, int head_dim, float theta, bool f32,
+                           int batch, int T, int head_dim, float theta, bool f32, void *table,
                            cudaStream_t stream) {
   if (size_t(batch) * T == 0) return cudaSuccess;
   Freqs fr = make_freqs(head_dim, theta);
+  float2 *cs = static_cast<float2 *>(table);
+  const int half = head_dim / 2;
+  rope_table_kernel<<<(T * half + 255) / 256, 256, 0, stream>>>(cs, T, half, fr);
+  const size_t n = size_t(batch) * T * (Hq + Hkv) * (half / 8);
+  const unsigned grid = unsigned((n + 255) / 256);
   if (f32)
-    rope_kernel<float><<<batch * T, 128, 0, stream>>>(
-        static_cast<const float *>(q), static_cast<float *>(q_out), Hq,
-        static_cast<const float *>(k), static_cast<float *>(k_out), Hkv, T, head_dim, fr);
+    rope_vec_kernel<float><<<grid, 256, 0, stream>>>(
+        static_cast<const float *>(q), static_cast<float *>(q_out), Hq, static_cast<const float *>(k),
+        static_cast<float *>(k_out), Hkv, T, head_dim, cs, n);
   else
-    rope_kernel<uint16_t><<<batch * T, 128, 0, stream>>>(
+    rope_vec_kernel<uint16_t><<<grid, 256, 0, stream>>>(
         static_cast<const uint16_t *>(q), static_cast<uint16_t *>(q_out), Hq,
-        static_cast<const uint16_t *>(k), static_cast<uint16_t *>(k_out), Hkv, T, head_dim, fr);
+        static_cast<const uint16_t *>(k), static_cast<uint16_t *>(k_out), Hkv, T, head_dim, cs, n);
   return cudaGetLastError();
 }
 
