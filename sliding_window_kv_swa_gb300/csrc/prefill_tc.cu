@@ -186,28 +186,69 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
+// One lane of a converged warp, chosen by elect.sync (1 there, 0 elsewhere).
+// The MMA, commit and TMA helpers below take it as a predicate: the whole warp
+// executes them converged and only the elected lane issues.  Issuing tcgen05
+// instructions this way is several times cheaper than from a lane-divergent
+// branch.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t r;
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+      "{\n .reg .pred e;\n .reg .b32 x;\n elect.sync x|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}\n"
+      : "=r"(r));
+  return r;
+}
+
+// tcgen05 MMA, kind::f16 (bf16 operands, fp32 accumulation), A and B from
+// shared memory.
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate, uint32_t leader) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 e, %5, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(leader));
 }
 
 // Same with the A operand (M x K, K-major) read from TMEM.
 __device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
-                                            uint32_t accumulate) {
+                                            uint32_t accumulate, uint32_t leader) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate));
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 e, %5, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate), "r"(leader));
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+__device__ __forceinline__ void mma_commit(uint64_t *bar, uint32_t leader) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
+      "{\n .reg .pred e;\n setp.ne.b32 e, %1, 0;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          smem_u32(bar)),
+      "r"(leader)
       : "memory");
+}
+
+// Packed fp32 pairs (sm_100 family): (o0, o1) = (a0, a1) * b + c with b, c packed.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void fma_f32x2(float &o0, float &o1, float a0, float a1, uint64_t b, uint64_t c) {
+  asm("{\n .reg .b64 a, r;\n mov.b64 a, {%2, %3};\n fma.rn.f32x2 r, a, %4, %5;\n mov.b64 {%0, %1}, r;\n}\n"
+      : "=f"(o0), "=f"(o1)
+      : "f"(a0), "f"(a1), "l"(b), "l"(c));
+}
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void add_f32x2(float &s0, float &s1, float a0, float a1) {
+  asm("{\n .reg .b64 s, a;\n mov.b64 s, {%0, %1};\n mov.b64 a, {%2, %3};\n add.rn.f32x2 s, s, a;\n"
+      " mov.b64 {%0, %1}, s;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -218,11 +259,21 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, int c3, uint64_t *bar) {
+                                            int c2, int c3, uint64_t *bar, uint32_t leader) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      "{\n .reg .pred e;\n setp.ne.b32 e, %7, 0;\n"
+      " @e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];\n}\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
+      "r"(leader)
+      : "memory");
+}
+
+__device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes, uint32_t leader) {
+  asm volatile(
+      "{\n .reg .pred e;\n setp.ne.b32 e, %2, 0;\n"
+      " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(smem_u32(bar)),
+      "r"(bytes), "r"(leader)
       : "memory");
 }
 
@@ -294,6 +345,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
   raise_device_error(err, ND_DEVERR_TIMEOUT);
   *abort_flag = 1;
   return false;
+}
+
+// The same for a whole warp: lane 0 polls, every lane gets the outcome and the
+// warp leaves converged.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err, volatile int *abort_flag) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, err, abort_flag);
+  return __shfl_sync(0xffffffffu, ok, 0);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -407,38 +466,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   Rings: K tiles (NK stages, freed once both blocks' S MMAs read them),
     //   V tiles (NV stages, freed after both blocks' PV) and tile records
     //   (NM stages, freed once all eight softmax warps built their masks).
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(&bar_q, 2 * L::kQ);
+    const uint32_t leader = elect_one();
+    if (n > 0) {
+      expect_tx(&bar_q, 2 * L::kQ, leader);
       for (int x = 0; x < L::kBoxes; ++x) {
-        tma_load_4d(sQ(0) + x * BM * 128, &tm_q, 64 * x, head0, row00, b, &bar_q);
-        tma_load_4d(sQ(1) + x * BM * 128, &tm_q, 64 * x, head1, row01, b, &bar_q);
+        tma_load_4d(sQ(0) + x * BM * 128, &tm_q, 64 * x, head0, row00, b, &bar_q, leader);
+        tma_load_4d(sQ(1) + x * BM * 128, &tm_q, 64 * x, head1, row01, b, &bar_q, leader);
       }
     }
-    // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...  Every
-    // wait blocks in hardware (no polling loop competing for issue slots).
+    // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...  The warp
+    // stays converged; lane 0 waits, the elected lane issues.
     auto load_k = [&](int j) {
       const int e = tiles[j];
       const bool pooled = (e >> 20) & 1;
       const int jt = e & 0xFFFFF;
       const int st = j % NK, sm = j % NM;
-      bool ok = true;
-      if (lane == 0) {
-        ok = (j < NK || wait_or_abort(&k_empty[st], ((j / NK) - 1) & 1, p.err, abort_flag)) &&
-             (j < NM || wait_or_abort(&m_empty[sm], ((j / NM) - 1) & 1, p.err, abort_flag));
-        if (ok) {
-          mbar_arrive_expect_tx(&k_full[st], L::kKV);
-          for (int x = 0; x < L::kBoxes; ++x)
-            tma_load_4d(sK(st) + x * BN * 128, pooled ? &tm_pk : &tm_k, 64 * x, hk, jt * BN, b, &k_full[st]);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) return false;
+      if (!((j < NK || warp_wait(&k_empty[st], ((j / NK) - 1) & 1, p.err, abort_flag)) &&
+            (j < NM || warp_wait(&m_empty[sm], ((j / NM) - 1) & 1, p.err, abort_flag))))
+        return false;
+      expect_tx(&k_full[st], L::kKV, leader);
+      for (int x = 0; x < L::kBoxes; ++x)
+        tma_load_4d(sK(st) + x * BN * 128, pooled ? &tm_pk : &tm_k, 64 * x, hk, jt * BN, b, &k_full[st], leader);
       // the exact tile's record (384 bytes) rides along asynchronously;
       // pooled tiles need none, but every lane still arrives
       constexpr int kChunks = int(sizeof(TileMeta)) / 16;
       if (!pooled && lane < kChunks)
         cp_async16(sM(sm) + lane * 16, reinterpret_cast<const char *>(p.meta + size_t(b) * p.n_kt + jt) + lane * 16);
       cp_async_arrive(&m_full[sm]);
+      __syncwarp();
       return true;
     };
     auto load_v = [&](int j) {
@@ -446,16 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool pooled = (e >> 20) & 1;
       const int jt = e & 0xFFFFF;
       const int st = j % NV;
-      bool ok = true;
-      if (lane == 0) {
-        ok = j < NV || wait_or_abort(&v_empty[st], ((j / NV) - 1) & 1, p.err, abort_flag);
-        if (ok) {
-          mbar_arrive_expect_tx(&v_full[st], L::kKV);
-          for (int x = 0; x < L::kBoxes; ++x)
-            tma_load_4d(sV(st) + x * BN * 128, pooled ? &tm_pv : &tm_v, 64 * x, hk, jt * BN, b, &v_full[st]);
-        }
-      }
-      return __shfl_sync(0xffffffffu, ok, 0);
+      if (!(j < NV || warp_wait(&v_empty[st], ((j / NV) - 1) & 1, p.err, abort_flag))) return false;
+      expect_tx(&v_full[st], L::kKV, leader);
+      for (int x = 0; x < L::kBoxes; ++x)
+        tma_load_4d(sV(st) + x * BN * 128, pooled ? &tm_pv : &tm_v, 64 * x, hk, jt * BN, b, &v_full[st], leader);
+      return true;
     };
     for (int j = 0; j <= n && !fail; ++j) {
       if (j < n && !load_k(j)) fail = true;
@@ -466,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   S(0), S(1); then per tile j, once this block's P(j) is written: O += P V,
     //   and S(j+2) into the same TMEM buffer once that PV has read P(j).
     const int rb = warp - kWarpMma0;
-    if (lane == 0 && n > 0) {
+    const uint32_t leader = elect_one();
+    if (n > 0) {
       constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
       auto issue_s = [&](int j) {
@@ -476,14 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes inside the atom
           const uint64_t a = sdesc_sw128(sQ(rb) + (kk >> 2) * BM * 128 + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
-          mma_bf16(tS(rb, j & 1), a, bd, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16(tS(rb, j & 1), a, bd, kIdS, kk > 0 ? 1u : 0u, leader);
         }
-        mma_commit(&s_full[rb][j & 1]);
-        mma_commit(&k_empty[st]);
+        mma_commit(&s_full[rb][j & 1], leader);
+        mma_commit(&k_empty[st], leader);
       };
-      bool ok = wait_or_abort(&bar_q, 0, p.err, abort_flag);
+      bool ok = warp_wait(&bar_q, 0, p.err, abort_flag);
       for (int j = 0; j < 2 && j < n && ok; ++j) {
-        ok = wait_or_abort(&k_full[j % NK], (j / NK) & 1, p.err, abort_flag);
+        ok = warp_wait(&k_full[j % NK], (j / NK) & 1, p.err, abort_flag);
         if (ok) {
           tc_fence_after();
           issue_s(j);
@@ -491,21 +542,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = 0; j < n && ok; ++j) {
         const int sv = j % NV;
-        ok = wait_or_abort(&p_full[rb], j & 1, p.err, abort_flag) &&
-             wait_or_abort(&v_full[sv], (j / NV) & 1, p.err, abort_flag);
+        ok = warp_wait(&p_full[rb], j & 1, p.err, abort_flag) &&
+             warp_wait(&v_full[sv], (j / NV) & 1, p.err, abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys = 8 TMEM columns of bf16 pairs
           const uint64_t bd = sdesc_sw128(sV(sv) + kk * 16 * 128, BN * 128, 1024);
-          mma_bf16_ts(tO(rb), tS(rb, j & 1) + kk * 8, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tO(rb), tS(rb, j & 1) + kk * 8, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u, leader);
         }
-        mma_commit(&pv_done[rb]);
-        mma_commit(&v_empty[sv]);
+        mma_commit(&pv_done[rb], leader);
+        mma_commit(&v_empty[sv], leader);
         if (j + 2 < n) {
           // S(j+2) overwrites the columns PV(j) reads P(j) from: wait for it
-          ok = wait_or_abort(&pv_done[rb], j & 1, p.err, abort_flag) &&
-               wait_or_abort(&k_full[(j + 2) % NK], ((j + 2) / NK) & 1, p.err, abort_flag);
+          ok = warp_wait(&pv_done[rb], j & 1, p.err, abort_flag) &&
+               warp_wait(&k_full[(j + 2) % NK], ((j + 2) / NK) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
           issue_s(j + 2);
@@ -608,13 +659,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_empty[sm]);  // this warp is done with the tile record
+      // row max: three-input max over 8 independent chains (keys i, i+8, ...,
+      // i+56 on chain i)
+      static_assert(BN == 64, "max chains cover 64 keys");
       float mxp[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mxp[i] = __uint_as_float(v[i]);
+      for (int i = 0; i < 8; ++i)
+        mxp[i] = max3(__uint_as_float(v[i]), __uint_as_float(v[8 + i]), __uint_as_float(v[16 + i]));
 #pragma unroll
-      for (int x = 8; x < BN; ++x) mxp[x & 7] = fmaxf(mxp[x & 7], __uint_as_float(v[x]));
-      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      for (int i = 0; i < 8; ++i) {
+        mxp[i] = max3(mxp[i], __uint_as_float(v[24 + i]), __uint_as_float(v[32 + i]));
+        mxp[i] = max3(mxp[i], __uint_as_float(v[40 + i]), __uint_as_float(v[48 + i]));
+        mxp[i] = fmaxf(mxp[i], __uint_as_float(v[56 + i]));
+      }
+      const float mx = max3(max3(mxp[0], mxp[1], mxp[2]), max3(mxp[3], mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]));
       if (m_used == -INFINITY) m_used = mx;  // nothing accumulated yet: no rescale
       const bool need = mx > m_used && (mx - m_used) * c > kRescaleLog2;
       const float alpha = need ? ex2((m_used - mx) * c) : 1.f;
@@ -623,12 +681,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mx;
       }
       const float mc = m_used == -INFINITY ? 0.f : m_used * c;
+      // p = 2^(s c - m c), two scores per packed fp32 FMA / add
+      const uint64_t c2 = pack_f32x2(c, c), nmc2 = pack_f32x2(-mc, -mc);
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int x = 0; x < BN; ++x) {
-        const float pv = ex2(fmaf(__uint_as_float(v[x]), c, -mc));
-        rsp[x & 3] += pv;
-        v[x] = __float_as_uint(pv);
+      for (int x = 0; x < BN; x += 2) {
+        float a, bb;
+        fma_f32x2(a, bb, __uint_as_float(v[x]), __uint_as_float(v[x + 1]), c2, nmc2);
+        a = ex2(a);
+        bb = ex2(bb);
+        add_f32x2(rsp[(x >> 1) & 1 ? 2 : 0], rsp[(x >> 1) & 1 ? 3 : 1], a, bb);
+        v[x] = __float_as_uint(a);
+        v[x + 1] = __float_as_uint(bb);
       }
       l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       // O is rescaled only after PV(j-1) has landed (rare: the max grew by
@@ -658,6 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[rb]);
     }
     // ---- epilogue: O / l from TMEM
+    //   PV(n-2) may still be in flight here (only PV(n-3) is known to have
+    //   landed: S(n-1) waited for it), so wait for PV(n-2) and then PV(n-1);
+    //   a parity wait on PV(n-1) alone would match PV(n-3)'s phase.
+    if (n > 1 && !fail && !wait_or_abort(&pv_done[rb], (n - 2) & 1, p.err, abort_flag)) fail = true;
     if (n > 0 && !fail && !wait_or_abort(&pv_done[rb], (n - 1) & 1, p.err, abort_flag)) fail = true;
     __syncwarp();
     tc_fence_after();
