@@ -404,6 +404,8 @@ def main():
     ap.add_argument("--impl", default="nd", choices=["nd", "reference"])
     ap.add_argument("--rows", default="all", help="comma list of extra rows: sweep,packed,compressed or none")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--sweep-batches", default="32,64,128,256,512",
+                    help="batch sizes of the large-batch decode sweep (all five = the measured configuration)")
     ap.add_argument("--packed-batch", type=int, default=8,
                     help="sequences in the packed-prefill row (8 = the measured configuration; smaller for profiling)")
     args = ap.parse_args()
@@ -463,7 +465,7 @@ def main():
         {"sweep", "packed", "compressed"} if args.rows == "all" else set())
     if "sweep" in want:
         sweep = {}
-        for Bs in (32, 64, 128, 256, 512):
+        for Bs in [int(x) for x in args.sweep_batches.split(",")]:
             r = bench_decode(torch, nd, Bs, 32, 8, 128, 1024, 256, max(20, steps // 4), warmup,
                              seed=rank_seed(1234 + 4, rank), pk=pk, dist=dist)
             r.pop("_state")

@@ -156,7 +156,9 @@ ND_API int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim,
  * A sequence with no visible key (empty cache) gets out = 0, lse = -inf.
  * Split-K partials go to the workspace, sized by
  * nd_swa_sink_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
- * sink_cap + min(ring_cap, window)); the size may be 0 (no split).
+ * sink_cap + ring_cap); the size may be 0 (no split).  The kernel walks every
+ * physical slot of the cache and masks the ones the metadata marks invisible,
+ * so its loads do not wait for the metadata.
  */
 ND_API size_t nd_swa_sink_decode_workspace_size(int batch, int n_q_heads,
                                                 int n_kv_heads, int head_dim,

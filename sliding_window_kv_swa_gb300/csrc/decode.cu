@@ -123,19 +123,18 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     int sl = c.sink_len[b], rs = c.ring_start[b], rl = c.ring_len[b];
     const bool sane = sl >= 0 && sl <= c.sink_cap && rl >= 0 && rl <= c.ring_cap && rs >= 0 &&
                       (c.ring_cap == 0 || rs < c.ring_cap);
-    int total = 0, rs_eff = 0;
+    int n_vis = 0, rs_eff = 0;
     if (!sane) {
       raise_device_error(p.err, ND_DEVERR_METADATA);
       sl = 0;
     } else {
-      const int n_vis = rl < p.window ? rl : p.window;
+      n_vis = rl < p.window ? rl : p.window;
       const int i0 = rl - n_vis;  // oldest visible ring entry (logical)
       rs_eff = c.ring_cap ? (rs + i0) % c.ring_cap : 0;
-      total = sl + n_vis;
     }
     s_meta[0] = sl;
     s_meta[1] = rs_eff;
-    s_meta[2] = total;
+    s_meta[2] = n_vis;
   }
 
   // ---- q fragments while the metadata read is in flight.  Thread t owns
@@ -169,18 +168,12 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       }
     }
   }
-  __syncthreads();
-  const int sink_len = s_meta[0], rs_eff = s_meta[1], total = s_meta[2];
+  // The CTA walks physical slots [v_begin, v_end) of the pair -- sink region,
+  // then ring -- in storage order: the softmax does not depend on slot order,
+  // so the copies start before the metadata read lands, and the metadata only
+  // masks slots that are not visible.
   const int v_begin = split * p.slots_per_cta;
-  const int v_end = min(v_begin + p.slots_per_cta, total);
-
-  // virtual visible index -> physical slot
-  auto phys = [&](int v) -> int {
-    if (v < sink_len) return v;
-    int r = rs_eff + (v - sink_len);
-    if (r >= c.ring_cap) r -= c.ring_cap;
-    return c.sink_cap + r;
-  };
+  const int v_end = min(v_begin + p.slots_per_cta, nslot);
 
   const int8_t *kc = c.k_codes + pair * nslot * D;
   const int8_t *vc = c.v_codes + pair * nslot * D;
@@ -205,7 +198,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       for (int i = lane; i < kChunks; i += 32) {
         const int row = i / (D / 16), ch = i % (D / 16);
         const int v = base + row;
-        const int ps = phys(v < v_end ? v : base);
+        const int ps = v < v_end ? v : base;
         const uint32_t off = swz(uint32_t(row * D + ch * 16));
         cp_async16(st + off, kc + size_t(ps) * D + ch * 16);
         cp_async16(st + S::kCodes + off, vc + size_t(ps) * D + ch * 16);
@@ -213,7 +206,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       {
         const int row = lane & 15, which = lane >> 4;
         const int v = base + row;
-        const int ps = phys(v < v_end ? v : base);
+        const int ps = v < v_end ? v : base;
         const uint32_t dst = st + 2 * S::kCodes + which * S::kScales + row * NG * 4;
         const float *src = (which ? vs : ks) + size_t(ps) * NG;
         if constexpr (NG == 4) cp_async16(dst, src);
@@ -225,6 +218,16 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
 
 #pragma unroll
   for (int n = 0; n < kStages - 1; ++n) issue(n);
+  __syncthreads();  // the metadata is in
+  const int sink_len = s_meta[0], rs_eff = s_meta[1], n_vis = s_meta[2];
+  // visible: a filled sink slot, or a ring slot inside the window's arc
+  auto visible = [&](int ps) -> bool {
+    if (ps >= v_end) return false;
+    if (ps < c.sink_cap) return ps < sink_len;
+    int d = ps - c.sink_cap - rs_eff;
+    if (d < 0) d += c.ring_cap;
+    return d < n_vis;
+  };
 
   float o[NG][2][4];
 #pragma unroll
@@ -245,6 +248,9 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     const int base = base_of(n);
     const uint32_t st = my_stages + (n % kStages) * S::kBytes;
     const int col[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    bool vis[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vis[i] = visible(base + col[i]);
 
     // ---- QK: scores for head g at columns 2t, 2t+1 of tiles 0 and 1
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -269,7 +275,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      sc[i] = (base + col[i] < v_end && g < G) ? sc[i] * head_coef : -INFINITY;
+      sc[i] = (vis[i] && g < G) ? sc[i] * head_coef : -INFINITY;
       mx = fmaxf(mx, sc[i]);
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         vsc[i] = ldsf(st + 2 * S::kCodes + S::kScales + col[i] * NG * 4 + grp * 4);
-        vm = fmaxf(vm, base + col[i] < v_end ? vsc[i] : 0.f);
+        vm = fmaxf(vm, vis[i] ? vsc[i] : 0.f);
       }
       vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
       vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
@@ -314,8 +320,9 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
         o[grp][tt][3] *= f_hi;
       }
       const float u = exp2i(e_acc[grp]);
-      const uint32_t b0 = pack_half2(pr[0] * (vsc[0] * u), pr[1] * (vsc[1] * u));
-      const uint32_t b1 = pack_half2(pr[2] * (vsc[2] * u), pr[3] * (vsc[3] * u));
+      // masked slots contribute 0 (their scale may be anything, even non-finite)
+      const uint32_t b0 = pack_half2(vis[0] ? pr[0] * (vsc[0] * u) : 0.f, vis[1] ? pr[1] * (vsc[1] * u) : 0.f);
+      const uint32_t b1 = pack_half2(vis[2] ? pr[2] * (vsc[2] * u) : 0.f, vis[3] ? pr[3] * (vsc[3] * u) : 0.f);
       uint32_t vw[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -473,7 +480,7 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_sl
 cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, int window,
                           void *out, float *lse, void *ws, size_t ws_bytes, int *err,
                           cudaStream_t stream) {
-  const int max_slots = c.sink_cap + (c.ring_cap < window ? c.ring_cap : window);
+  const int max_slots = c.sink_cap + c.ring_cap;  // every physical slot is walked
   DecodePlan pl = plan_decode(c.batch, c.n_kv_heads, max_slots, c.head_dim);
   DecodeParams p;
   p.q = static_cast<const uint16_t *>(q);

@@ -56,9 +56,8 @@ extern "C" int nd_swa_sink_decode_noalloc(const void *q, const nd_kv_cache *cach
   if (!cache || window < 1 || n_q_heads <= 0 || cache->n_kv_heads <= 0 || cache->batch < 0)
     return ND_ERR_INVALID_ARG;
   if (cache->batch == 0) return ND_OK;
-  const int ring = cache->ring_cap < window ? cache->ring_cap : window;
   const size_t need = nd_swa_sink_decode_workspace_size(cache->batch, n_q_heads, cache->n_kv_heads,
-                                                        cache->head_dim, cache->sink_cap + ring);
+                                                        cache->head_dim, cache->sink_cap + cache->ring_cap);
   if (need > ND_NOALLOC_SCRATCH_BYTES) return ND_ERR_WORKSPACE;
   void *scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) {

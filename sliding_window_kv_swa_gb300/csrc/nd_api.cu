@@ -173,7 +173,7 @@ int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, i
   if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
   if (cache->batch == 0) return ND_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
-  const int max_slots = cache->sink_cap + (cache->ring_cap < window ? cache->ring_cap : window);
+  const int max_slots = cache->sink_cap + cache->ring_cap;  // every physical slot is walked
   if (max_slots <= 0) return ND_ERR_INVALID_ARG;
   DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim);
   if (pl.n_split > 1) {

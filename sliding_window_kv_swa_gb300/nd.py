@@ -213,7 +213,7 @@ def nd_swa_sink_decode(q: torch.Tensor, cache: KVCache, window: int, out: Option
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        max_slots = cache.sink_cap + min(cache.ring_cap, window)
+        max_slots = cache.sink_cap + cache.ring_cap
         nbytes = nd_swa_sink_decode_workspace_size(B, Hq, cache.n_kv_heads, d, max_slots)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     s = cache.struct()
