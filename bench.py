@@ -253,9 +253,10 @@ def bench_decode(torch, nd, B, Hq, Hkv, d, S, W, steps, warmup, seed, pk, dist=N
 
     def step(i):
         r = reps[i % replicas]
-        if with_append:
-            nd.nd_kv_append_quant(r["cache"], r["kn"], r["vn"], False)
-        nd.nd_swa_sink_decode(r["q"], r["cache"], W, out=r["out"], workspace=ws)
+        if with_append:   # one decode step: append the current token, attend with it
+            nd.nd_swa_sink_decode_step(r["q"], r["cache"], r["kn"], r["vn"], W, out=r["out"], workspace=ws)
+        else:
+            nd.nd_swa_sink_decode(r["q"], r["cache"], W, out=r["out"], workspace=ws)
 
     def decode_only(i):
         r = reps[i % replicas]
@@ -265,14 +266,23 @@ def bench_decode(torch, nd, B, Hq, Hkv, d, S, W, steps, warmup, seed, pk, dist=N
     ms_kernel = time_graph(torch, decode_only, steps, warmup, dist)
     step_bytes = cache_b + qo_b + (app_b if with_append else 0)
     split = nd.nd_swa_sink_decode_workspace_size(B, Hq, Hkv, d, S + W) > 0
-    launches_per_step = (1 if with_append else 0) + (2 if split else 1)
-    kernel_gbs = (cache_b + qo_b) / (ms_kernel / steps * 1e-3) / 1e9
+    # unsplit with at most 4 KV heads, a sequence's CTAs form one small cluster
+    # and the step is a single fused launch (the library's rule); otherwise the
+    # append is its own launch and a split decode adds its combine launch
+    fused = with_append and not split and Hkv <= 4
+    launches_per_step = 1 if fused else (1 if with_append else 0) + (2 if split else 1)
+    step_gbs = step_bytes / (ms / steps * 1e-3) / 1e9
+    decode_gbs = (cache_b + qo_b) / (ms_kernel / steps * 1e-3) / 1e9
+    if fused:   # the dominant (only) kernel of the step is the fused one
+        kernel = dict(name="decode_kernel (nd_swa_sink_decode_step: fused append + decode)",
+                      ms_per_launch=ms / steps, bytes_per_launch=step_bytes, gbs=step_gbs, frac=step_gbs / pk["hbm"])
+    else:
+        kernel = dict(name="decode_kernel (nd_swa_sink_decode)", ms_per_launch=ms_kernel / steps,
+                      bytes_per_launch=cache_b + qo_b, gbs=decode_gbs, frac=decode_gbs / pk["hbm"])
+    kernel["decode_only"] = dict(ms_per_launch=ms_kernel / steps, bytes_per_launch=cache_b + qo_b, gbs=decode_gbs)
     return dict(
-        ms_per_step=ms / steps, gbs=step_bytes / (ms / steps * 1e-3) / 1e9, bytes_per_step=step_bytes,
-        replicas=replicas, launches=launches_per_step * steps,
-        kernel=dict(name="nd_swa_sink_decode", ms_per_launch=ms_kernel / steps, bytes_per_launch=cache_b + qo_b,
-                    gbs=kernel_gbs, frac=kernel_gbs / pk["hbm"]),
-        _state=(reps, ws))
+        ms_per_step=ms / steps, gbs=step_gbs, bytes_per_step=step_bytes,
+        replicas=replicas, launches=launches_per_step * steps, kernel=kernel, _state=(reps, ws))
 
 
 def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
@@ -348,8 +358,7 @@ def e2e_decode(torch, nd, state, B, Hq, Hkv, d, S, W, steps, warmup):
         r["q"].copy_(qh[i], non_blocking=True)
         r["kn"].copy_(kh[i], non_blocking=True)
         r["vn"].copy_(vh[i], non_blocking=True)
-        nd.nd_kv_append_quant(r["cache"], r["kn"], r["vn"], False)
-        nd.nd_swa_sink_decode(r["q"], r["cache"], W, out=r["out"], workspace=ws)
+        nd.nd_swa_sink_decode_step(r["q"], r["cache"], r["kn"], r["vn"], W, out=r["out"], workspace=ws)
         oh[i].copy_(r["out"], non_blocking=True)
 
     for i in range(warmup):
@@ -486,7 +495,7 @@ def main():
     traffic = None
     try:
         tr = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-        traffic = tr.get("nd_swa_sink_decode@decode_b64")
+        traffic = tr.get("decode_step@decode_b64") if "fused" in k["name"] else tr.get("decode@decode_b64")
     except Exception:
         pass
     line = {

@@ -168,6 +168,23 @@ ND_API int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_h
                        size_t workspace_bytes, nd_stream_t stream);
 
 /*
+ * One whole decode step: ring-append the current token (exactly as
+ * nd_kv_append_quant with to_sink = 0) and attend with it (exactly as
+ * nd_swa_sink_decode afterwards).  When a sequence's CTAs form a small
+ * thread-block cluster (at most 4 of them: n_kv_heads x the split the decode
+ * would use) both happen in one launch: the CTA that owns the new slot
+ * quantises the token, writes it to the cache and uses it directly, and the
+ * sequence's metadata is advanced after all of its CTAs have read it.
+ * Otherwise the call makes the two launches itself.  Same arguments, layouts,
+ * workspace and errors as the two calls; requires ring_cap > 0.
+ *   k_new, v_new  bf16 [batch][n_kv_heads][head_dim]
+ */
+ND_API int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache,
+                                   const void *k_new, const void *v_new, int n_q_heads,
+                                   int window, void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, nd_stream_t stream);
+
+/*
  * nd_swa_sink_decode without a workspace argument.  The pages have no
  * counterpart: this is a library convenience for callers that cannot
  * allocate device memory -- a thread recording a CUDA graph with a frozen

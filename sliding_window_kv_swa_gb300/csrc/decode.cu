@@ -40,6 +40,9 @@ namespace {
 constexpr int kStep = 16;    // slots per warp step (one MMA k-step)
 constexpr int kStages = 4;   // copies in flight per warp: kStages - 1 steps ahead
 constexpr int kTargetCtas = 152;
+// Largest cluster the fused step uses.  Clusters are co-scheduled on one GPC;
+// at 8 CTAs that costs the large-batch step more than the saved launch.
+constexpr int kMaxFusedCluster = 4;
 
 struct DecodeParams {
   const uint16_t *q;
@@ -51,7 +54,50 @@ struct DecodeParams {
   float *ws_ml;  // [B*Hkv][n_split][G][2]   (m in log2 units, l)
   float *ws_o;   // [B*Hkv][n_split][G][D]
   int *err;
+  // fused step: the current token, appended to the ring before attending
+  // (NULL: plain decode).  The launch is then a thread-block cluster over one
+  // sequence's (split, KV head) CTAs.
+  const uint16_t *k_new, *v_new;
 };
+
+// Cluster barrier halves: every thread arrives once it no longer needs the
+// sequence's cache metadata; a wait returns once every non-exited thread of
+// the cluster has arrived.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Quantise one bf16 row of D channels held by a full warp (lane l has
+// channels [l*CPL, l*CPL + CPL)) with the cache codec -- scale = amax/127,
+// code = clamp(rint(x/scale), +-127), IEEE fp32 divides -- the same
+// arithmetic as the append kernel, so the codes agree bit for bit.
+template <int D>
+__device__ __forceinline__ void quant_row_regs(const uint16_t *src, int lane, int *code, float &scale) {
+  constexpr int CPL = D / 32, kLanesPerGroup = 32 / CPL;
+  float x[CPL];
+  if constexpr (CPL == 4) {
+    const uint2 w = reinterpret_cast<const uint2 *>(src)[lane];
+    x[0] = bf16_lo(w.x), x[1] = bf16_hi(w.x), x[2] = bf16_lo(w.y), x[3] = bf16_hi(w.y);
+  } else {
+    const uint32_t w = reinterpret_cast<const uint32_t *>(src)[lane];
+    x[0] = bf16_lo(w), x[1] = bf16_hi(w);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int off = kLanesPerGroup / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    float r = 0.f;
+    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    code[i] = int(r);
+  }
+}
 
 template <int D>
 struct Stage {
@@ -109,7 +155,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
   constexpr int NG = D / 32;  // scale groups per row
   using S = Stage<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ int s_meta[4];
+  __shared__ int s_meta[8];
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,15 +165,26 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
   const int nslot = c.sink_cap + c.ring_cap;
   const size_t pair = size_t(b) * c.n_kv_heads + hkv;
 
+  const bool fused = p.k_new != nullptr;
   if (threadIdx.x == 0) {
     int sl = c.sink_len[b], rs = c.ring_start[b], rl = c.ring_len[b];
     const bool sane = sl >= 0 && sl <= c.sink_cap && rl >= 0 && rl <= c.ring_cap && rs >= 0 &&
                       (c.ring_cap == 0 || rs < c.ring_cap);
-    int n_vis = 0, rs_eff = 0;
+    int n_vis = 0, rs_eff = 0, new_slot = -1;
     if (!sane) {
       raise_device_error(p.err, ND_DEVERR_METADATA);
       sl = 0;
     } else {
+      if (fused) {
+        // ring append of the current token: the slot after the newest, or
+        // the oldest one (which advances the ring start) when the ring is full
+        new_slot = c.sink_cap + (rl < c.ring_cap ? (rs + rl) % c.ring_cap : rs);
+        if (rl == c.ring_cap) rs = (rs + 1) % c.ring_cap;
+        else ++rl;
+        s_meta[4] = rs;
+        s_meta[5] = rl;
+        s_meta[6] = c.seq_len[b] + 1;
+      }
       n_vis = rl < p.window ? rl : p.window;
       const int i0 = rl - n_vis;  // oldest visible ring entry (logical)
       rs_eff = c.ring_cap ? (rs + i0) % c.ring_cap : 0;
@@ -135,6 +192,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     s_meta[0] = sl;
     s_meta[1] = rs_eff;
     s_meta[2] = n_vis;
+    s_meta[3] = new_slot;
   }
 
   // ---- q fragments while the metadata read is in flight.  Thread t owns
@@ -219,7 +277,8 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
 #pragma unroll
   for (int n = 0; n < kStages - 1; ++n) issue(n);
   __syncthreads();  // the metadata is in
-  const int sink_len = s_meta[0], rs_eff = s_meta[1], n_vis = s_meta[2];
+  const int sink_len = s_meta[0], rs_eff = s_meta[1], n_vis = s_meta[2], new_slot = s_meta[3];
+  if (fused) cluster_arrive();  // this CTA is done reading the sequence's metadata
   // visible: a filled sink slot, or a ring slot inside the window's arc
   auto visible = [&](int ps) -> bool {
     if (ps >= v_end) return false;
@@ -247,6 +306,40 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     __syncwarp();
     const int base = base_of(n);
     const uint32_t st = my_stages + (n % kStages) * S::kBytes;
+    if (fused && new_slot >= base && new_slot < base + kStep && new_slot < v_end) {
+      // this warp owns the appended slot: quantise the token, store it in the
+      // cache, and put it into the stage over the stale copy
+      const int row = new_slot - base;
+      constexpr int CPL = D / 32, kLanesPerGroup = 32 / CPL;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        int code[CPL];
+        float scale;
+        quant_row_regs<D>((which ? p.v_new : p.k_new) + pair * D, lane, code, scale);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) packed |= uint32_t(code[i] & 0xff) << (8 * i);
+        int8_t *gcodes = (which ? c.v_codes : c.k_codes) + (pair * nslot + new_slot) * D;
+        float *gscale = (which ? c.v_scale : c.k_scale) + (pair * nslot + new_slot) * NG;
+        const uint32_t scodes = st + which * S::kCodes + swz(uint32_t(row * D + lane * CPL));
+        if constexpr (CPL == 4) {
+          reinterpret_cast<uint32_t *>(gcodes)[lane] = packed;
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(scodes), "r"(packed) : "memory");
+        } else {
+          reinterpret_cast<uint16_t *>(gcodes)[lane] = uint16_t(packed);
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(scodes), "h"(uint16_t(packed)) : "memory");
+        }
+        if (lane % kLanesPerGroup == 0) {
+          const int grp = lane / kLanesPerGroup;
+          gscale[grp] = scale;
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(st + 2 * S::kCodes + which * S::kScales +
+                                                       (row * NG + grp) * 4),
+                       "f"(scale)
+                       : "memory");
+        }
+      }
+      __syncwarp();
+    }
     const int col[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
     bool vis[4];
 #pragma unroll
@@ -398,6 +491,17 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       }
     }
   }
+  if (fused && split == 0 && hkv == 0) {
+    // the cluster barrier completes once every CTA of the sequence has read
+    // its metadata (threads that have exited count as arrived); then the first
+    // CTA publishes the appended state.  The others leave without waiting.
+    cluster_wait();
+    if (threadIdx.x == 0 && new_slot >= 0) {
+      c.ring_start[b] = s_meta[4];
+      c.ring_len[b] = s_meta[5];
+      c.seq_len[b] = s_meta[6];
+    }
+  }
 }
 
 // Merge the split-K partials of one (sequence, query head) per block.
@@ -443,7 +547,25 @@ cudaError_t launch_d(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
   auto kern = decode_kernel<D, NW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, NW * 32, smem, stream>>>(p);
+  if (p.k_new) {
+    // one cluster per sequence: its (split, KV head) CTAs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = grid.y;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
+  } else {
+    kern<<<grid, NW * 32, smem, stream>>>(p);
+  }
   if (p.n_split > 1) decode_combine_kernel<D><<<p.c.batch * p.Hq, D, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -471,6 +593,10 @@ DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots, int head_dim) {
   return pl;
 }
 
+bool decode_step_fuses(int batch, int n_kv_heads, int max_slots, int head_dim) {
+  return plan_decode(batch, n_kv_heads, max_slots, head_dim).n_split * n_kv_heads <= kMaxFusedCluster;
+}
+
 size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_slots, int n_kv_heads) {
   DecodePlan pl = plan_decode(batch, n_kv_heads, max_slots, head_dim);
   if (pl.n_split <= 1) return 0;
@@ -479,7 +605,7 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_sl
 
 cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, int window,
                           void *out, float *lse, void *ws, size_t ws_bytes, int *err,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const void *k_new, const void *v_new) {
   const int max_slots = c.sink_cap + c.ring_cap;  // every physical slot is walked
   DecodePlan pl = plan_decode(c.batch, c.n_kv_heads, max_slots, c.head_dim);
   DecodeParams p;
@@ -495,6 +621,9 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
   p.ws_ml = nullptr;
   p.ws_o = nullptr;
   p.err = err;
+  p.k_new = static_cast<const uint16_t *>(k_new);
+  p.v_new = static_cast<const uint16_t *>(v_new);
+  if (k_new && pl.n_split * c.n_kv_heads > kMaxFusedCluster) return cudaErrorInvalidConfiguration;
   if (pl.n_split > 1) {
     const size_t parts = size_t(c.batch) * n_q_heads * pl.n_split;
     if (ws == nullptr || ws_bytes < parts * (c.head_dim + 2) * sizeof(float))

@@ -185,6 +185,36 @@ int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, i
                               device_error_word(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache, const void *k_new,
+                            const void *v_new, int n_q_heads, int window, void *out, float *lse,
+                            void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return ND_ERR_INVALID_ARG;
+  const int G = n_q_heads / cache->n_kv_heads;
+  if (G > 8) return ND_ERR_UNSUPPORTED;
+  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
+  if (cache->ring_cap <= 0) return ND_ERR_INVALID_ARG;
+  if (cache->batch == 0) return ND_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ND_ERR_INVALID_ARG;
+  const int max_slots = cache->sink_cap + cache->ring_cap;
+  DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim);
+  if (pl.n_split > 1) {
+    size_t need = size_t(cache->batch) * n_q_heads * pl.n_split * (cache->head_dim + 2) * sizeof(float);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ND_ERR_WORKSPACE;
+  }
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int *err = device_error_word();
+  if (decode_step_fuses(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim))
+    return finish(launch_decode(q, *cache, n_q_heads, window, out, lse, workspace, workspace_bytes, err, s,
+                                k_new, v_new));
+  cudaError_t e = launch_kv_append_quant(*cache, k_new, v_new, 0, err, s);
+  if (e != cudaSuccess) return finish(e);
+  return finish(launch_decode(q, *cache, n_q_heads, window, out, lse, workspace, workspace_bytes, err, s));
+}
+
 size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,
                                           int n_kv_heads, int head_dim, float rope_theta,
                                           int block) {

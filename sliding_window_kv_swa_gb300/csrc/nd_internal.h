@@ -28,9 +28,16 @@ struct DecodePlan {
 DecodePlan plan_decode(int batch, int n_kv_heads, int max_slots, int head_dim);
 size_t decode_workspace_bytes(int batch, int n_q_heads, int head_dim, int max_slots,
                               int n_kv_heads_hint);
+// k_new / v_new non-NULL: fused step (ring append of the current token, then
+// attention with it) in one clustered launch; cudaErrorInvalidConfiguration
+// when the sequence's CTAs make a cluster larger than the fused step uses
+// (decode_step_fuses() says which; the caller then appends and decodes in two
+// launches).
 cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, int window,
                           void *out, float *lse, void *ws, size_t ws_bytes, int *err,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const void *k_new = nullptr,
+                          const void *v_new = nullptr);
+bool decode_step_fuses(int batch, int n_kv_heads, int max_slots, int head_dim);
 
 cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                         float theta, cudaStream_t stream);

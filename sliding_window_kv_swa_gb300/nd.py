@@ -70,6 +70,7 @@ def _lib():
             "nd_swa_sink_decode_workspace_size": (S, [I, I, I, I, I]),
             "nd_swa_sink_decode": (I, [P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_decode_noalloc": (I, [P, P, I, I, P, P, P]),
+            "nd_swa_sink_decode_step": (I, [P, P, P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
@@ -91,7 +92,8 @@ def library_path() -> str:
 
 EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_errors",
             "nd_kv_append_quant", "nd_kv_quant_rows", "nd_swa_sink_decode_workspace_size",
-            "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_prefill_workspace_size",
+            "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_decode_step",
+            "nd_swa_sink_prefill_workspace_size",
             "nd_swa_sink_prefill",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
 
@@ -220,6 +222,25 @@ def nd_swa_sink_decode(q: torch.Tensor, cache: KVCache, window: int, out: Option
     _check("nd_swa_sink_decode", _lib().nd_swa_sink_decode(
         _ptr(q), ctypes.byref(s), Hq, int(window), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+    return out
+
+
+def nd_swa_sink_decode_step(q: torch.Tensor, cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                            window: int, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Ring-append the current token (k_new, v_new: bf16 [B][Hkv][d]) and
+    attend with it: nd_kv_append_quant(to_sink=False) + nd_swa_sink_decode,
+    in one launch when the sequence's CTAs fit a thread-block cluster."""
+    B, Hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = nd_swa_sink_decode_workspace_size(B, Hq, cache.n_kv_heads, d, cache.sink_cap + cache.ring_cap)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    s = cache.struct()
+    _check("nd_swa_sink_decode_step", _lib().nd_swa_sink_decode_step(
+        _ptr(q), ctypes.byref(s), _ptr(k_new), _ptr(v_new), Hq, int(window), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -220,3 +220,42 @@ def test_append_then_decode_step():
         want, _ = oracle.decode(qf, ref, W)
         assert_close_bf16(host(out), want, f"step {step}")
     np.testing.assert_array_equal(host(cache.k_codes), ref.k_codes)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,S,W,fill", [
+    (10, 32, 8, 128, 64, 32, "full"),    # 8 KV heads: append and decode as two launches
+    (20, 16, 4, 128, 64, 32, "full"),    # one cluster of 4 KV heads per sequence: fused
+    (64, 8, 2, 64, 64, 256, "full"),     # the decode-step configuration: fused
+    (5, 4, 1, 64, 24, 40, "partial"),    # rings still filling, then wrapping
+    (1, 16, 8, 128, 64, 192, "partial"),  # one sequence: 4-way split x 8 KV heads, two launches
+])
+def test_decode_step_matches_append_then_decode(B, Hq, Hkv, d, S, W, fill):
+    """nd_swa_sink_decode_step (append the token, then attend with it) against
+    the oracle's append followed by its decode: output within the bf16
+    tolerance; codes, scales and metadata bit-exact after every step."""
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=700 + B + d, full=(fill == "full"))
+    ref = oracle_cache(w, S, W)
+    if fill == "partial":
+        ref.ring_len[:] = np.arange(B) % 3
+        ref.ring_start[:] = 0
+        ref.seq_len[:] = ref.sink_len + ref.ring_len
+    cache = device_cache(ref)
+    rng = philox(701 + B)
+    steps = W + 3 if fill == "partial" else 3
+    for step in range(steps):
+        kb, kf = normal_bf16(rng, (B, Hkv, d))
+        vb, vf = normal_bf16(rng, (B, Hkv, d))
+        qb, qf = normal_bf16(rng, (B, Hq, d))
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        out = nd().nd_swa_sink_decode_step(dev_bf16(qb), cache, dev_bf16(kb), dev_bf16(vb), W, lse=lse)
+        oracle.kv_append(ref, kf, vf, False)
+        if step % 7 == 0 or step == steps - 1:
+            want, wlse = oracle.decode(qf, ref, W)
+            assert_close_bf16(host(out), want, f"step {step}")
+            np.testing.assert_allclose(host(lse), wlse, atol=2e-3, rtol=0)
+            for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
+                np.testing.assert_array_equal(host(getattr(cache, f)), getattr(ref, f), err_msg=f)
+    np.testing.assert_array_equal(host(cache.k_codes), ref.k_codes)
+    np.testing.assert_array_equal(host(cache.v_codes), ref.v_codes)
+    np.testing.assert_array_equal(host(cache.k_scale), ref.k_scale)
+    np.testing.assert_array_equal(host(cache.v_scale), ref.v_scale)
