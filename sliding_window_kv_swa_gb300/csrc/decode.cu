@@ -40,6 +40,7 @@ namespace {
 constexpr int kStep = 16;    // slots per warp step (one MMA k-step)
 constexpr int kStages = 4;   // copies in flight per warp: kStages - 1 steps ahead
 constexpr int kTargetCtas = 152;
+constexpr float kLazyLog2 = 8.f;  // p is taken against a max at most 2^8 below the true one
 // Largest cluster the fused step uses.  Clusters are co-scheduled on one GPC;
 // at 8 CTAs that costs the large-batch step more than the saved launch.
 constexpr int kMaxFusedCluster = 4;
@@ -247,19 +248,22 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
   // Every lane copies its share of one step: 16-byte chunks of K and V codes
   // and one scale row (K or V) of one slot.  One commit group per step
   // (empty past the end) keeps the group count uniform.
+  // this lane's 16-byte chunks of a step: rows lane/(D/16) + k*(32*16/D),
+  // column chunk lane % (D/16); fixed for every step
+  constexpr int kChunks = kStep * D / 16, kPerLane = kChunks / 32, kRowStride = 32 * 16 / D;
+  const int my_row0 = lane / (D / 16), my_ch = lane % (D / 16);
   auto issue = [&](int n) {
     if (n < n_steps) {
       const int base = base_of(n);
       const uint32_t st = my_stages + (n % kStages) * S::kBytes;
-      constexpr int kChunks = kStep * D / 16;
 #pragma unroll
-      for (int i = lane; i < kChunks; i += 32) {
-        const int row = i / (D / 16), ch = i % (D / 16);
-        const int v = base + row;
-        const int ps = v < v_end ? v : base;
-        const uint32_t off = swz(uint32_t(row * D + ch * 16));
-        cp_async16(st + off, kc + size_t(ps) * D + ch * 16);
-        cp_async16(st + S::kCodes + off, vc + size_t(ps) * D + ch * 16);
+      for (int k = 0; k < kPerLane; ++k) {
+        const int row = my_row0 + k * kRowStride;
+        const int ps = base + row < v_end ? base + row : base;
+        const uint32_t off = swz(uint32_t(row * D + my_ch * 16));
+        const size_t goff = size_t(ps) * D + my_ch * 16;
+        cp_async16(st + off, kc + goff);
+        cp_async16(st + S::kCodes + off, vc + goff);
       }
       {
         const int row = lane & 15, which = lane >> 4;
@@ -295,10 +299,8 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[grp][tt][i] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  int e_acc[NG];  // power-of-two pre-scale of P' per group (never increases; 127 = unset)
-#pragma unroll
-  for (int grp = 0; grp < NG; ++grp) e_acc[grp] = 127;
+  float m_run = -INFINITY, l_run = 0.f;  // m_run: the max p is taken against (log2 units)
+  int e_acc = 127;  // power-of-two pre-scale of P' (never increases; 127 = unset)
 
   for (int n = 0; n < n_steps; ++n) {
     issue(n + kStages - 1);
@@ -341,9 +343,13 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       __syncwarp();
     }
     const int col[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    // whole step visible (a filled sink run, or a full ring) -- the common
+    // case -- or per slot
+    const bool all_vis = base + kStep <= v_end &&
+                         (base + kStep <= sink_len || (base >= c.sink_cap && n_vis == c.ring_cap));
     bool vis[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) vis[i] = visible(base + col[i]);
+    for (int i = 0; i < 4; ++i) vis[i] = all_vis || visible(base + col[i]);
 
     // ---- QK: scores for head g at columns 2t, 2t+1 of tiles 0 and 1
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -373,49 +379,60 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
+    // lazy max: p is taken against m_run, which moves (and O is rescaled)
+    // only when a score exceeds it by more than 2^kLazyLog2, so p <= 2^8
+    const bool need = mx > m_run + kLazyLog2;
+    const float m_new = need ? mx : m_run;
+    const float alpha = need ? (m_run == -INFINITY ? 0.f : ex2(m_run - m_new)) : 1.f;
     float pr[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) pr[i] = (m_new == -INFINITY) ? 0.f : ex2(sc[i] - m_new);
     l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
     m_run = m_new;
-    // this thread's O columns are heads 2t and 2t+1
-    const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
-    const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
+    // V scales of the step, and one exponent for all groups that keeps
+    // p * v_scale * 2^e below 2^15 (p <= 2^8); the accumulator keeps the
+    // smallest exponent seen so far
+    float vsc[NG][4];
+    float vm = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        vsc[grp][i] = ldsf(st + 2 * S::kCodes + S::kScales + col[i] * NG * 4 + grp * 4);
+        vm = fmaxf(vm, vis[i] ? vsc[grp][i] : 0.f);
+      }
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
+    const int e_step = vm > 0.f ? 14 - int(kLazyLog2) - ilog2_floor(vm) : 127;
+    const bool shrink_e = e_step < e_acc;
+    // rescale O (this thread's columns are heads 2t and 2t+1) only when a
+    // head's max moved or the exponent shrank: warp-uniform, and rare
+    if (__any_sync(0xffffffffu, need || shrink_e)) {
+      const float shrink = shrink_e ? (e_acc == 127 ? 0.f : exp2i(e_step - e_acc)) : 1.f;
+      const float f_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4) * shrink;
+      const float f_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4) * shrink;
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp)
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          o[grp][tt][0] *= f_lo;
+          o[grp][tt][1] *= f_hi;
+          o[grp][tt][2] *= f_lo;
+          o[grp][tt][3] *= f_hi;
+        }
+      if (shrink_e) e_acc = e_step;
+    }
+    // (while no scale has been seen, every visible scale is 0 and u is moot)
+    const float u = e_acc == 127 ? 1.f : exp2i(e_acc);
+    float pu[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pu[i] = vis[i] ? pr[i] * u : 0.f;
     // ---- PV per group: B = P'^T (slot x head), A = V^T (channel x slot)
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
-      float vsc[4];
-      float vm = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        vsc[i] = ldsf(st + 2 * S::kCodes + S::kScales + col[i] * NG * 4 + grp * 4);
-        vm = fmaxf(vm, vis[i] ? vsc[i] : 0.f);
-      }
-      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
-      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
-      // exponent that keeps p * v_scale * 2^e below 2^15 for this step; the
-      // accumulator keeps the smallest exponent seen so far (warp-uniform)
-      const int e_step = vm > 0.f ? 14 - ilog2_floor(vm) : 127;
-      float f_lo = a_lo, f_hi = a_hi;
-      if (e_step < e_acc[grp]) {
-        const float shrink = e_acc[grp] == 127 ? 0.f : exp2i(e_step - e_acc[grp]);
-        f_lo *= shrink;
-        f_hi *= shrink;
-        e_acc[grp] = e_step;
-      }
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        o[grp][tt][0] *= f_lo;
-        o[grp][tt][1] *= f_hi;
-        o[grp][tt][2] *= f_lo;
-        o[grp][tt][3] *= f_hi;
-      }
-      const float u = exp2i(e_acc[grp]);
       // masked slots contribute 0 (their scale may be anything, even non-finite)
-      const uint32_t b0 = pack_half2(vis[0] ? pr[0] * (vsc[0] * u) : 0.f, vis[1] ? pr[1] * (vsc[1] * u) : 0.f);
-      const uint32_t b1 = pack_half2(vis[2] ? pr[2] * (vsc[2] * u) : 0.f, vis[3] ? pr[3] * (vsc[3] * u) : 0.f);
+      const uint32_t b0 = pack_half2(vis[0] ? pu[0] * vsc[grp][0] : 0.f, vis[1] ? pu[1] * vsc[grp][1] : 0.f);
+      const uint32_t b1 = pack_half2(vis[2] ? pu[2] * vsc[grp][2] : 0.f, vis[3] ? pu[3] * vsc[grp][3] : 0.f);
       uint32_t vw[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -449,9 +466,9 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
     s_m[warp * 8 + g] = m_run;
     s_l[warp * 8 + g] = l_run;
   }
+  const float down = e_acc == 127 ? 0.f : exp2i(-e_acc);
 #pragma unroll
   for (int grp = 0; grp < NG; ++grp) {
-    const float down = e_acc[grp] == 127 ? 0.f : exp2i(-e_acc[grp]);
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
       const int ch0 = 32 * grp + 4 * g + 2 * tt;  // row g; row g+8 is ch0 + 1
