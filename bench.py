@@ -179,6 +179,53 @@ def visible_pairs_packed(seg, sink, W):
     return np.array(total)
 
 
+def performed_tiles_packed(seg, sink, W, span=128, bn=64):
+    """(128-row span, 64-key tile) pairs the prefill kernel computes, summed
+    over batch rows: the tile plan's rule -- the tile holds a key whose segment
+    id lies in the span's id range, and it reaches into the span's window or
+    holds a sink."""
+    B, T = seg.shape
+    n_kt = (T + bn - 1) // bn
+    total = 0
+    for b in range(B):
+        s = np.where(seg[b] > 0, seg[b], 0)
+        pad = np.zeros(n_kt * bn, np.int64)
+        pad[:T] = s
+        tiles = pad.reshape(n_kt, bn)
+        big = np.iinfo(np.int64).max
+        lo = np.where(tiles > 0, tiles, big).min(axis=1)
+        hi = tiles.max(axis=1)
+        skp = np.zeros(n_kt * bn, bool)
+        skp[:T] = sink[b] != 0
+        any_sink = skp.reshape(n_kt, bn).any(axis=1)
+        for q0 in range(0, T, span):
+            q1 = min(T, q0 + span) - 1
+            qs = s[q0:q1 + 1]
+            qs = qs[qs > 0]
+            if qs.size == 0:
+                continue
+            j = np.arange(q1 // bn + 1)
+            ok = (lo[j] <= hi[j]) & (lo[j] <= qs.max()) & (hi[j] >= qs.min())
+            in_win = (W == 0) | ((j + 1) * bn - 1 >= q0 - W + 1)
+            total += int((ok & (in_win | any_sink[j])).sum())
+    return total
+
+
+def performed_tiles_compressed(T, W, block, span=128, bn=64):
+    """The same count for one compressed-attention row: pooled tiles below the
+    block threshold plus exact tiles reaching into the window."""
+    total = 0
+    nb = T // block
+    for q0 in range(0, T, span):
+        q1 = min(T, q0 + span) - 1
+        lim = q1 - W + 1
+        ncol = min(lim // block, nb) if lim >= block else 0
+        total += (ncol + bn - 1) // bn
+        j = np.arange(q1 // bn + 1)
+        total += int(((j + 1) * bn - 1 >= q0 - W + 1).sum())
+    return total
+
+
 def visible_pairs_compressed(T, W, b):
     q = np.arange(T)
     exact = np.minimum(q + 1, W)
@@ -301,13 +348,28 @@ def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
         nd.nd_swa_sink_prefill(q, k, v, seg, sink, w["window"], rope_theta=w["rope_theta"], out=out, workspace=ws)
 
     ms = time_graph(torch, step, steps, warmup, dist)
+    # the attention kernel's share: the same call on pre-rotated q/k (no RoPE pass)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    nd.nd_rope_apply(q, qr, w["rope_theta"])
+    nd.nd_rope_apply(k, kr, w["rope_theta"])
+    ws0 = torch.empty(max(nd.nd_swa_sink_prefill_workspace_size(nd.ND_BF16, B, T, Hq, Hkv, d, 0.0, 0), 16),
+                      dtype=torch.uint8, device="cuda")
+
+    def attn(i):
+        nd.nd_swa_sink_prefill(qr, kr, v, seg, sink, w["window"], rope_theta=0.0, out=out, workspace=ws0)
+
+    ms_attn = time_graph(torch, attn, steps, warmup, dist)
     pairs = int(visible_pairs_packed(w["seg_ids"], w["sink"], w["window"]).sum())
     flops = 4.0 * d * pairs * Hq
-    t = ms / steps * 1e-3
+    tiles = performed_tiles_packed(w["seg_ids"], w["sink"], w["window"])
+    tile_flops = 4.0 * 128 * 64 * d * tiles * Hq
+    t, ta = ms / steps * 1e-3, ms_attn / steps * 1e-3
     return dict(config=f"packed prefill B{B} T{T} Hq{Hq} Hkv{Hkv} d{d} W256 RoPE, 3-6 segments with 64-512 sink prefixes",
                 ms_per_step=ms / steps, tok_s=B * T / t, tflops=flops / t / 1e12,
                 frac=flops / t / 1e12 / pk["bf16"], visible_pairs=pairs, flops_per_step=flops,
-                launches=2 * steps)
+                attn_ms=ms_attn / steps, tiles=tiles * Hq, tile_flops=tile_flops,
+                tile_tflops=tile_flops / ta / 1e12, tile_frac=tile_flops / ta / 1e12 / pk["bf16"],
+                launches=5 * steps)
 
 
 def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
@@ -328,12 +390,27 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
                                pooled_v=pvv, block=w["block"], out=out, workspace=ws)
 
     ms = time_graph(torch, step, steps, warmup, dist)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    nd.nd_rope_apply(q, qr, w["rope_theta"])
+    nd.nd_rope_apply(k, kr, w["rope_theta"])
+    ws0 = torch.empty(max(nd.nd_swa_sink_prefill_workspace_size(nd.ND_BF16, B, T, H, H, d, 0.0, w["block"]), 16),
+                      dtype=torch.uint8, device="cuda")
+
+    def attn(i):
+        nd.nd_swa_sink_prefill(qr, kr, v, None, None, w["window"], rope_theta=0.0, pooled_k=pkk, pooled_v=pvv,
+                               block=w["block"], out=out, workspace=ws0)
+
+    ms_attn = time_graph(torch, attn, steps, warmup, dist)
     pairs = visible_pairs_compressed(T, w["window"], w["block"]) * B * H
     flops = 4.0 * d * pairs
-    t = ms / steps * 1e-3
+    tiles = performed_tiles_compressed(T, w["window"], w["block"]) * B * H
+    tile_flops = 4.0 * 128 * 64 * d * tiles
+    t, ta = ms / steps * 1e-3, ms_attn / steps * 1e-3
     return dict(config="compressed prefill B4 T4096 H16 d64 W256 b4 RoPE", ms_per_step=ms / steps,
                 tok_s=B * T / t, tflops=flops / t / 1e12, frac=flops / t / 1e12 / pk["bf16"],
-                visible_pairs=pairs, launches=3 * steps)
+                visible_pairs=pairs, attn_ms=ms_attn / steps, tiles=tiles, tile_flops=tile_flops,
+                tile_tflops=tile_flops / ta / 1e12, tile_frac=tile_flops / ta / 1e12 / pk["bf16"],
+                launches=6 * steps)
 
 
 # ----------------------------------------------------------------------------

@@ -35,3 +35,28 @@ def test_decode_bytes():
     assert qo == 2 * 64 * 8 * 64 * 2
     cache5, _, _ = bench.decode_bytes(512, 32, 8, 128, 1024, 256)
     assert cache5 == 512 * 1280 * 2304
+
+
+def test_performed_tile_counts_bound_the_visible_tiles():
+    """The prefill tile count the bench reports sits between the tiles that
+    hold a visible pair (brute force on the oracle's mask) and all causal
+    tiles."""
+    import bench
+    import oracle
+    rng = philox(77)
+    B, T, W, span, bn = 2, 700, 100, 128, 64
+    seg, sink = packed_segments(rng, B, T, 2, 4, 120, 3, 40)
+    mask = oracle.causal_packing_mask(seg, sink, W)   # [B][T][T] bool
+    visible, causal = 0, 0
+    for b in range(B):
+        for q0 in range(0, T, span):
+            q1 = min(T, q0 + span)
+            for k0 in range(0, q1, bn):
+                causal += 1
+                visible += bool(mask[b, q0:q1, k0:k0 + bn].any())
+    got = bench.performed_tiles_packed(seg, sink, W, span, bn)
+    assert visible <= got <= causal, (visible, got, causal)
+    # one segment, no sinks, no window: every causal tile
+    seg1 = np.ones((1, T), np.int32)
+    assert bench.performed_tiles_packed(seg1, np.zeros((1, T), np.uint8), 0, span, bn) == \
+        sum((min(T, q0 + span) - 1) // bn + 1 for q0 in range(0, T, span))
