@@ -13,20 +13,26 @@
 //
 // One CTA runs two 128-row blocks that share their K/V tiles: two query heads
 // of one GQA group (same rows), or, when the group size is odd, two
-// consecutive row blocks of one head.  Its eleven warps specialise:
+// consecutive row blocks of one head.  The kernel is persistent: one CTA per
+// SM walks work items (sequence, row span, block pair) with a stride of the
+// grid, and every role keeps running tile counts, so the next item's Q and
+// first tiles load while the current one finishes.  Its eleven warps
+// specialise:
 //   warps 0-3, 4-7 : one softmax warpgroup per row block; thread i owns row i
 //                    (= TMEM lane i): exact mask, online softmax in the log2
-//                    domain; bf16 P goes back into TMEM over the S columns
-//                    it came from.
+//                    domain; bf16 P goes into one of the block's two TMEM P
+//                    buffers, so P(g) is written while PV(g-1) still runs.
 //   warp 8         : TMA loader over three rings: K tiles
 //                    (freed as soon as both blocks' S MMAs have read them),
 //                    V tiles (freed after both blocks' PV) and the exact
 //                    tiles' segment / sink records (cp.async, freed once the
 //                    softmax warps have built their masks).
-//   warps 9, 10    : one MMA issuer per row block -- S = Q K^T (M128 N64,
-//                    double-buffered in TMEM, two tiles ahead) and O += P V
-//                    (M128, N=d, P read from TMEM, V an MN-major shared
-//                    operand) -- so neither block waits behind the other's.
+//   warps 9, 10    : one MMA issuer per row block: S(g) = Q K(g)^T (M128
+//                    N64) into the block's S buffer as soon as the softmax
+//                    has read S(g-1), then O += P(g-1) V(g-1) (M128, N=d,
+//                    P read from TMEM, V an MN-major shared operand), so
+//                    neither block waits behind the other's.
+// TMEM per CTA: S 2 x 64, P 2 x 2 x 32, O 2 x d fp32 columns (512 at d=128).
 // O accumulates in TMEM; a row's O is rescaled (TMEM load / multiply / store)
 // only when its running max grows by more than 2^8, so most tiles touch O
 // only through the MMA.  Tiles every row of a warp fully sees skip the
@@ -47,28 +53,35 @@ namespace {
 
 constexpr int BM = 128;  // rows per block = TMEM lanes
 constexpr int BN = 64;   // keys per tile
-constexpr int NM = 8;    // tile-record stages
-constexpr int kWarpLoad = 8, kWarpMma0 = 9, kWarpMma1 = 10;
-constexpr int kThreads = 11 * 32;
+// warps 0-7 softmax (block 0: 0-3, block 1: 4-7), 8 loader, 9-10 MMA issuers
+// (block 0, block 1), 11 idle, 12-15 epilogue
+constexpr int kWarpLoad = 8, kWarpMma0 = 9, kWarpEpi0 = 12;
+constexpr int kThreads = 16 * 32;
+// Register split (setmaxnreg, per warpgroup): the softmax warpgroups hold a
+// 64-score row per thread; the loader / issuer and epilogue warpgroups need
+// few.  Launched at 128 a thread: 2 x 128 x 168 + 2 x 128 x 88 = 512 x 128.
+constexpr int kRegsSoftmax = 168, kRegsOther = 88;
+static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther == kThreads * 128, "register split");
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
-constexpr int kMaxPlan = 1024;      // tile-list entries staged in shared memory
 
 // Per (sequence, 64-key tile) metadata record, written once per call by
 // tile_meta_kernel and copied asynchronously into shared memory by the loader
 // next to the tile's K/V: segment ids, sink flags and summary flags.
 struct alignas(128) TileMeta {
-  int seg[BN];                 // 0 for keys past T
-  unsigned char sink[BN];
-  int seg_lo, seg_hi;          // over keys with a positive id (lo > hi: none)
+  int seg[BN];                     // 0 for keys past T
+  unsigned long long sink_bits;    // bit x = key x is a sink
+  unsigned long long id_mask[4];   // bit x = key x carries ids[i]
+  int ids[4];                      // the distinct positive segment ids, in key order
+  int n_ids;                       // how many (0..4); -1: more than four
+  int seg_lo, seg_hi;              // over keys with a positive id (lo > hi: none)
   int all_sink, any_sink;
-  unsigned long long sink_bits;  // bit x = key x is a sink
-  int uniform_seg;             // the one id every key < T carries (> 0), else 0
-  int pad[9];
+  int uniform_seg;                 // the one id every key < T carries (> 0), else 0
+  int pad[12];
 };
 static_assert(sizeof(TileMeta) == 384, "16-byte chunks for cp.async");
 
 struct TcParams {
-  int B, T, Hq, Hkv, G, W, block, nb, n_span, span, n_kt, plan_stride, pair_heads;
+  int B, T, Hq, Hkv, G, W, block, nb, n_span, span, n_kt, plan_stride, pair_heads, n_pairs;
   const int32_t *seg;
   const uint8_t *sink;
   const int32_t *plan;
@@ -89,12 +102,13 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
   TileMeta &m = meta[w];
   int lo = INT_MAX, hi = INT_MIN, all = 1, any = 0, padding = 0;
   uint32_t sink_word[2];
+  int sv[2];
   for (int kk = lane, half = 0; kk < BN; kk += 32, ++half) {
     const int k = j * BN + kk;
     const int s = k < T ? (seg ? seg[size_t(b) * T + k] : 1) : 0;
     const int sk = (k < T && sink) ? (sink[size_t(b) * T + k] != 0) : 0;
     m.seg[kk] = s;
-    m.sink[kk] = (unsigned char)sk;
+    sv[half] = s;
     if (s > 0) {
       lo = min(lo, s);
       hi = max(hi, s);
@@ -103,6 +117,28 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
     all &= sk;
     any |= sk;
     sink_word[half] = __ballot_sync(0xffffffffu, sk != 0);
+  }
+  // the distinct positive ids and, for each, the keys carrying it: at most
+  // four, taken in key order (a tile with more keeps n_ids = -1)
+  bool done0 = sv[0] <= 0, done1 = sv[1] <= 0;
+  int n_ids = 0;
+  for (int i = 0; i <= 4; ++i) {
+    const unsigned b0 = __ballot_sync(0xffffffffu, !done0), b1 = __ballot_sync(0xffffffffu, !done1);
+    if (!b0 && !b1) break;
+    if (i == 4) {
+      n_ids = -1;
+      break;
+    }
+    const int cand = b0 ? __shfl_sync(0xffffffffu, sv[0], __ffs(b0) - 1)
+                        : __shfl_sync(0xffffffffu, sv[1], __ffs(b1) - 1);
+    const unsigned m0 = __ballot_sync(0xffffffffu, sv[0] == cand), m1 = __ballot_sync(0xffffffffu, sv[1] == cand);
+    if (lane == 0) {
+      m.ids[i] = cand;
+      m.id_mask[i] = (unsigned long long)m0 | ((unsigned long long)m1 << 32);
+    }
+    done0 |= sv[0] == cand;
+    done1 |= sv[1] == cand;
+    n_ids = i + 1;
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) {
@@ -119,6 +155,7 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
     m.any_sink = any;
     m.sink_bits = (unsigned long long)sink_word[0] | ((unsigned long long)sink_word[1] << 32);
     m.uniform_seg = (lo == hi && !padding) ? lo : 0;
+    m.n_ids = n_ids;
   }
 }
 
@@ -277,24 +314,6 @@ __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes, uint32_
       : "memory");
 }
 
-// TMA tile store from shared memory (rows past the tensor's extent are not
-// written), then wait until the copy has read its shared-memory source.
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2,
-                                             int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
-__device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(BM) : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -324,17 +343,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Bounded wait that also gives up at once when another role already did.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
                                               volatile int *abort_flag) {
@@ -347,32 +355,34 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
   return false;
 }
 
-// The same for a whole warp: lane 0 polls, every lane gets the outcome and the
-// warp leaves converged.
+// The same for a whole warp: every lane polls (the warp never diverges, so
+// it is woken as one), and leaves converged with the common outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err, volatile int *abort_flag) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, err, abort_flag);
-  return __shfl_sync(0xffffffffu, ok, 0);
+  const bool ok = wait_or_abort(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ------------------------------------------------------------------ kernel
 
 template <int D>
 struct Lay {
-  static constexpr int NK = D == 64 ? 6 : 4;       // K stages
-  static constexpr int NV = D == 64 ? 5 : 3;       // V stages
+  static constexpr int NK = D == 64 ? 6 : 3;       // K stages
+  static constexpr int NV = D == 64 ? 5 : 2;       // V stages
+  static constexpr int NM = D == 64 ? 8 : 4;       // tile-record stages (>= NK: a record rides with its K tile)
   static constexpr int kBoxes = D / 64;            // 64-column swizzle atoms per row
   static constexpr int kQ = kBoxes * BM * 128;     // one block's Q tile
   static constexpr int kKV = kBoxes * BN * 128;    // one K (or V) tile
-  static constexpr int kP = BM * 64 * 2;           // one 64-column bf16 O slab
-  static constexpr int oQ = 0;                     // Q[2 blocks]
-  static constexpr int oK = 2 * kQ;                // K[NK stages]
+  static constexpr int oQ = 0;                     // Q[2 buffers][2 blocks]
+  static constexpr int oK = 4 * kQ;                // K[NK stages]
   static constexpr int oV = oK + NK * kKV;         // V[NV stages]
-  static constexpr int oP = oV + NV * kKV;         // O staging slab[2 blocks]
-  static constexpr int oM = oP + 2 * kP;           // TileMeta[NM stages]
+  static constexpr int oM = oV + NV * kKV;         // TileMeta[NM stages]
   static constexpr int kBytes = oM + NM * int(sizeof(TileMeta)) + 1024;  // + alignment slack
-  // TMEM columns: S[block][2 buffers] (BN each), then O[block] (D each)
-  static constexpr int kCols = 4 * BN + 2 * D;
+  static_assert(NM >= NK, "tile records ride with K tiles");
+  // TMEM columns: S[block][2 buffers] (BN fp32 each; P(g), BN/2 columns of
+  // bf16 pairs, overwrites the front of S(g)'s buffer), O[block] (D fp32 each)
+  static constexpr int cS = 0, cO = 4 * BN;
+  static constexpr int kCols = cO + 2 * D;
+  static_assert(kCols <= 512, "TMEM budget");
   static constexpr int kTmemCols = kCols <= 256 ? 256 : 512;
 };
 
@@ -384,47 +394,86 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
+                                             uint32_t &d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_pk,
-                      const __grid_constant__ CUtensorMap tm_pv, const __grid_constant__ CUtensorMap tm_o,
-                      const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_pv, const TcParams p) {
   using L = Lay<D>;
-  constexpr int NK = L::NK, NV = L::NV;
+  constexpr int NK = L::NK, NV = L::NV, NM = L::NM;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-      m_full[NM], m_empty[NM], s_full[2][2], p_full[2], pv_done[2];
+  __shared__ __align__(8) uint64_t q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+      m_full[NM], m_empty[NM], s_full[2][2], p_full[2][2], pv_done[2][2], o_free[2], epi_full[2],
+      epi_empty[2];
+  __shared__ float s_inv[2][BM];  // 1 / row sum, from the softmax warps to the epilogue warps
+  __shared__ __align__(128) uint8_t s_stage[4][32 * 64];  // epilogue staging, one block per warp
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_plan[kMaxPlan];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z;
-  const int head0 = p.pair_heads ? 2 * blockIdx.y : blockIdx.y;
-  const int head1 = p.pair_heads ? head0 + 1 : head0;
-  const int row00 = p.pair_heads ? blockIdx.x * BM : blockIdx.x * 2 * BM;
-  const int row01 = p.pair_heads ? row00 : row00 + BM;
-  const int hk = head0 / p.G;
-  const int32_t *plan = p.plan + (size_t(b) * p.n_span + blockIdx.x) * p.plan_stride;
-  const int n = plan[0];
   volatile int *abort_flag = &s_abort;
-  // the tile list, staged once in shared memory (read by every role each tile)
-  for (int i = tid; i < n && i < kMaxPlan; i += kThreads) s_plan[i] = plan[1 + i];
-  const int32_t *tiles = n <= kMaxPlan ? s_plan : plan + 1;
+  // Work items (sequence, 128-row span, head pair), pairs fastest so CTAs
+  // running side by side share K/V tiles in L2; CTA c takes items c,
+  // c + gridDim.x, ...  Every role walks the same items and keeps running
+  // tile counts, so the barrier phases carry over from item to item.
+  const int n_items = p.B * p.n_span * p.n_pairs;
+  struct Item {
+    int b, head0, head1, row00, row01, hk, n;
+    const int32_t *tiles;  // the plan's tile entries (global memory)
+  };
+  auto item_at = [&](int w) {
+    Item it;
+    const int pr = w % p.n_pairs, rest = w / p.n_pairs, sp = rest % p.n_span;
+    it.b = rest / p.n_span;
+    it.head0 = p.pair_heads ? 2 * pr : pr;
+    it.head1 = p.pair_heads ? it.head0 + 1 : it.head0;
+    it.row00 = p.pair_heads ? sp * BM : sp * 2 * BM;
+    it.row01 = p.pair_heads ? it.row00 : it.row00 + BM;
+    it.hk = it.head0 / p.G;
+    const int32_t *plan = p.plan + (size_t(it.b) * p.n_span + sp) * p.plan_stride;
+    it.n = plan[0];
+    it.tiles = plan + 1;
+    return it;
+  };
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  auto sQ = [&](int rb) { return base + L::oQ + rb * L::kQ; };
+  auto sQ = [&](int qb, int rb) { return base + L::oQ + (2 * qb + rb) * L::kQ; };
   auto sK = [&](int st) { return base + L::oK + st * L::kKV; };
   auto sV = [&](int st) { return base + L::oV + st * L::kKV; };
-  auto sP = [&](int rb) { return base + L::oP + rb * L::kP; };
   auto sM = [&](int st) { return base + L::oM + st * uint32_t(sizeof(TileMeta)); };
   auto meta_at = [&](int st) {  // generic pointer to a stage's tile record
     return reinterpret_cast<const TileMeta *>(smem_raw + (sM(st) - smem_u32(smem_raw)));
   };
 
   if (tid == 0) {
-    mbar_init(&bar_q, 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&q_full[u], 1);
+      mbar_init(&q_empty[u], 2);  // committed by both issuers after an item's last S MMA
+    }
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 2);  // one commit from each block's issuer
@@ -438,10 +487,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&m_empty[s], 8);   // one arrival per softmax warp
     }
     for (int r = 0; r < 2; ++r) {
-      mbar_init(&s_full[r][0], 1);
-      mbar_init(&s_full[r][1], 1);
-      mbar_init(&p_full[r], BM);
-      mbar_init(&pv_done[r], 1);
+      // one barrier triple per S/P buffer: a buffer's next use (two tiles
+      // on) cannot start before the current one has been consumed, so no
+      // wait ever sees a phase run two ahead
+      for (int u = 0; u < 2; ++u) {
+        mbar_init(&s_full[r][u], 1);
+        mbar_init(&p_full[r][u], BM);
+        mbar_init(&pv_done[r][u], 1);
+      }
+      mbar_init(&o_free[r], BM);     // the epilogue warps have read the block's O out of TMEM
+      mbar_init(&epi_full[r], BM);   // the softmax threads have posted 1 / l for the item
+      mbar_init(&epi_empty[r], BM);  // the epilogue threads have taken it
     }
     s_abort = 0;
     fence_barrier_init();
@@ -457,138 +513,264 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  auto tS = [&](int rb, int buf) { return tmem + (rb * 2 + buf) * BN; };
-  auto tO = [&](int rb) { return tmem + 4 * BN + rb * D; };
+  auto tS = [&](int rb, int buf) { return tmem + L::cS + (2 * rb + buf) * BN; };
+  auto tO = [&](int rb) { return tmem + L::cO + rb * D; };
   bool fail = false;
 
+  if (warp >= 8) {
+  // loader / issuer / epilogue warpgroups: registers to the softmax warpgroups
+  regs_dec<kRegsOther>();
   if (warp == kWarpLoad) {
     // ------------------------------------------------ TMA loader
-    //   Rings: K tiles (NK stages, freed once both blocks' S MMAs read them),
-    //   V tiles (NV stages, freed after both blocks' PV) and tile records
-    //   (NM stages, freed once all eight softmax warps built their masks).
+    //   Q: two buffers, so item i+1's Q lands while item i runs.  Rings: K
+    //   tiles (NK stages, freed once both blocks' S MMAs read them), V tiles
+    //   (NV stages, freed after both blocks' PV) and tile records (NM stages,
+    //   freed once all eight softmax warps built their masks).  The warp
+    //   stays converged; the elected lane issues.
     const uint32_t leader = elect_one();
-    if (n > 0) {
-      expect_tx(&bar_q, 2 * L::kQ, leader);
+    int gt = 0;  // tiles loaded before the current item
+    auto load_q = [&](int w, int it) {
+      const Item I = item_at(w);
+      const int qb = it & 1;
+      // the buffer's previous user, item it-2, has run all its S MMAs
+      if (it >= 2 && !warp_wait(&q_empty[qb], ((it >> 1) - 1) & 1, p.err, abort_flag)) return false;
+      expect_tx(&q_full[qb], 2 * L::kQ, leader);
       for (int x = 0; x < L::kBoxes; ++x) {
-        tma_load_4d(sQ(0) + x * BM * 128, &tm_q, 64 * x, head0, row00, b, &bar_q, leader);
-        tma_load_4d(sQ(1) + x * BM * 128, &tm_q, 64 * x, head1, row01, b, &bar_q, leader);
+        tma_load_4d(sQ(qb, 0) + x * BM * 128, &tm_q, 64 * x, I.head0, I.row00, I.b, &q_full[qb], leader);
+        tma_load_4d(sQ(qb, 1) + x * BM * 128, &tm_q, 64 * x, I.head1, I.row01, I.b, &q_full[qb], leader);
       }
-    }
-    // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...  The warp
-    // stays converged; lane 0 waits, the elected lane issues.
-    auto load_k = [&](int j) {
-      const int e = tiles[j];
-      const bool pooled = (e >> 20) & 1;
-      const int jt = e & 0xFFFFF;
-      const int st = j % NK, sm = j % NM;
-      if (!((j < NK || warp_wait(&k_empty[st], ((j / NK) - 1) & 1, p.err, abort_flag)) &&
-            (j < NM || warp_wait(&m_empty[sm], ((j / NM) - 1) & 1, p.err, abort_flag))))
-        return false;
-      expect_tx(&k_full[st], L::kKV, leader);
-      for (int x = 0; x < L::kBoxes; ++x)
-        tma_load_4d(sK(st) + x * BN * 128, pooled ? &tm_pk : &tm_k, 64 * x, hk, jt * BN, b, &k_full[st], leader);
-      // the exact tile's record (384 bytes) rides along asynchronously;
-      // pooled tiles need none, but every lane still arrives
-      constexpr int kChunks = int(sizeof(TileMeta)) / 16;
-      if (!pooled && lane < kChunks)
-        cp_async16(sM(sm) + lane * 16, reinterpret_cast<const char *>(p.meta + size_t(b) * p.n_kt + jt) + lane * 16);
-      cp_async_arrive(&m_full[sm]);
-      __syncwarp();
       return true;
     };
-    auto load_v = [&](int j) {
-      const int e = tiles[j];
-      const bool pooled = (e >> 20) & 1;
-      const int jt = e & 0xFFFFF;
-      const int st = j % NV;
-      if (!(j < NV || warp_wait(&v_empty[st], ((j / NV) - 1) & 1, p.err, abort_flag))) return false;
-      expect_tx(&v_full[st], L::kKV, leader);
-      for (int x = 0; x < L::kBoxes; ++x)
-        tma_load_4d(sV(st) + x * BN * 128, pooled ? &tm_pv : &tm_v, 64 * x, hk, jt * BN, b, &v_full[st], leader);
-      return true;
-    };
-    for (int j = 0; j <= n && !fail; ++j) {
-      if (j < n && !load_k(j)) fail = true;
-      if (!fail && j >= 1 && !load_v(j - 1)) fail = true;
+    if (blockIdx.x < n_items) fail = !load_q(blockIdx.x, 0);
+    for (int w = blockIdx.x, it = 0; w < n_items && !fail; w += gridDim.x, ++it) {
+      const Item I = item_at(w);
+      // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...  Ring
+      // positions and phases follow the running tile count g.
+      auto load_k = [&](int j) {
+        const int e = I.tiles[j];
+        const bool pooled = (e >> 20) & 1;
+        const int jt = e & 0xFFFFF;
+        const int g = gt + j, st = g % NK, sm = g % NM;
+        if (!((g < NK || warp_wait(&k_empty[st], ((g / NK) - 1) & 1, p.err, abort_flag)) &&
+              (g < NM || warp_wait(&m_empty[sm], ((g / NM) - 1) & 1, p.err, abort_flag))))
+          return false;
+        expect_tx(&k_full[st], L::kKV, leader);
+        for (int x = 0; x < L::kBoxes; ++x)
+          tma_load_4d(sK(st) + x * BN * 128, pooled ? &tm_pk : &tm_k, 64 * x, I.hk, jt * BN, I.b, &k_full[st], leader);
+        // the exact tile's record (384 bytes) rides along asynchronously;
+        // pooled tiles need none, but every lane still arrives
+        constexpr int kChunks = int(sizeof(TileMeta)) / 16;
+        if (!pooled && lane < kChunks)
+          cp_async16(sM(sm) + lane * 16, reinterpret_cast<const char *>(p.meta + size_t(I.b) * p.n_kt + jt) + lane * 16);
+        cp_async_arrive(&m_full[sm]);
+        __syncwarp();
+        return true;
+      };
+      auto load_v = [&](int j) {
+        const int e = I.tiles[j];
+        const bool pooled = (e >> 20) & 1;
+        const int jt = e & 0xFFFFF;
+        const int g = gt + j, st = g % NV;
+        if (!(g < NV || warp_wait(&v_empty[st], ((g / NV) - 1) & 1, p.err, abort_flag))) return false;
+        expect_tx(&v_full[st], L::kKV, leader);
+        for (int x = 0; x < L::kBoxes; ++x)
+          tma_load_4d(sV(st) + x * BN * 128, pooled ? &tm_pv : &tm_v, 64 * x, I.hk, jt * BN, I.b, &v_full[st], leader);
+        return true;
+      };
+      // the next item's Q goes out once K(NK-1) of this one has (its ring
+      // slot freed means the previous item's S MMAs, the last readers of
+      // that Q buffer, are done or nearly so)
+      const int jq = I.n < NK - 1 ? I.n : NK - 1;
+      const bool more = w + int(gridDim.x) < n_items;
+      for (int j = 0; j <= I.n && !fail; ++j) {
+        if (j < I.n && !load_k(j)) fail = true;
+        if (!fail && j >= 1 && !load_v(j - 1)) fail = true;
+        if (!fail && j == jq && more && !load_q(w + gridDim.x, it + 1)) fail = true;
+      }
+      gt += I.n;
     }
-  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+  } else if (warp == kWarpMma0 || warp == kWarpMma0 + 1) {
     // ------------------------------------------------ MMA issuers, one per block
-    //   S(0), S(1); then per tile j, once this block's P(j) is written: O += P V,
-    //   and S(j+2) into the same TMEM buffer once that PV has read P(j).
+    //   Per tile g of the block (g: running tile count over its items):
+    //   S(g) = Q K(g)^T into S buffer g&1 once PV(g-2) has read the P that
+    //   buffer held and K(g) has landed; then O += P(g-1) V(g-1) once P(g-1)
+    //   is in TMEM and V(g-1) has landed.
     const int rb = warp - kWarpMma0;
     const uint32_t leader = elect_one();
-    if (n > 0) {
-      constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
-      constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
-      auto issue_s = [&](int j) {
-        const int st = j % NK;
+    constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
+    constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
+    bool ok = true;
+    int gt = 0, used = 0;  // used: items so far whose O went through TMEM
+    // PV of a tile is issued after the S of the next tile, also across items:
+    // the next item's first S goes out before this item's last PV.
+    int pv_g = -1, pv_first = 0, pv_ofree = -1;  // the pending PV (o_free parity or -1)
+    auto issue_pv = [&]() {
+      const int g = pv_g, sv = g % NV;
+      // an item's first PV overwrites O: the epilogue warps must have read
+      // out the O of the previous item that used it
+      ok = (pv_ofree < 0 || warp_wait(&o_free[rb], pv_ofree, p.err, abort_flag)) &&
+           warp_wait(&p_full[rb][g & 1], (g >> 1) & 1, p.err, abort_flag) &&
+           warp_wait(&v_full[sv], (g / NV) & 1, p.err, abort_flag);
+      if (!ok) return;
+      tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes inside the atom
-          const uint64_t a = sdesc_sw128(sQ(rb) + (kk >> 2) * BM * 128 + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
-          mma_bf16(tS(rb, j & 1), a, bd, kIdS, kk > 0 ? 1u : 0u, leader);
-        }
-        mma_commit(&s_full[rb][j & 1], leader);
-        mma_commit(&k_empty[st], leader);
-      };
-      bool ok = warp_wait(&bar_q, 0, p.err, abort_flag);
-      for (int j = 0; j < 2 && j < n && ok; ++j) {
-        ok = warp_wait(&k_full[j % NK], (j / NK) & 1, p.err, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          issue_s(j);
-        }
+      for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys = 8 TMEM columns of bf16 pairs
+        const uint64_t bd = sdesc_sw128(sV(sv) + kk * 16 * 128, BN * 128, 1024);
+        mma_bf16_ts(tO(rb), tS(rb, g & 1) + kk * 8, bd, kIdPV, (!pv_first || kk > 0) ? 1u : 0u, leader);
       }
-      for (int j = 0; j < n && ok; ++j) {
-        const int sv = j % NV;
-        ok = warp_wait(&p_full[rb], j & 1, p.err, abort_flag) &&
-             warp_wait(&v_full[sv], (j / NV) & 1, p.err, abort_flag);
+      mma_commit(&pv_done[rb][g & 1], leader);
+      mma_commit(&v_empty[sv], leader);
+    };
+    Item In = item_at(blockIdx.x);  // the next item's plan row, read one item ahead
+    for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
+      const Item I = In;
+      if (w + int(gridDim.x) < n_items) In = item_at(w + gridDim.x);
+      const int qb = it & 1;
+      ok = warp_wait(&q_full[qb], (it >> 1) & 1, p.err, abort_flag);
+      for (int j = 0; j < I.n && ok; ++j) {
+        const int g = gt + j, st = g % NK;
+        ok = (g < 2 || warp_wait(&pv_done[rb][g & 1], ((g - 2) >> 1) & 1, p.err, abort_flag)) &&
+             warp_wait(&k_full[st], (g / NK) & 1, p.err, abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys = 8 TMEM columns of bf16 pairs
-          const uint64_t bd = sdesc_sw128(sV(sv) + kk * 16 * 128, BN * 128, 1024);
-          mma_bf16_ts(tO(rb), tS(rb, j & 1) + kk * 8, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u, leader);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes inside the atom
+          const uint64_t a = sdesc_sw128(sQ(qb, rb) + (kk >> 2) * BM * 128 + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
+          mma_bf16(tS(rb, g & 1), a, bd, kIdS, kk > 0 ? 1u : 0u, leader);
         }
-        mma_commit(&pv_done[rb], leader);
-        mma_commit(&v_empty[sv], leader);
-        if (j + 2 < n) {
-          // S(j+2) overwrites the columns PV(j) reads P(j) from: wait for it
-          ok = warp_wait(&pv_done[rb], j & 1, p.err, abort_flag) &&
-               warp_wait(&k_full[(j + 2) % NK], ((j + 2) / NK) & 1, p.err, abort_flag);
+        mma_commit(&s_full[rb][g & 1], leader);
+        mma_commit(&k_empty[st], leader);
+        if (j + 1 == I.n) mma_commit(&q_empty[qb], leader);  // Q may be replaced once these have run
+        if (pv_g >= 0) issue_pv();
+        pv_g = g;
+        pv_first = j == 0;
+        pv_ofree = (j == 0 && used > 0) ? ((used - 1) & 1) : -1;
+      }
+      if (I.n == 0) mma_commit(&q_empty[qb], leader);
+      if (I.n > 0) ++used;
+      gt += I.n;
+    }
+    if (ok && pv_g >= 0) issue_pv();
+    fail = !ok;
+  } else if (warp >= kWarpEpi0) {
+    // ------------------------------------------------ epilogue warps
+    //   Warp 12 + x reads TMEM lanes 32x..32x+31 of each block's O once the
+    //   item's last PV has landed, frees O for the next item, and writes
+    //   O / l as bf16 rows straight to global memory (one row per thread,
+    //   sixteen-byte stores).
+    const int qd = warp & 3;
+    const int r = qd * 32 + lane;
+    const uint32_t lane_base = uint32_t(qd * 32) << 16;
+    const uint32_t stage = smem_u32(&s_stage[qd][0]);
+    bool ok = true;
+    int gt = 0;
+    for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
+      const Item I = item_at(w);
+      const int n = I.n;
+      for (int rb = 0; rb < 2 && ok; ++rb) {
+        ok = warp_wait(&epi_full[rb], it & 1, p.err, abort_flag);
+        if (!ok) break;
+        const float inv = s_inv[rb][r];
+        mbar_arrive(&epi_empty[rb]);
+        const int head = rb ? I.head1 : I.head0;
+        if (n > 0) {
+          // PV(gl) landing implies every earlier MMA of the block has
+          const int gl = gt + n - 1;
+          ok = warp_wait(&pv_done[rb][gl & 1], (gl >> 1) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          issue_s(j + 2);
+        }
+        // 32 columns at a time: TMEM -> registers (scaled, bf16) -> this
+        // warp's 2 KB staging block (row = lane, 64 bytes, 16-byte chunks
+        // swizzled) -> 8 rows x 64 contiguous bytes per warp store
+        const int row0 = (rb ? I.row01 : I.row00) + qd * 32;
+#pragma unroll 1
+        for (int x = 0; x < D; x += 32) {
+          uint32_t ov[32];
+          if (n > 0) {
+            tmem_ld32(tO(rb) + lane_base + x, ov);
+            tmem_ld_wait();
+            if (x + 32 == D) {
+              tc_fence_before();
+              mbar_arrive(&o_free[rb]);  // the next item's PV may overwrite O
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = 0u;  // no visible key
+          }
+#pragma unroll
+          for (int y = 0; y < 4; ++y)
+            st_shared_v4(stage + lane * 64 + ((y ^ ((lane >> 1) & 3)) << 4),
+                         pack_bf16x2(__uint_as_float(ov[8 * y]) * inv, __uint_as_float(ov[8 * y + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[8 * y + 2]) * inv, __uint_as_float(ov[8 * y + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[8 * y + 4]) * inv, __uint_as_float(ov[8 * y + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[8 * y + 6]) * inv, __uint_as_float(ov[8 * y + 7]) * inv));
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + (lane >> 2), ch = lane & 3;
+            uint32_t a0, a1, a2, a3;
+            ld_shared_v4(stage + rr * 64 + ((ch ^ ((rr >> 1) & 3)) << 4), a0, a1, a2, a3);
+            const int qq = row0 + rr;
+            if (qq < p.T)
+              st_global_v4(p.out + ((size_t(I.b) * p.T + qq) * p.Hq + head) * D + x + 8 * ch, a0, a1, a2, a3);
+          }
+          __syncwarp();  // the staging block is free again
         }
       }
-      fail = !ok;
+      gt += n;
     }
+    fail = !ok;
+  }
   } else {
     // ------------------------------------------------ softmax warpgroups
+    regs_inc<kRegsSoftmax>();
     const int rb = warp >> 2;
     const int r = tid & (BM - 1);
-    const int q = (rb ? row01 : row00) + r;
-    const int head = rb ? head1 : head0;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    const int myseg = q < p.T ? (p.seg ? p.seg[size_t(b) * p.T + q] : 1) : 0;
     const int W = p.W == 0 ? INT_MAX : p.W;
     const float c = 1.4426950408889634f * rsqrtf(float(D));  // log2(e) / sqrt(d)
+    int gt = 0;
+    // An item's plan count, first tile entry and this row's segment id are
+    // fetched one item ahead: at an item boundary these global loads would
+    // otherwise queue behind the epilogue warps' stores.  (A plan row always
+    // has room for one entry, so tiles[0] is read even when n is 0.)
+    auto row_seg = [&](const Item &J) {
+      const int qq = (rb ? J.row01 : J.row00) + r;
+      return qq < p.T ? (p.seg ? p.seg[size_t(J.b) * p.T + qq] : 1) : 0;
+    };
+    Item In = item_at(blockIdx.x);
+    int seg_n = row_seg(In), e_n = In.tiles[0];
+    for (int w = blockIdx.x, it = 0; w < n_items; w += gridDim.x, ++it) {
+    const Item I = In;
+    const int n = I.n, b = I.b;
+    const int q = (rb ? I.row01 : I.row00) + r;
+    const int head = rb ? I.head1 : I.head0;
+    const int myseg = seg_n;
     float m_used = -INFINITY, l = 0.f;
+    int e_next = e_n;  // the next tile's entry, read a tile ahead
+    if (w + int(gridDim.x) < n_items) {
+      In = item_at(w + gridDim.x);
+      seg_n = row_seg(In);
+      e_n = In.tiles[0];
+    }
     for (int j = 0; j < n; ++j) {
-      const int sm = j % NM;
-      const int e = tiles[j];
+      const int g = gt + j, sm = g % NM;
+      const int e = e_next;
+      if (j + 1 < n) e_next = I.tiles[j + 1];
       const bool pooled = (e >> 20) & 1;
       const int k0 = (e & 0xFFFFF) * BN;
-      if (!fail && !(wait_or_abort(&s_full[rb][j & 1], (j >> 1) & 1, p.err, abort_flag) &&
-                     wait_or_abort(&m_full[sm], (j / NM) & 1, p.err, abort_flag)))
+      if (!fail && !(wait_or_abort(&s_full[rb][g & 1], (g >> 1) & 1, p.err, abort_flag) &&
+                     wait_or_abort(&m_full[sm], (g / NM) & 1, p.err, abort_flag)))
         fail = true;
       __syncwarp();
       tc_fence_after();
       // one 64-register row buffer: raw scores, then masked scores, then p
       uint32_t v[BN];
-      tmem_ld32(tS(rb, j & 1) + lane_base, v);
-      tmem_ld32(tS(rb, j & 1) + lane_base + 32, v + 32);
+      tmem_ld32(tS(rb, g & 1) + lane_base, v);
+      tmem_ld32(tS(rb, g & 1) + lane_base + 32, v + 32);
       tmem_ld_wait();
       constexpr uint32_t kNegInf = 0xff800000u;
       // every key of the tile visible for this row?  (warp-uniform fast path)
@@ -597,8 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         full = myseg > 0 && k0 + BN - 1 < p.nb && (k0 + BN) * p.block <= q - p.W + 1;
       } else {
         const TileMeta *f = meta_at(sm);
-        full = myseg > 0 && f->seg_lo == myseg && f->seg_hi == myseg && k0 + BN - 1 <= q &&
-               (q - k0 < W || f->all_sink);
+        full = myseg > 0 && f->uniform_seg == myseg && k0 + BN - 1 <= q && (q - k0 < W || f->all_sink);
       }
       if (__all_sync(0xffffffffu, full)) {
         // nothing to mask
@@ -613,44 +794,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         // A 64-bit visibility mask for this row, then one bit test and a
         // select per key.
         const TileMeta *f = meta_at(sm);
-        uint32_t v0 = 0u, v1 = 0u;
-        if (f->uniform_seg != 0) {
-          // every key in one segment: (causal bound) and (window range or
-          // sink), built from shifts
-          const int hi = q - k0;                             // last causal key (tile-relative)
-          const int lo = W == INT_MAX ? 0 : q - W + 1 - k0;  // first key inside the window
-          const unsigned long long all1 = ~0ull;
-          const unsigned long long causal = hi < 0 ? 0ull : (hi >= 63 ? all1 : (all1 >> (63 - hi)));
-          const unsigned long long window = lo <= 0 ? all1 : (lo > 63 ? 0ull : (all1 << lo));
-          const unsigned long long vis =
-              (f->uniform_seg == myseg && myseg > 0) ? (causal & (window | f->sink_bits)) : 0ull;
-          v0 = uint32_t(vis);
-          v1 = uint32_t(vis >> 32);
+        // (causal bound) and (window range or sink), from shifts
+        const int hi = q - k0;                             // last causal key (tile-relative)
+        const int lo = W == INT_MAX ? 0 : q - W + 1 - k0;  // first key inside the window
+        const unsigned long long all1 = ~0ull;
+        const unsigned long long causal = hi < 0 ? 0ull : (hi >= 63 ? all1 : (all1 >> (63 - hi)));
+        const unsigned long long window = lo <= 0 ? all1 : (lo > 63 ? 0ull : (all1 << lo));
+        const unsigned long long cw = causal & (window | f->sink_bits);
+        const int nid = f->n_ids;
+        unsigned long long vis = 0ull;
+        if (nid >= 0) {
+          // the keys of this row's segment: one of the tile's few ids
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vis = (i < nid && f->ids[i] == myseg) ? f->id_mask[i] : vis;
+          vis = myseg > 0 ? (vis & cw) : 0ull;
         } else {
-          // keys from several segments (or padding): compare every key's
-          // segment id and sink flag, four at a time, branch-free; the loop
-          // stays rolled so the loads do not pile up in registers
-          const uint32_t mseg = sM(sm), msink = sM(sm) + BN * 4;
+          // more than four ids in the tile: compare every key's id, four at
+          // a time; the loop stays rolled so the loads do not pile up
+          const uint32_t mseg = sM(sm);
 #pragma unroll 1
           for (int x = 0; x < BN; x += 4) {
             int sg[4];
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(sg[0]), "=r"(sg[1]), "=r"(sg[2]), "=r"(sg[3])
                          : "r"(mseg + x * 4));
-            uint32_t sk;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sk) : "r"(msink + x));
-            uint32_t bits = 0u;
+            unsigned long long bits = 0ull;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k = k0 + x + i;
-              const bool vis = (myseg > 0) & (k <= q) & (sg[i] == myseg) &
-                               ((q - k < W) | (((sk >> (8 * i)) & 0xffu) != 0u));
-              bits |= uint32_t(vis) << i;
-            }
-            if (x < 32) v0 |= bits << x;
-            else v1 |= bits << (x - 32);
+            for (int i = 0; i < 4; ++i) bits |= (unsigned long long)(sg[i] == myseg) << i;
+            vis |= bits << x;
           }
+          vis = myseg > 0 ? (vis & cw) : 0ull;
         }
+        const uint32_t v0 = uint32_t(vis), v1 = uint32_t(vis >> 32);
 #pragma unroll
         for (int x = 0; x < BN; ++x) {
           const uint32_t bit = x < 32 ? (v0 >> x) & 1u : (v1 >> (x - 32)) & 1u;
@@ -695,10 +870,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[x + 1] = __float_as_uint(bb);
       }
       l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
-      // O is rescaled only after PV(j-1) has landed (rare: the max grew by
-      // more than 2^8); otherwise nothing here waits for the tensor core
+      // O is rescaled only when the max grew by more than 2^8 (rare), after
+      // PV(g-1) has landed
       if (__any_sync(0xffffffffu, need) && j >= 1) {
-        if (!fail && !wait_or_abort(&pv_done[rb], (j - 1) & 1, p.err, abort_flag)) fail = true;
+        if (!fail && !wait_or_abort(&pv_done[rb][(g - 1) & 1], ((g - 1) >> 1) & 1, p.err, abort_flag))
+          fail = true;
         __syncwarp();
         tc_fence_after();
 #pragma unroll 1
@@ -711,60 +887,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO(rb) + lane_base + x, ov);
         }
       }
-      // P(j) as bf16 pairs over the first 32 columns of S(j)'s TMEM buffer
-      // (already read), where the PV MMA takes it as its A operand
+      // P(g) as bf16 pairs over the front of S(g)'s buffer (already read out),
+      // the A operand of the block's PV
 #pragma unroll
       for (int i = 0; i < BN / 2; ++i)
         v[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-      tmem_st32(tS(rb, j & 1) + lane_base, v);
+      tmem_st32(tS(rb, g & 1) + lane_base, v);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[rb]);
+      mbar_arrive(&p_full[rb][g & 1]);
     }
-    // ---- epilogue: O / l from TMEM
-    //   PV(n-2) may still be in flight here (only PV(n-3) is known to have
-    //   landed: S(n-1) waited for it), so wait for PV(n-2) and then PV(n-1);
-    //   a parity wait on PV(n-1) alone would match PV(n-3)'s phase.
-    if (n > 1 && !fail && !wait_or_abort(&pv_done[rb], (n - 2) & 1, p.err, abort_flag)) fail = true;
-    if (n > 0 && !fail && !wait_or_abort(&pv_done[rb], (n - 1) & 1, p.err, abort_flag)) fail = true;
-    __syncwarp();
-    tc_fence_after();
-    // O / l, staged through this block's slab buffer as 64-column swizzled
-    // slabs and written by TMA
-    const bool store = q < p.T;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const int row0 = rb ? row01 : row00;
-    const uint32_t prow = sP(rb) + r * 128;
-#pragma unroll 1
-    for (int x0 = 0; x0 < D; x0 += 64) {
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t ov[32];
-        if (n > 0) {
-          tmem_ld32(tO(rb) + lane_base + x0 + 32 * h, ov);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = 0u;
-        }
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          const int ch = 4 * h + y;
-          st_shared_v4(prow + ((ch ^ (r & 7)) << 4),
-                       pack_bf16x2(__uint_as_float(ov[8 * y]) * inv, __uint_as_float(ov[8 * y + 1]) * inv),
-                       pack_bf16x2(__uint_as_float(ov[8 * y + 2]) * inv, __uint_as_float(ov[8 * y + 3]) * inv),
-                       pack_bf16x2(__uint_as_float(ov[8 * y + 4]) * inv, __uint_as_float(ov[8 * y + 5]) * inv),
-                       pack_bf16x2(__uint_as_float(ov[8 * y + 6]) * inv, __uint_as_float(ov[8 * y + 7]) * inv));
-        }
-      }
-      fence_proxy_async_smem();
-      group_sync(1 + rb);
-      if (r == 0 && row0 < p.T && !fail && !*abort_flag) tma_store_4d(&tm_o, sP(rb), x0, head, row0, b);
-      group_sync(1 + rb);  // the slab buffer is free again
-    }
-    if (store && p.lse && !fail)
+    // post 1 / l for the epilogue warps (once they have taken the previous
+    // item's) and write the row's log-sum-exp
+    if (it >= 1 && !fail && !wait_or_abort(&epi_empty[rb], (it - 1) & 1, p.err, abort_flag)) fail = true;
+    s_inv[rb][r] = l > 0.f ? 1.f / l : 0.f;
+    mbar_arrive(&epi_full[rb]);
+    if (q < p.T && p.lse && !fail)
       p.lse[(size_t(b) * p.Hq + head) * p.T + q] =
           l > 0.f ? (m_used * c + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+    gt += n;
+    }
   }
 
   // ---- common exit: on the error path give copies and MMAs still in flight a
@@ -851,6 +993,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.n_kt = pd.n_kt;
   p.plan_stride = pd.stride;
   p.pair_heads = pair_heads ? 1 : 0;
+  p.n_pairs = pair_heads ? a.Hq / 2 : a.Hq;
   p.seg = a.seg_ids;
   p.sink = a.sink;
   p.plan = plan;
@@ -859,9 +1002,9 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.lse = a.lse;
   p.err = err;
 
-  CUtensorMap tq, tk, tv, tpk, tpv, to;
+  CUtensorMap tq, tk, tv, tpk, tpv;
   if (!make_map(&tq, a.q, a.batch, a.T, a.Hq, D, BM) || !make_map(&tk, a.k, a.batch, a.T, a.Hkv, D, BN) ||
-      !make_map(&tv, a.v, a.batch, a.T, a.Hkv, D, BN) || !make_map(&to, a.out, a.batch, a.T, a.Hq, D, BM))
+      !make_map(&tv, a.v, a.batch, a.T, a.Hkv, D, BN))
     return cudaErrorInvalidValue;
   if (a.block > 0 && p.nb > 0) {
     if (!make_map(&tpk, a.pooled_k, a.batch, p.nb, a.Hkv, D, BN) ||
@@ -878,8 +1021,14 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(pd.n_span, pair_heads ? a.Hq / 2 : a.Hq, a.batch);
-  kern<<<grid, kThreads, Lay<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, to, p);
+  // persistent: one CTA per SM (or per item, when there are fewer items)
+  int sms = 0, dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long n_items = long(a.batch) * pd.n_span * p.n_pairs;
+  dim3 grid(unsigned(n_items < sms ? n_items : sms));
+  kern<<<grid, kThreads, Lay<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, p);
   return cudaGetLastError();
 }
 

@@ -115,6 +115,45 @@ def test_bf16_padding_rows_are_zero():
     assert_close_bf16(out, want, "padding")
 
 
+@pytest.mark.parametrize("window", [0, 256])
+def test_bf16_zero_gap_inside_segment(window):
+    """Keys with segment id 0 between two runs of the same id are never
+    visible, also to whole warps of later rows that see their tile entirely
+    (causal bound and window), where the per-tile fast path applies."""
+    rng = philox(910 + window)
+    B, T, Hq, Hkv, d = 1, 640, 4, 2, 128
+    qb, q = normal_bf16(rng, (B, T, Hq, d))
+    kb, k = normal_bf16(rng, (B, T, Hkv, d))
+    vb, v = normal_bf16(rng, (B, T, Hkv, d))
+    seg = np.ones((B, T), np.int32)
+    seg[0, 100:180] = 0
+    sink = np.zeros((B, T), np.uint8)
+    sink[0, [5, 64, 130, 200]] = 1
+    out = host(nd().nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), dev(sink), window))
+    want, _ = oracle.swa_sink_prefill(q, k, v, seg, sink, window)
+    assert_close_bf16(out, want, f"zero gap W={window}")
+
+
+def test_bf16_many_segments_per_tile():
+    """Tiles holding more than four segment ids (short segments, ids
+    repeating out of order) and tiles holding two to four."""
+    rng = philox(920)
+    B, T, Hq, Hkv, d = 2, 512, 4, 2, 64
+    qb, q = normal_bf16(rng, (B, T, Hq, d))
+    kb, k = normal_bf16(rng, (B, T, Hkv, d))
+    vb, v = normal_bf16(rng, (B, T, Hkv, d))
+    seg = np.empty((B, T), np.int32)
+    seg[0] = 1 + (np.arange(T) // 6) % 9          # runs of 6: up to 11 ids per 64-key tile
+    seg[1] = 1 + (np.arange(T) // 24)             # runs of 24: 3 or 4 ids per tile
+    seg[1, 300:310] = 0
+    sink = (philox(921).random((B, T)) < 0.05).astype(np.uint8)
+    for window in (0, 40):
+        out = host(nd().nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), dev(sink),
+                                            window))
+        want, _ = oracle.swa_sink_prefill(q, k, v, seg, sink, window)
+        assert_close_bf16(out, want, f"many segments W={window}")
+
+
 def test_packed_prefill_full_size_sampled():
     """Packed-segment prefill at full size (B8 T4096 Hq32 Hkv8 d128, W256,
     RoPE) in the bench's launch configuration; sampled rows vs the oracle."""
