@@ -378,9 +378,12 @@ struct Lay {
   static constexpr int oM = oV + NV * kKV;         // TileMeta[NM stages]
   static constexpr int kBytes = oM + NM * int(sizeof(TileMeta)) + 1024;  // + alignment slack
   static_assert(NM >= NK, "tile records ride with K tiles");
-  // TMEM columns: S[block][2 buffers] (BN fp32 each; P(g), BN/2 columns of
+  // S buffers per block: P(g) is written over the front of S(g)'s buffer, so
+  // S(g + NS) waits for PV(g); at d = 64 three fit beside O
+  static constexpr int NS = D == 64 ? 3 : 2;
+  // TMEM columns: S[block][NS buffers] (BN fp32 each; P(g), BN/2 columns of
   // bf16 pairs, overwrites the front of S(g)'s buffer), O[block] (D fp32 each)
-  static constexpr int cS = 0, cO = 4 * BN;
+  static constexpr int cS = 0, cO = 2 * NS * BN;
   static constexpr int kCols = cO + 2 * D;
   static_assert(kCols <= 512, "TMEM budget");
   static constexpr int kTmemCols = kCols <= 256 ? 256 : 512;
@@ -418,16 +421,19 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D>
+// kPooled: the compressed variant (pooled column tiles, no segment ids or
+// sinks); otherwise exact tiles under the packing mask only.  The two are
+// separate instantiations so each carries only its own masking code.
+template <int D, bool kPooled>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_pk,
                       const __grid_constant__ CUtensorMap tm_pv, const TcParams p) {
   using L = Lay<D>;
-  constexpr int NK = L::NK, NV = L::NV, NM = L::NM;
+  constexpr int NK = L::NK, NV = L::NV, NM = L::NM, NS = L::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-      m_full[NM], m_empty[NM], s_full[2][2], p_full[2][2], pv_done[2][2], o_free[2], epi_full[2],
+      m_full[NM], m_empty[NM], s_full[2][NS], p_full[2][NS], pv_done[2][NS], o_free[2], epi_full[2],
       epi_empty[2];
   __shared__ float s_inv[2][BM];  // 1 / row sum, from the softmax warps to the epilogue warps
   __shared__ __align__(128) uint8_t s_stage[4][32 * 64];  // epilogue staging, one block per warp
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one barrier triple per S/P buffer: a buffer's next use (two tiles
       // on) cannot start before the current one has been consumed, so no
       // wait ever sees a phase run two ahead
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < NS; ++u) {
         mbar_init(&s_full[r][u], 1);
         mbar_init(&p_full[r][u], BM);
         mbar_init(&pv_done[r][u], 1);
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  auto tS = [&](int rb, int buf) { return tmem + L::cS + (2 * rb + buf) * BN; };
+  auto tS = [&](int rb, int buf) { return tmem + L::cS + (NS * rb + buf) * BN; };
   auto tO = [&](int rb) { return tmem + L::cO + rb * D; };
   bool fail = false;
 
@@ -548,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // positions and phases follow the running tile count g.
       auto load_k = [&](int j) {
         const int e = I.tiles[j];
-        const bool pooled = (e >> 20) & 1;
+        const bool pooled = kPooled && ((e >> 20) & 1);
         const int jt = e & 0xFFFFF;
         const int g = gt + j, st = g % NK, sm = g % NM;
         if (!((g < NK || warp_wait(&k_empty[st], ((g / NK) - 1) & 1, p.err, abort_flag)) &&
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_v = [&](int j) {
         const int e = I.tiles[j];
-        const bool pooled = (e >> 20) & 1;
+        const bool pooled = kPooled && ((e >> 20) & 1);
         const int jt = e & 0xFFFFF;
         const int g = gt + j, st = g % NV;
         if (!(g < NV || warp_wait(&v_empty[st], ((g / NV) - 1) & 1, p.err, abort_flag))) return false;
@@ -601,24 +607,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdPV = idesc_bf16(BM, D, 1);
     bool ok = true;
     int gt = 0, used = 0;  // used: items so far whose O went through TMEM
-    // PV of a tile is issued after the S of the next tile, also across items:
-    // the next item's first S goes out before this item's last PV.
-    int pv_g = -1, pv_first = 0, pv_ofree = -1;  // the pending PV (o_free parity or -1)
+    // PV(g) is issued after S(g + 1), also across items (the next item's
+    // first S goes out before this item's last PV).  S(g) waits for
+    // PV(g - NS), issued NS - 1 iterations earlier: with NS = 3 that wait
+    // has a tile of slack, with NS = 2 it follows the PV just issued.
+    constexpr int kLag = 1;
+    int pv_g[2] = {-1, -1}, pv_first[2] = {0, 0}, pv_ofree[2] = {-1, -1};  // pending PVs, oldest first
+    int npend = 0;
     auto issue_pv = [&]() {
-      const int g = pv_g, sv = g % NV;
+      const int g = pv_g[0], first = pv_first[0], ofree = pv_ofree[0], sv = g % NV, u = g % NS;
+      pv_g[0] = pv_g[1];
+      pv_first[0] = pv_first[1];
+      pv_ofree[0] = pv_ofree[1];
+      --npend;
       // an item's first PV overwrites O: the epilogue warps must have read
       // out the O of the previous item that used it
-      ok = (pv_ofree < 0 || warp_wait(&o_free[rb], pv_ofree, p.err, abort_flag)) &&
-           warp_wait(&p_full[rb][g & 1], (g >> 1) & 1, p.err, abort_flag) &&
+      ok = (ofree < 0 || warp_wait(&o_free[rb], ofree, p.err, abort_flag)) &&
+           warp_wait(&p_full[rb][u], (g / NS) & 1, p.err, abort_flag) &&
            warp_wait(&v_full[sv], (g / NV) & 1, p.err, abort_flag);
       if (!ok) return;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys = 8 TMEM columns of bf16 pairs
         const uint64_t bd = sdesc_sw128(sV(sv) + kk * 16 * 128, BN * 128, 1024);
-        mma_bf16_ts(tO(rb), tS(rb, g & 1) + kk * 8, bd, kIdPV, (!pv_first || kk > 0) ? 1u : 0u, leader);
+        mma_bf16_ts(tO(rb), tS(rb, u) + kk * 8, bd, kIdPV, (!first || kk > 0) ? 1u : 0u, leader);
       }
-      mma_commit(&pv_done[rb][g & 1], leader);
+      mma_commit(&pv_done[rb][u], leader);
       mma_commit(&v_empty[sv], leader);
     };
     Item In = item_at(blockIdx.x);  // the next item's plan row, read one item ahead
@@ -629,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&q_full[qb], (it >> 1) & 1, p.err, abort_flag);
       for (int j = 0; j < I.n && ok; ++j) {
         const int g = gt + j, st = g % NK;
-        ok = (g < 2 || warp_wait(&pv_done[rb][g & 1], ((g - 2) >> 1) & 1, p.err, abort_flag)) &&
+        // the buffer holds P(g - NS) until PV(g - NS) has read it
+        ok = (g < NS || warp_wait(&pv_done[rb][g % NS], ((g - NS) / NS) & 1, p.err, abort_flag)) &&
              warp_wait(&k_full[st], (g / NK) & 1, p.err, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -638,21 +653,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes inside the atom
           const uint64_t a = sdesc_sw128(sQ(qb, rb) + (kk >> 2) * BM * 128 + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
-          mma_bf16(tS(rb, g & 1), a, bd, kIdS, kk > 0 ? 1u : 0u, leader);
+          mma_bf16(tS(rb, g % NS), a, bd, kIdS, kk > 0 ? 1u : 0u, leader);
         }
-        mma_commit(&s_full[rb][g & 1], leader);
+        mma_commit(&s_full[rb][g % NS], leader);
         mma_commit(&k_empty[st], leader);
         if (j + 1 == I.n) mma_commit(&q_empty[qb], leader);  // Q may be replaced once these have run
-        if (pv_g >= 0) issue_pv();
-        pv_g = g;
-        pv_first = j == 0;
-        pv_ofree = (j == 0 && used > 0) ? ((used - 1) & 1) : -1;
+        if (npend == kLag) issue_pv();
+        const int of = (j == 0 && used > 0) ? ((used - 1) & 1) : -1;
+        if (npend == 0) {  // (fixed slots keep the queue in registers)
+          pv_g[0] = g;
+          pv_first[0] = j == 0;
+          pv_ofree[0] = of;
+        } else {
+          pv_g[1] = g;
+          pv_first[1] = j == 0;
+          pv_ofree[1] = of;
+        }
+        ++npend;
       }
       if (I.n == 0) mma_commit(&q_empty[qb], leader);
       if (I.n > 0) ++used;
       gt += I.n;
     }
-    if (ok && pv_g >= 0) issue_pv();
+    while (ok && npend > 0) issue_pv();
     fail = !ok;
   } else if (warp >= kWarpEpi0) {
     // ------------------------------------------------ epilogue warps
@@ -678,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n > 0) {
           // PV(gl) landing implies every earlier MMA of the block has
           const int gl = gt + n - 1;
-          ok = warp_wait(&pv_done[rb][gl & 1], (gl >> 1) & 1, p.err, abort_flag);
+          ok = warp_wait(&pv_done[rb][gl % NS], (gl / NS) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
         }
@@ -760,71 +783,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = gt + j, sm = g % NM;
       const int e = e_next;
       if (j + 1 < n) e_next = I.tiles[j + 1];
-      const bool pooled = (e >> 20) & 1;
+      const bool pooled = kPooled && ((e >> 20) & 1);
       const int k0 = (e & 0xFFFFF) * BN;
-      if (!fail && !(wait_or_abort(&s_full[rb][g & 1], (g >> 1) & 1, p.err, abort_flag) &&
+      if (!fail && !(wait_or_abort(&s_full[rb][g % NS], (g / NS) & 1, p.err, abort_flag) &&
                      wait_or_abort(&m_full[sm], (g / NM) & 1, p.err, abort_flag)))
         fail = true;
       __syncwarp();
       tc_fence_after();
       // one 64-register row buffer: raw scores, then masked scores, then p
       uint32_t v[BN];
-      tmem_ld32(tS(rb, g & 1) + lane_base, v);
-      tmem_ld32(tS(rb, g & 1) + lane_base + 32, v + 32);
+      tmem_ld32(tS(rb, g % NS) + lane_base, v);
+      tmem_ld32(tS(rb, g % NS) + lane_base + 32, v + 32);
       tmem_ld_wait();
       constexpr uint32_t kNegInf = 0xff800000u;
-      // every key of the tile visible for this row?  (warp-uniform fast path)
-      bool full;
+      // This row's 64-bit visibility word over the tile (bit x = key k0 + x),
+      // built from shifts: a prefix for pooled columns (j visible iff
+      // (j+1)*block <= q-W+1), (causal bound) and (window or sink) and (the
+      // row's segment) for exact keys.  Whole-warp all-visible tiles skip
+      // the per-key select.
+      const unsigned long long all1 = ~0ull;
+      auto prefix = [&](int last) {  // bits 0..last
+        return last < 0 ? 0ull : (last >= 63 ? all1 : (all1 >> (63 - last)));
+      };
+      unsigned long long vis;
       if (pooled) {
-        full = myseg > 0 && k0 + BN - 1 < p.nb && (k0 + BN) * p.block <= q - p.W + 1;
+        const int lim = q - p.W + 1;
+        const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
+        vis = myseg > 0 ? prefix(ncol - 1 - k0) : 0ull;
       } else {
-        const TileMeta *f = meta_at(sm);
-        full = myseg > 0 && f->uniform_seg == myseg && k0 + BN - 1 <= q && (q - k0 < W || f->all_sink);
-      }
-      if (__all_sync(0xffffffffu, full)) {
-        // nothing to mask
-      } else if (pooled) {
-#pragma unroll
-        for (int x = 0; x < BN; ++x) {
-          const int jp = k0 + x;
-          const bool vis = (myseg > 0) & (jp < p.nb) & ((jp + 1) * p.block <= q - p.W + 1);
-          v[x] = vis ? v[x] : kNegInf;
-        }
-      } else {
-        // A 64-bit visibility mask for this row, then one bit test and a
-        // select per key.
-        const TileMeta *f = meta_at(sm);
-        // (causal bound) and (window range or sink), from shifts
-        const int hi = q - k0;                             // last causal key (tile-relative)
         const int lo = W == INT_MAX ? 0 : q - W + 1 - k0;  // first key inside the window
-        const unsigned long long all1 = ~0ull;
-        const unsigned long long causal = hi < 0 ? 0ull : (hi >= 63 ? all1 : (all1 >> (63 - hi)));
         const unsigned long long window = lo <= 0 ? all1 : (lo > 63 ? 0ull : (all1 << lo));
-        const unsigned long long cw = causal & (window | f->sink_bits);
-        const int nid = f->n_ids;
-        unsigned long long vis = 0ull;
-        if (nid >= 0) {
-          // the keys of this row's segment: one of the tile's few ids
-#pragma unroll
-          for (int i = 0; i < 4; ++i) vis = (i < nid && f->ids[i] == myseg) ? f->id_mask[i] : vis;
-          vis = myseg > 0 ? (vis & cw) : 0ull;
+        const unsigned long long causal = prefix(q - k0);
+        if (kPooled) {
+          // no segment ids or sinks in the compressed variant
+          vis = myseg > 0 ? (causal & window) : 0ull;
         } else {
-          // more than four ids in the tile: compare every key's id, four at
-          // a time; the loop stays rolled so the loads do not pile up
-          const uint32_t mseg = sM(sm);
-#pragma unroll 1
-          for (int x = 0; x < BN; x += 4) {
-            int sg[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(sg[0]), "=r"(sg[1]), "=r"(sg[2]), "=r"(sg[3])
-                         : "r"(mseg + x * 4));
-            unsigned long long bits = 0ull;
+          const TileMeta *f = meta_at(sm);
+          const unsigned long long cw = causal & (window | f->sink_bits);
+          const int nid = f->n_ids;
+          vis = 0ull;
+          if (nid >= 0) {
+            // the keys of this row's segment: one of the tile's few ids
 #pragma unroll
-            for (int i = 0; i < 4; ++i) bits |= (unsigned long long)(sg[i] == myseg) << i;
-            vis |= bits << x;
+            for (int i = 0; i < 4; ++i) vis = (i < nid && f->ids[i] == myseg) ? f->id_mask[i] : vis;
+          } else {
+            // more than four ids in the tile: compare every key's id, four
+            // at a time; the loop stays rolled so the loads do not pile up
+            const uint32_t mseg = sM(sm);
+#pragma unroll 1
+            for (int x = 0; x < BN; x += 4) {
+              int sg[4];
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(sg[0]), "=r"(sg[1]), "=r"(sg[2]), "=r"(sg[3])
+                           : "r"(mseg + x * 4));
+              unsigned long long bits = 0ull;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) bits |= (unsigned long long)(sg[i] == myseg) << i;
+              vis |= bits << x;
+            }
           }
           vis = myseg > 0 ? (vis & cw) : 0ull;
         }
+      }
+      if (!__all_sync(0xffffffffu, vis == all1)) {
         const uint32_t v0 = uint32_t(vis), v1 = uint32_t(vis >> 32);
 #pragma unroll
         for (int x = 0; x < BN; ++x) {
@@ -873,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O is rescaled only when the max grew by more than 2^8 (rare), after
       // PV(g-1) has landed
       if (__any_sync(0xffffffffu, need) && j >= 1) {
-        if (!fail && !wait_or_abort(&pv_done[rb][(g - 1) & 1], ((g - 1) >> 1) & 1, p.err, abort_flag))
+        if (!fail && !wait_or_abort(&pv_done[rb][(g - 1) % NS], ((g - 1) / NS) & 1, p.err, abort_flag))
           fail = true;
         __syncwarp();
         tc_fence_after();
@@ -892,10 +913,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < BN / 2; ++i)
         v[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-      tmem_st32(tS(rb, g & 1) + lane_base, v);
+      tmem_st32(tS(rb, g % NS) + lane_base, v);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[rb][g & 1]);
+      mbar_arrive(&p_full[rb][g % NS]);
     }
     // post 1 / l for the epilogue warps (once they have taken the previous
     // item's) and write the row's log-sum-exp
@@ -1018,7 +1039,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   tile_meta_kernel<<<(ns + 3) / 4, 128, 0, stream>>>(a.seg_ids, a.sink, a.T, pd.n_kt, meta, a.batch);
   const int nq = a.batch * pd.n_span;
   tile_plan_kernel<<<(nq + 3) / 4, 128, 0, stream>>>(meta, p, plan);
-  auto kern = prefill_tc_kernel<D>;
+  auto kern = a.block > 0 ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (or per item, when there are fewer items)
