@@ -418,10 +418,12 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
 # ----------------------------------------------------------------------------
 
 def e2e_decode(torch, nd, state, B, Hq, Hkv, d, S, W, steps, warmup):
-    """Same step through the public API with host inputs: pinned host -> device
-    copy of the step's query and new token, append + decode, device -> host copy
-    of the output, all inside the timed region."""
-    reps, ws = state
+    """Same step through the public API with host buffers: one
+    nd_swa_sink_decode_step_host call per step, which enqueues the pinned
+    host -> device copies of the step's query and new token, the append +
+    decode and the device -> host copy of the output; all inside the timed
+    region."""
+    reps, _ = state
     r = reps[0]
     qh = torch.empty((steps + warmup, B, Hq, d), dtype=torch.bfloat16).pin_memory()
     kh = torch.empty((steps + warmup, B, Hkv, d), dtype=torch.bfloat16).pin_memory()
@@ -430,13 +432,13 @@ def e2e_decode(torch, nd, state, B, Hq, Hkv, d, S, W, steps, warmup):
     for t_ in (qh, kh, vh):
         t_.copy_(torch.randn(t_.shape).to(torch.bfloat16))
     stream = torch.cuda.current_stream()
+    ws = torch.empty(nd.nd_swa_sink_decode_step_host_workspace_size(B, Hq, Hkv, d, S + W),
+                     dtype=torch.uint8, device="cuda")
+    st = r["cache"].struct()
 
     def one(i):
-        r["q"].copy_(qh[i], non_blocking=True)
-        r["kn"].copy_(kh[i], non_blocking=True)
-        r["vn"].copy_(vh[i], non_blocking=True)
-        nd.nd_swa_sink_decode_step(r["q"], r["cache"], r["kn"], r["vn"], W, out=r["out"], workspace=ws)
-        oh[i].copy_(r["out"], non_blocking=True)
+        nd.nd_swa_sink_decode_step_host(qh[i], r["cache"], kh[i], vh[i], W, oh[i], workspace=ws,
+                                        stream=stream, cache_struct=st)
 
     for i in range(warmup):
         one(i)

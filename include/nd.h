@@ -185,6 +185,35 @@ ND_API int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache,
                                    size_t workspace_bytes, nd_stream_t stream);
 
 /*
+ * nd_swa_sink_decode_step with the step's inputs and outputs in host memory,
+ * for a caller whose token and query live on the host: the call enqueues on
+ * `stream` the copies of q, k_new and v_new to the device (one
+ * cudaMemcpyAsync each), the step exactly as nd_swa_sink_decode_step, and the
+ * copies of out (and lse, when lse_host is not NULL) back to the host.  The
+ * host results are valid once the stream has passed the call (synchronise
+ * the stream, or an event recorded after the call).  Page-locked host
+ * buffers let the copies run asynchronously; pageable ones are still
+ * correct but make the copies synchronous.
+ *   q_host, out_host        bf16 [batch][n_q_heads][head_dim], host memory
+ *   k_new_host, v_new_host  bf16 [batch][n_kv_heads][head_dim], host memory
+ *   lse_host                fp32 [batch][n_q_heads], host memory, or NULL
+ * The device staging buffers and the decode's split scratch are carved from
+ * `workspace` (device, 16-byte aligned), which must hold
+ * nd_swa_sink_decode_step_host_workspace_size(batch, n_q_heads, n_kv_heads,
+ * head_dim, sink_cap + ring_cap) bytes, else ND_ERR_WORKSPACE.  Other errors
+ * as nd_swa_sink_decode_step; a NULL host pointer (lse_host excepted) is
+ * ND_ERR_INVALID_ARG.
+ */
+ND_API size_t nd_swa_sink_decode_step_host_workspace_size(int batch, int n_q_heads,
+                                                          int n_kv_heads, int head_dim,
+                                                          int max_slots);
+ND_API int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *cache,
+                                        const void *k_new_host, const void *v_new_host,
+                                        int n_q_heads, int window, void *out_host,
+                                        float *lse_host, void *workspace,
+                                        size_t workspace_bytes, nd_stream_t stream);
+
+/*
  * nd_swa_sink_decode without a workspace argument.  The pages have no
  * counterpart: this is a library convenience for callers that cannot
  * allocate device memory -- a thread recording a CUDA graph with a frozen

@@ -185,27 +185,12 @@ int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, i
                               device_error_word(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache, const void *k_new,
-                            const void *v_new, int n_q_heads, int window, void *out, float *lse,
-                            void *workspace, size_t workspace_bytes, nd_stream_t stream) {
-  int st = validate_cache(cache);
-  if (st != ND_OK) return st;
-  if (window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return ND_ERR_INVALID_ARG;
-  const int G = n_q_heads / cache->n_kv_heads;
-  if (G > 8) return ND_ERR_UNSUPPORTED;
-  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
-  if (cache->ring_cap <= 0) return ND_ERR_INVALID_ARG;
-  if (cache->batch == 0) return ND_OK;
-  if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
-  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ND_ERR_INVALID_ARG;
+// Shared by nd_swa_sink_decode_step and its host-buffer form; every pointer
+// is a device pointer and the arguments are already validated.
+static int decode_step_device(const void *q, const nd_kv_cache *cache, const void *k_new,
+                              const void *v_new, int n_q_heads, int window, void *out, float *lse,
+                              void *workspace, size_t workspace_bytes, cudaStream_t s) {
   const int max_slots = cache->sink_cap + cache->ring_cap;
-  DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim);
-  if (pl.n_split > 1) {
-    size_t need = size_t(cache->batch) * n_q_heads * pl.n_split * (cache->head_dim + 2) * sizeof(float);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ND_ERR_WORKSPACE;
-  }
-  if ((st = check_device(nullptr)) != ND_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int *err = device_error_word();
   if (decode_step_fuses(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim))
     return finish(launch_decode(q, *cache, n_q_heads, window, out, lse, workspace, workspace_bytes, err, s,
@@ -213,6 +198,97 @@ int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache, const void 
   cudaError_t e = launch_kv_append_quant(*cache, k_new, v_new, 0, err, s);
   if (e != cudaSuccess) return finish(e);
   return finish(launch_decode(q, *cache, n_q_heads, window, out, lse, workspace, workspace_bytes, err, s));
+}
+
+// Argument checks shared by both forms of the step (pointer alignment is
+// checked where the pointers are device pointers).
+static int check_step_args(const nd_kv_cache *cache, int n_q_heads, int window) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return ND_ERR_INVALID_ARG;
+  const int G = n_q_heads / cache->n_kv_heads;
+  if (G > 8) return ND_ERR_UNSUPPORTED;
+  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
+  if (cache->ring_cap <= 0) return ND_ERR_INVALID_ARG;
+  return ND_OK;
+}
+
+static size_t split_scratch_bytes(const nd_kv_cache *cache, int n_q_heads) {
+  const int max_slots = cache->sink_cap + cache->ring_cap;
+  DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim);
+  return pl.n_split > 1 ? size_t(cache->batch) * n_q_heads * pl.n_split * (cache->head_dim + 2) * sizeof(float)
+                        : 0;
+}
+
+int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache, const void *k_new,
+                            const void *v_new, int n_q_heads, int window, void *out, float *lse,
+                            void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+  int st = check_step_args(cache, n_q_heads, window);
+  if (st != ND_OK) return st;
+  if (cache->batch == 0) return ND_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ND_ERR_INVALID_ARG;
+  const size_t need = split_scratch_bytes(cache, n_q_heads);
+  if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return ND_ERR_WORKSPACE;
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  return decode_step_device(q, cache, k_new, v_new, n_q_heads, window, out, lse, workspace, workspace_bytes,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Device staging for the host-buffer step, at the front of its workspace:
+// q, k_new, v_new, out, lse, each rounded to 256 bytes, then the decode's own
+// split scratch.
+struct HostStepLayout {
+  size_t q, kn, vn, out, lse, split, total;
+};
+static HostStepLayout host_step_layout(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int max_slots) {
+  HostStepLayout L;
+  const size_t qb = size_t(batch) * n_q_heads * head_dim * 2, kb = size_t(batch) * n_kv_heads * head_dim * 2;
+  L.q = 0;
+  L.kn = L.q + round_up(qb, 256);
+  L.vn = L.kn + round_up(kb, 256);
+  L.out = L.vn + round_up(kb, 256);
+  L.lse = L.out + round_up(qb, 256);
+  L.split = L.lse + round_up(size_t(batch) * n_q_heads * sizeof(float), 256);
+  L.total = L.split + decode_workspace_bytes(batch, n_q_heads, head_dim, max_slots, n_kv_heads);
+  return L;
+}
+
+size_t nd_swa_sink_decode_step_host_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                                   int head_dim, int max_slots) {
+  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || max_slots <= 0) return 0;
+  return host_step_layout(batch, n_q_heads, n_kv_heads, head_dim, max_slots).total;
+}
+
+int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *cache, const void *k_new_host,
+                                 const void *v_new_host, int n_q_heads, int window, void *out_host,
+                                 float *lse_host, void *workspace, size_t workspace_bytes,
+                                 nd_stream_t stream) {
+  int st = check_step_args(cache, n_q_heads, window);
+  if (st != ND_OK) return st;
+  if (cache->batch == 0) return ND_OK;
+  if (!q_host || !k_new_host || !v_new_host || !out_host) return ND_ERR_INVALID_ARG;
+  const int B = cache->batch, Hkv = cache->n_kv_heads, d = cache->head_dim;
+  const HostStepLayout L = host_step_layout(B, n_q_heads, Hkv, d, cache->sink_cap + cache->ring_cap);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return ND_ERR_WORKSPACE;
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  const size_t qb = size_t(B) * n_q_heads * d * 2, kb = size_t(B) * Hkv * d * 2;
+  // one cudaMemcpyAsync per buffer
+  cudaError_t e = cudaMemcpyAsync(ws + L.q, q_host, qb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.kn, k_new_host, kb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.vn, v_new_host, kb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return finish(e);
+  float *lse_dev = lse_host ? reinterpret_cast<float *>(ws + L.lse) : nullptr;
+  st = decode_step_device(ws + L.q, cache, ws + L.kn, ws + L.vn, n_q_heads, window, ws + L.out, lse_dev,
+                          ws + L.split, workspace_bytes - L.split, s);
+  if (st != ND_OK) return st;
+  e = cudaMemcpyAsync(out_host, ws + L.out, qb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && lse_host)
+    e = cudaMemcpyAsync(lse_host, lse_dev, size_t(B) * n_q_heads * sizeof(float), cudaMemcpyDeviceToHost, s);
+  return finish(e);
 }
 
 size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,

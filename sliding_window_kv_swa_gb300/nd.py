@@ -71,6 +71,8 @@ def _lib():
             "nd_swa_sink_decode": (I, [P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_decode_noalloc": (I, [P, P, I, I, P, P, P]),
             "nd_swa_sink_decode_step": (I, [P, P, P, P, I, I, P, P, P, S, P]),
+            "nd_swa_sink_decode_step_host_workspace_size": (S, [I, I, I, I, I]),
+            "nd_swa_sink_decode_step_host": (I, [P, P, P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
@@ -93,6 +95,7 @@ def library_path() -> str:
 EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_errors",
             "nd_kv_append_quant", "nd_kv_quant_rows", "nd_swa_sink_decode_workspace_size",
             "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_decode_step",
+            "nd_swa_sink_decode_step_host_workspace_size", "nd_swa_sink_decode_step_host",
             "nd_swa_sink_prefill_workspace_size",
             "nd_swa_sink_prefill",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
@@ -242,6 +245,38 @@ def nd_swa_sink_decode_step(q: torch.Tensor, cache: KVCache, k_new: torch.Tensor
         _ptr(q), ctypes.byref(s), _ptr(k_new), _ptr(v_new), Hq, int(window), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def nd_swa_sink_decode_step_host_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                                                max_slots: int) -> int:
+    return int(_lib().nd_swa_sink_decode_step_host_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                                                  max_slots))
+
+
+def nd_swa_sink_decode_step_host(q_host: torch.Tensor, cache: KVCache, k_new_host: torch.Tensor,
+                                 v_new_host: torch.Tensor, window: int, out_host: torch.Tensor,
+                                 lse_host: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                                 stream=None, cache_struct=None) -> torch.Tensor:
+    """nd_swa_sink_decode_step with q / k_new / v_new / out (/ lse) in host
+    memory (CPU tensors, page-locked for asynchronous copies): the copies and
+    the step are enqueued on the stream; out_host is valid once the stream
+    has passed the call.  cache_struct: cache.struct(), built once by a
+    caller that repeats the call on the same cache."""
+    for t, name in ((q_host, "q_host"), (k_new_host, "k_new_host"), (v_new_host, "v_new_host"),
+                    (out_host, "out_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    B, Hq, d = q_host.shape
+    if workspace is None:
+        nbytes = nd_swa_sink_decode_step_host_workspace_size(B, Hq, cache.n_kv_heads, d,
+                                                             cache.sink_cap + cache.ring_cap)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=cache.k_codes.device)
+    s = cache_struct if cache_struct is not None else cache.struct()
+    _check("nd_swa_sink_decode_step_host", _lib().nd_swa_sink_decode_step_host(
+        q_host.data_ptr(), ctypes.byref(s), k_new_host.data_ptr(), v_new_host.data_ptr(), Hq, int(window),
+        out_host.data_ptr(), None if lse_host is None else lse_host.data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream(stream)))
+    return out_host
 
 
 NOALLOC_SCRATCH_BYTES = 512 << 10   # ND_NOALLOC_SCRATCH_BYTES in nd.h

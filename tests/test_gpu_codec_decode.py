@@ -259,3 +259,38 @@ def test_decode_step_matches_append_then_decode(B, Hq, Hkv, d, S, W, fill):
     np.testing.assert_array_equal(host(cache.v_codes), ref.v_codes)
     np.testing.assert_array_equal(host(cache.k_scale), ref.k_scale)
     np.testing.assert_array_equal(host(cache.v_scale), ref.v_scale)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,S,W", [
+    (64, 8, 2, 64, 64, 256),     # fused step
+    (10, 32, 8, 128, 64, 32),    # append and decode as two launches
+])
+def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W):
+    """nd_swa_sink_decode_step_host: q, the new token and the output (and lse)
+    in page-locked host memory, copies enqueued by the call; same results as
+    the oracle's append + decode, cache bit-exact."""
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=760 + B + d, full=True)
+    ref = oracle_cache(w, S, W)
+    cache = device_cache(ref)
+    st = cache.struct()
+    ws = torch.empty(nd().nd_swa_sink_decode_step_host_workspace_size(B, Hq, Hkv, d, S + W),
+                     dtype=torch.uint8, device="cuda")
+    rng = philox(761 + B)
+    out_h = torch.empty((B, Hq, d), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    for step in range(3):
+        kb, kf = normal_bf16(rng, (B, Hkv, d))
+        vb, vf = normal_bf16(rng, (B, Hkv, d))
+        qb, qf = normal_bf16(rng, (B, Hq, d))
+        pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+        nd().nd_swa_sink_decode_step_host(pin(qb), cache, pin(kb), pin(vb), W, out_h, lse_host=lse_h,
+                                          workspace=ws, cache_struct=st)
+        torch.cuda.current_stream().synchronize()
+        oracle.kv_append(ref, kf, vf, False)
+        want, wlse = oracle.decode(qf, ref, W)
+        assert_close_bf16(out_h.float().numpy(), want, f"host step {step}")
+        np.testing.assert_allclose(lse_h.numpy(), wlse, atol=2e-3, rtol=0)
+    np.testing.assert_array_equal(host(cache.k_codes), ref.k_codes)
+    np.testing.assert_array_equal(host(cache.v_scale), ref.v_scale)
+    for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
+        np.testing.assert_array_equal(host(getattr(cache, f)), getattr(ref, f), err_msg=f)
