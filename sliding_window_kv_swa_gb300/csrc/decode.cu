@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 
 // Warps per CTA: 16 at head_dim 64 (one CTA per SM covers a whole short
 // sequence in one or two steps per warp), 4 at head_dim 128 (three CTAs per SM).
-constexpr int warps_for(int D) { return D == 64 ? 16 : 4; }
+constexpr int warps_for(int D) { return D == 64 ? 20 : 4; }
 
 template <int D, int NW>
 size_t decode_smem_bytes() {

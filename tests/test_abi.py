@@ -93,8 +93,8 @@ def test_host_validation_before_any_device_work():
                                   ctypes.c_size_t(0), None) == 1
     assert lib.nd_swa_sink_decode(P(16), ctypes.byref(cache), 16, 8, P(16), None, None,
                                   ctypes.c_size_t(0), None) == 2
-    # workspace required when the decode splits (1 sequence, 64 + 256 slots)
-    big = nd.nd._Cache(1, 1, 64, 64, 256, 16, 16, 16, 16, 16, 16, 16, 16)
+    # workspace required when the decode splits (1 sequence, 64 + 1024 slots)
+    big = nd.nd._Cache(1, 1, 64, 64, 1024, 16, 16, 16, 16, 16, 16, 16, 16)
     assert lib.nd_swa_sink_decode(P(16), ctypes.byref(big), 4, 256, P(16), None, None,
                                   ctypes.c_size_t(0), None) == 4
     # append: head_dim not a multiple of 32
@@ -107,8 +107,11 @@ def test_workspace_sizes():
     # one CTA per (sequence, KV head) once that fills half the GPU: no split
     assert nd.nd_swa_sink_decode_workspace_size(64, 8, 2, 64, 320) == 0
     assert nd.nd_swa_sink_decode_workspace_size(512, 32, 8, 128, 1280) == 0
-    # 8 sequences x 2 KV heads: two-way split, (64+2) floats per partial
-    assert nd.nd_swa_sink_decode_workspace_size(8, 8, 2, 64, 320) == 8 * 8 * 2 * 66 * 4
+    # 8 sequences x 2 KV heads, 320 slots: one 16-slot step for each of the
+    # 20 warps already, no split; 1088 slots (68 steps): four-way split,
+    # (64+2) floats per partial
+    assert nd.nd_swa_sink_decode_workspace_size(8, 8, 2, 64, 320) == 0
+    assert nd.nd_swa_sink_decode_workspace_size(8, 8, 2, 64, 1088) == 8 * 8 * 4 * 66 * 4
     # prefill with rotation keeps rotated copies of q and k
     n = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, 1, 512, 4, 1, 64, 10000.0, 0)
     assert n >= 512 * 4 * 64 * 4 + 512 * 1 * 64 * 4

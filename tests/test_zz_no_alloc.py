@@ -33,9 +33,10 @@ def _device_cache(nd, w, S, W):
 def test_noalloc_decode_matches_workspace_decode_on_two_calls():
     need_gpu()
     import sliding_window_kv_swa_gb300 as nd
-    S, W = 64, 256
-    # 8 sequences x 2 KV heads are too few to fill the GPU, so the decode
-    # splits each sequence's slots and needs scratch for the partials
+    S, W = 64, 1024
+    # 8 sequences x 2 KV heads are too few to fill the GPU and 1088 slots are
+    # more than one step per warp, so the decode splits each sequence's slots
+    # and needs scratch for the partials
     w = decode_cache(8, 8, 2, 64, S, W, seed=2023, full=True)
     B, Hq, d = w["q"].shape
     cache = _device_cache(nd, w, S, W)
