@@ -339,6 +339,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
       "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -877,18 +885,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mx;
       }
       const float mc = m_used == -INFINITY ? 0.f : m_used * c;
-      // p = 2^(s c - m c), two scores per packed fp32 FMA / add
+      // p = 2^(s c - m c), two scores per packed fp32 FMA / add; P(g) as bf16
+      // pairs over the front of S(g)'s buffer (already read out), the A
+      // operand of the block's PV.  At d = 64 (softmax-bound) P is stored in
+      // two halves so the first store runs while the second half is
+      // computed; at d = 128 one store measured faster.
       const uint64_t c2 = pack_f32x2(c, c), nmc2 = pack_f32x2(-mc, -mc);
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (D == 64) {
 #pragma unroll
-      for (int x = 0; x < BN; x += 2) {
-        float a, bb;
-        fma_f32x2(a, bb, __uint_as_float(v[x]), __uint_as_float(v[x + 1]), c2, nmc2);
-        a = ex2(a);
-        bb = ex2(bb);
-        add_f32x2(rsp[(x >> 1) & 1 ? 2 : 0], rsp[(x >> 1) & 1 ? 3 : 1], a, bb);
-        v[x] = __float_as_uint(a);
-        v[x + 1] = __float_as_uint(bb);
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int x = 32 * hh; x < 32 * hh + 32; x += 2) {
+            float a, bb;
+            fma_f32x2(a, bb, __uint_as_float(v[x]), __uint_as_float(v[x + 1]), c2, nmc2);
+            a = ex2(a);
+            bb = ex2(bb);
+            add_f32x2(rsp[(x >> 1) & 1 ? 2 : 0], rsp[(x >> 1) & 1 ? 3 : 1], a, bb);
+            v[x] = __float_as_uint(a);
+            v[x + 1] = __float_as_uint(bb);
+          }
+          // keys 32hh..32hh+31 -> v[32hh .. 32hh+15] (reads never behind writes)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            v[32 * hh + i] = pack_bf16x2(__uint_as_float(v[32 * hh + 2 * i]), __uint_as_float(v[32 * hh + 2 * i + 1]));
+          tmem_st16(tS(rb, g % NS) + lane_base + 16 * hh, v + 32 * hh);
+        }
+      } else {
+#pragma unroll
+        for (int x = 0; x < BN; x += 2) {
+          float a, bb;
+          fma_f32x2(a, bb, __uint_as_float(v[x]), __uint_as_float(v[x + 1]), c2, nmc2);
+          a = ex2(a);
+          bb = ex2(bb);
+          add_f32x2(rsp[(x >> 1) & 1 ? 2 : 0], rsp[(x >> 1) & 1 ? 3 : 1], a, bb);
+          v[x] = __float_as_uint(a);
+          v[x + 1] = __float_as_uint(bb);
+        }
       }
       l += (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       // O is rescaled only when the max grew by more than 2^8 (rare), after
@@ -908,12 +941,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO(rb) + lane_base + x, ov);
         }
       }
-      // P(g) as bf16 pairs over the front of S(g)'s buffer (already read out),
-      // the A operand of the block's PV
+      if constexpr (D != 64) {
 #pragma unroll
-      for (int i = 0; i < BN / 2; ++i)
-        v[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-      tmem_st32(tS(rb, g % NS) + lane_base, v);
+        for (int i = 0; i < BN / 2; ++i)
+          v[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        tmem_st32(tS(rb, g % NS) + lane_base, v);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[rb][g % NS]);
