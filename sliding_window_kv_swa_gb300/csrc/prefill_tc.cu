@@ -53,9 +53,9 @@ namespace {
 
 constexpr int BM = 128;  // rows per block = TMEM lanes
 constexpr int BN = 64;   // keys per tile
-// warps 0-7 softmax (block 0: 0-3, block 1: 4-7), 8 loader, 9-10 MMA issuers
-// (block 0, block 1), 11 idle, 12-15 epilogue
-constexpr int kWarpLoad = 8, kWarpMma0 = 9, kWarpEpi0 = 12;
+// warps 0-7 softmax (block 0: 0-3, block 1: 4-7), 8 Q/K loader, 9-10 MMA
+// issuers (block 0, block 1), 11 V loader, 12-15 epilogue
+constexpr int kWarpLoad = 8, kWarpMma0 = 9, kWarpLoadV = 11, kWarpEpi0 = 12;
 constexpr int kThreads = 16 * 32;
 // Register split (setmaxnreg, per warpgroup): the softmax warpgroups hold a
 // 64-score row per thread; the loader / issuer and epilogue warpgroups need
@@ -534,13 +534,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
   // loader / issuer / epilogue warpgroups: registers to the softmax warpgroups
   regs_dec<kRegsOther>();
-  if (warp == kWarpLoad) {
-    // ------------------------------------------------ TMA loader
-    //   Q: two buffers, so item i+1's Q lands while item i runs.  Rings: K
-    //   tiles (NK stages, freed once both blocks' S MMAs read them), V tiles
-    //   (NV stages, freed after both blocks' PV) and tile records (NM stages,
-    //   freed once all eight softmax warps built their masks).  The warp
-    //   stays converged; the elected lane issues.
+  // at d = 64 (shallower tiles, deeper rings) one warp loads both and measured
+  // slightly faster; warp 11 then idles
+  constexpr bool kSplitLoad = D == 128;
+  if (warp == kWarpLoad || (kSplitLoad && warp == kWarpLoadV)) {
+    // ------------------------------------------------ TMA loaders
+    //   Warp 8: Q (two buffers, so item i+1's Q lands while item i runs), K
+    //   tiles (NK stages, freed once both blocks' S MMAs read them) and tile
+    //   records (NM stages, freed once all eight softmax warps built their
+    //   masks).  Warp 11: V tiles (NV stages, freed after both blocks' PV).
+    //   Two warps, so the K ring never waits behind the V ring (at an item
+    //   boundary the next item's first K tiles go out as soon as K slots
+    //   free).  Each warp stays converged; the elected lane issues.
+    const bool vwarp = warp == kWarpLoadV;
     const uint32_t leader = elect_one();
     int gt = 0;  // tiles loaded before the current item
     auto load_q = [&](int w, int it) {
@@ -555,11 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    if (blockIdx.x < n_items) fail = !load_q(blockIdx.x, 0);
+    if (!vwarp && blockIdx.x < n_items) fail = !load_q(blockIdx.x, 0);
     for (int w = blockIdx.x, it = 0; w < n_items && !fail; w += gridDim.x, ++it) {
       const Item I = item_at(w);
-      // K runs one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...  Ring
-      // positions and phases follow the running tile count g.
+      // Ring positions and phases follow the running tile count g.
       auto load_k = [&](int j) {
         const int e = I.tiles[j];
         const bool pooled = kPooled && ((e >> 20) & 1);
@@ -596,10 +601,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // that Q buffer, are done or nearly so)
       const int jq = I.n < NK - 1 ? I.n : NK - 1;
       const bool more = w + int(gridDim.x) < n_items;
-      for (int j = 0; j <= I.n && !fail; ++j) {
-        if (j < I.n && !load_k(j)) fail = true;
-        if (!fail && j >= 1 && !load_v(j - 1)) fail = true;
-        if (!fail && j == jq && more && !load_q(w + gridDim.x, it + 1)) fail = true;
+      if (vwarp) {
+        for (int j = 0; j < I.n && !fail; ++j)
+          if (!load_v(j)) fail = true;
+      } else {
+        // (one warp: K runs one tile ahead of V: K(0), K(1), V(0), K(2), ...)
+        for (int j = 0; j <= I.n && !fail; ++j) {
+          if (j < I.n && !load_k(j)) fail = true;
+          if (!kSplitLoad && !fail && j >= 1 && !load_v(j - 1)) fail = true;
+          if (!fail && j == jq && more && !load_q(w + gridDim.x, it + 1)) fail = true;
+        }
       }
       gt += I.n;
     }
