@@ -76,15 +76,13 @@ __device__ __forceinline__ void cluster_wait() {
 // code = clamp(rint(x/scale), +-127), IEEE fp32 divides -- the same
 // arithmetic as the append kernel, so the codes agree bit for bit.
 template <int D>
-__device__ __forceinline__ void quant_row_regs(const uint16_t *src, int lane, int *code, float &scale) {
+__device__ __forceinline__ void quant_row_regs(uint2 w, int lane, int *code, float &scale) {
   constexpr int CPL = D / 32, kLanesPerGroup = 32 / CPL;
   float x[CPL];
   if constexpr (CPL == 4) {
-    const uint2 w = reinterpret_cast<const uint2 *>(src)[lane];
     x[0] = bf16_lo(w.x), x[1] = bf16_hi(w.x), x[2] = bf16_lo(w.y), x[3] = bf16_hi(w.y);
   } else {
-    const uint32_t w = reinterpret_cast<const uint32_t *>(src)[lane];
-    x[0] = bf16_lo(w), x[1] = bf16_hi(w);
+    x[0] = bf16_lo(w.x), x[1] = bf16_hi(w.x);
   }
   float amax = 0.f;
 #pragma unroll
@@ -98,6 +96,13 @@ __device__ __forceinline__ void quant_row_regs(const uint16_t *src, int lane, in
     if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
     code[i] = int(r);
   }
+}
+
+// This lane's channels (D/32 of them, bf16) of one token row.
+template <int D>
+__device__ __forceinline__ uint2 load_row_words(const uint16_t *src, int lane) {
+  if constexpr (D / 32 == 4) return reinterpret_cast<const uint2 *>(src)[lane];
+  else return make_uint2(reinterpret_cast<const uint32_t *>(src)[lane], 0u);
 }
 
 template <int D>
@@ -167,6 +172,13 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
   const size_t pair = size_t(b) * c.n_kv_heads + hkv;
 
   const bool fused = p.k_new != nullptr;
+  // the appended token, read now so its latency hides behind the metadata
+  // read (only the warp that owns the new slot uses it)
+  uint2 k_row = make_uint2(0u, 0u), v_row = make_uint2(0u, 0u);
+  if (fused) {
+    k_row = load_row_words<D>(p.k_new + pair * D, lane);
+    v_row = load_row_words<D>(p.v_new + pair * D, lane);
+  }
   if (threadIdx.x == 0) {
     int sl = c.sink_len[b], rs = c.ring_start[b], rl = c.ring_len[b];
     const bool sane = sl >= 0 && sl <= c.sink_cap && rl >= 0 && rl <= c.ring_cap && rs >= 0 &&
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       for (int which = 0; which < 2; ++which) {
         int code[CPL];
         float scale;
-        quant_row_regs<D>((which ? p.v_new : p.k_new) + pair * D, lane, code, scale);
+        quant_row_regs<D>(which ? v_row : k_row, lane, code, scale);
         uint32_t packed = 0;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) packed |= uint32_t(code[i] & 0xff) << (8 * i);
