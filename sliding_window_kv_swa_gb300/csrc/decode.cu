@@ -173,9 +173,11 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
 
   const bool fused = p.k_new != nullptr;
   // the appended token, read now so its latency hides behind the metadata
-  // read (only the warp that owns the new slot uses it)
+  // read (only the warp that owns the new slot uses it).  At d = 128 the two
+  // live registers cost the large-batch decode more than the early read
+  // saves, so there the owning warp reads it when it needs it.
   uint2 k_row = make_uint2(0u, 0u), v_row = make_uint2(0u, 0u);
-  if (fused) {
+  if (D == 64 && fused) {
     k_row = load_row_words<D>(p.k_new + pair * D, lane);
     v_row = load_row_words<D>(p.v_new + pair * D, lane);
   }
@@ -329,7 +331,9 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
       for (int which = 0; which < 2; ++which) {
         int code[CPL];
         float scale;
-        quant_row_regs<D>(which ? v_row : k_row, lane, code, scale);
+        const uint2 row_w = D == 64 ? (which ? v_row : k_row)
+                                    : load_row_words<D>((which ? p.v_new : p.k_new) + pair * D, lane);
+        quant_row_regs<D>(row_w, lane, code, scale);
         uint32_t packed = 0;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) packed |= uint32_t(code[i] & 0xff) << (8 * i);
