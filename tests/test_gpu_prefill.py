@@ -134,6 +134,36 @@ def test_bf16_zero_gap_inside_segment(window):
     assert_close_bf16(out, want, f"zero gap W={window}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (3, 1, 64)])
+def test_bf16_empty_spans(Hq, Hkv, d):
+    """Row spans with no visible key at all (segment id 0 over whole 128-row
+    blocks, in the middle and at the end): their work items have no tiles,
+    output 0 and lse -inf, and the items after them (sharing the persistent
+    CTAs' barrier phases and O buffers) stay exact."""
+    rng = philox(930 + d)
+    B, T = 2, 1000
+    qb, q = normal_bf16(rng, (B, T, Hq, d))
+    kb, k = normal_bf16(rng, (B, T, Hkv, d))
+    vb, v = normal_bf16(rng, (B, T, Hkv, d))
+    seg = np.ones((B, T), np.int32)
+    seg[0, 256:512] = 0          # two whole 128-row blocks
+    seg[0, 512:] = 2             # then a new segment
+    seg[1, 640:] = 0             # a padded tail, including the ragged last block
+    sink = np.zeros((B, T), np.uint8)
+    sink[:, :8] = 1
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
+    out = host(nd().nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), dev(sink), 128,
+                                        lse=lse))
+    assert np.all(out[0, 256:512] == 0) and np.all(out[1, 640:] == 0)
+    assert np.all(np.isneginf(host(lse)[0, :, 256:512]))
+    want, wlse = oracle.swa_sink_prefill(q, k, v, seg, sink, 128)
+    assert_close_bf16(out, want, "empty spans")
+    got_lse = host(lse).transpose(0, 2, 1)
+    fin = np.isfinite(wlse)
+    assert np.array_equal(fin, np.isfinite(got_lse))
+    np.testing.assert_allclose(got_lse[fin], wlse[fin], atol=2e-2, rtol=0)
+
+
 def test_bf16_many_segments_per_tile():
     """Tiles holding more than four segment ids (short segments, ids
     repeating out of order) and tiles holding two to four."""
