@@ -369,7 +369,7 @@ def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
                 frac=flops / t / 1e12 / pk["bf16"], visible_pairs=pairs, flops_per_step=flops,
                 attn_ms=ms_attn / steps, tiles=tiles * Hq, tile_flops=tile_flops,
                 tile_tflops=tile_flops / ta / 1e12, tile_frac=tile_flops / ta / 1e12 / pk["bf16"],
-                launches=5 * steps)
+                launches=4 * steps)
 
 
 def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
@@ -410,7 +410,7 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
                 tok_s=B * T / t, tflops=flops / t / 1e12, frac=flops / t / 1e12 / pk["bf16"],
                 visible_pairs=pairs, attn_ms=ms_attn / steps, tiles=tiles, tile_flops=tile_flops,
                 tile_tflops=tile_flops / ta / 1e12, tile_frac=tile_flops / ta / 1e12 / pk["bf16"],
-                launches=6 * steps)
+                launches=5 * steps)
 
 
 # ----------------------------------------------------------------------------

@@ -65,7 +65,7 @@ static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther == kThreads * 128, "
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 
 // Per (sequence, 64-key tile) metadata record, written once per call by
-// tile_meta_kernel and copied asynchronously into shared memory by the loader
+// tile_prep_kernel and copied asynchronously into shared memory by the loader
 // next to the tile's K/V: segment ids, sink flags and summary flags.
 struct alignas(128) TileMeta {
   int seg[BN];                     // 0 for keys past T
@@ -93,13 +93,11 @@ struct TcParams {
 
 // ------------------------------------------------------------------ plan
 
-// One warp per (sequence, key tile); lane l handles keys l and l + 32.
-__global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T, int n_kt,
-                                 TileMeta *meta, int B) {
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (w >= B * n_kt) return;
-  const int b = w / n_kt, j = w % n_kt;
-  TileMeta &m = meta[w];
+// One warp builds the record of key tile j of sequence b; lane l handles keys
+// l and l + 32.  Returns (to every lane) the tile's positive segment-id range
+// and whether it holds a sink, for the plan.
+__device__ void build_tile_meta(const int32_t *seg, const uint8_t *sink, int T, int b, int j, int lane,
+                                TileMeta &m, int &seg_lo, int &seg_hi, int &any_sink) {
   int lo = INT_MAX, hi = INT_MIN, all = 1, any = 0, padding = 0;
   uint32_t sink_word[2];
   int sv[2];
@@ -157,52 +155,69 @@ __global__ void tile_meta_kernel(const int32_t *seg, const uint8_t *sink, int T,
     m.uniform_seg = (lo == hi && !padding) ? lo : 0;
     m.n_ids = n_ids;
   }
+  seg_lo = lo;
+  seg_hi = hi;
+  any_sink = any;
 }
 
-// One warp per (sequence, row span): the key tiles any row of the span may
-// see, pooled tiles first (entry bit 20 set), then exact tiles, ascending.
-__global__ void tile_plan_kernel(const TileMeta *meta, TcParams p, int32_t *plan) {
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (w >= p.B * p.n_span) return;  // whole warps only
-  const int b = w / p.n_span, sp = w % p.n_span;
-  const int q0 = sp * p.span, q1 = min(p.T, q0 + p.span) - 1;
-  int32_t *out = plan + size_t(w) * p.plan_stride;
-  int n = 0;
-  if (p.block > 0) {
-    const int lim = q1 - p.W + 1;  // pooled column j visible iff (j+1)*block <= q - W + 1
-    const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
-    n = (ncol + BN - 1) / BN;
-    for (int j = lane; j < n; j += 32) out[1 + j] = (1 << 20) | j;
-  }
-  int qlo = INT_MAX, qhi = INT_MIN;
-  for (int q = q0 + lane; q <= q1; q += 32) {
-    const int s = p.seg ? p.seg[size_t(b) * p.T + q] : 1;
-    if (s > 0) {
-      qlo = min(qlo, s);
-      qhi = max(qhi, s);
+// One block per sequence: first the records of all its key tiles (kept in
+// global memory for the attention kernel and, as segment-id range and sink
+// flag, in shared memory), then one warp per row span lists the key tiles any
+// row of the span may see -- pooled tiles first (entry bit 20 set), then
+// exact tiles, ascending.  Dynamic shared memory: 3 ints per key tile.
+__global__ void __launch_bounds__(1024) tile_prep_kernel(TcParams p, TileMeta *meta, int32_t *plan) {
+  extern __shared__ int s_tile[];  // [3][n_kt]: seg_lo, seg_hi, any_sink
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int *t_lo = s_tile, *t_hi = s_tile + p.n_kt, *t_any = s_tile + 2 * p.n_kt;
+  for (int j = warp; j < p.n_kt; j += nw) {
+    int lo, hi, any;
+    build_tile_meta(p.seg, p.sink, p.T, b, j, lane, meta[size_t(b) * p.n_kt + j], lo, hi, any);
+    if (lane == 0) {
+      t_lo[j] = lo;
+      t_hi[j] = hi;
+      t_any[j] = any;
     }
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    qlo = min(qlo, __shfl_xor_sync(0xffffffffu, qlo, off));
-    qhi = max(qhi, __shfl_xor_sync(0xffffffffu, qhi, off));
-  }
-  if (qlo <= qhi) {
-    const int jmax = q1 / BN;
-    for (int j0 = 0; j0 <= jmax; j0 += 32) {
-      const int j = j0 + lane;
-      bool keep = false;
-      if (j <= jmax) {
-        const TileMeta &t = meta[size_t(b) * p.n_kt + j];
-        const bool in_window = p.W == 0 || (j + 1) * BN - 1 >= q0 - p.W + 1;
-        keep = t.seg_lo <= t.seg_hi && t.seg_lo <= qhi && t.seg_hi >= qlo && (in_window || t.any_sink);
+  __syncthreads();
+  for (int sp = warp; sp < p.n_span; sp += nw) {
+    const int q0 = sp * p.span, q1 = min(p.T, q0 + p.span) - 1;
+    int32_t *out = plan + (size_t(b) * p.n_span + sp) * p.plan_stride;
+    int n = 0;
+    if (p.block > 0) {
+      const int lim = q1 - p.W + 1;  // pooled column j visible iff (j+1)*block <= q - W + 1
+      const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
+      n = (ncol + BN - 1) / BN;
+      for (int j = lane; j < n; j += 32) out[1 + j] = (1 << 20) | j;
+    }
+    int qlo = INT_MAX, qhi = INT_MIN;
+    for (int q = q0 + lane; q <= q1; q += 32) {
+      const int s = p.seg ? p.seg[size_t(b) * p.T + q] : 1;
+      if (s > 0) {
+        qlo = min(qlo, s);
+        qhi = max(qhi, s);
       }
-      const unsigned m = __ballot_sync(0xffffffffu, keep);
-      if (keep) out[1 + n + __popc(m & ((1u << lane) - 1u))] = j;
-      n += __popc(m);
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      qlo = min(qlo, __shfl_xor_sync(0xffffffffu, qlo, off));
+      qhi = max(qhi, __shfl_xor_sync(0xffffffffu, qhi, off));
+    }
+    if (qlo <= qhi) {
+      const int jmax = q1 / BN;
+      for (int j0 = 0; j0 <= jmax; j0 += 32) {
+        const int j = j0 + lane;
+        bool keep = false;
+        if (j <= jmax) {
+          const bool in_window = p.W == 0 || (j + 1) * BN - 1 >= q0 - p.W + 1;
+          keep = t_lo[j] <= t_hi[j] && t_lo[j] <= qhi && t_hi[j] >= qlo && (in_window || t_any[j]);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (keep) out[1 + n + __popc(m & ((1u << lane) - 1u))] = j;
+        n += __popc(m);
+      }
+    }
+    if (lane == 0) out[0] = n;
   }
-  if (lane == 0) out[0] = n;
 }
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -1079,12 +1094,15 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
     tpk = tk;
     tpv = tv;
   }
-  const int ns = a.batch * pd.n_kt;
-  tile_meta_kernel<<<(ns + 3) / 4, 128, 0, stream>>>(a.seg_ids, a.sink, a.T, pd.n_kt, meta, a.batch);
-  const int nq = a.batch * pd.n_span;
-  tile_plan_kernel<<<(nq + 3) / 4, 128, 0, stream>>>(meta, p, plan);
+  // tile records and plan: one block per sequence
+  const size_t prep_smem = size_t(3) * pd.n_kt * sizeof(int);
+  cudaError_t e = cudaSuccess;
+  if (prep_smem > 48 * 1024)
+    e = cudaFuncSetAttribute(tile_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(prep_smem));
+  if (e != cudaSuccess) return e;
+  tile_prep_kernel<<<a.batch, 1024, prep_smem, stream>>>(p, meta, plan);
   auto kern = a.block > 0 ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (or per item, when there are fewer items)
   int sms = 0, dev = 0;
