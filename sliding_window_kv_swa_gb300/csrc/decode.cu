@@ -171,6 +171,12 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
   const int nslot = c.sink_cap + c.ring_cap;
   const size_t pair = size_t(b) * c.n_kv_heads + hkv;
 
+  // The launch allows programmatic dependent launch: this grid may be
+  // scheduled while the previous kernel on the stream is still running.
+  // Nothing above reads global memory; the wait returns once that kernel
+  // has completed and its writes (the cache, its metadata, q) are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   const bool fused = p.k_new != nullptr;
   // the appended token, read now so its latency hides behind the metadata
   // read (only the warp that owns the new slot uses it).  At d = 128 the two
@@ -470,6 +476,10 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const
   }
   cp_async_wait<0>();
 
+  // At d = 64 (one CTA per SM) the next kernel's CTAs may be scheduled from
+  // here on; at d = 128 three CTAs share an SM and early-placed CTAs of the
+  // next step crowd unevenly, so there the trigger stays implicit (exit).
+  if (D == 64) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- merge: quad-sum l, then the warps through shared memory (the stage
   //      buffers are free once every warp is past its loop)
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -580,25 +590,26 @@ cudaError_t launch_d(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
   auto kern = decode_kernel<D, NW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (p.k_new) {
     // one cluster per sequence: its (split, KV head) CTAs
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(NW * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = grid.x;
-    attr[0].val.clusterDim.y = grid.y;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p);
-    if (e != cudaSuccess) return e;
-  } else {
-    kern<<<grid, NW * 32, smem, stream>>>(p);
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = grid.x;
+    attr[1].val.clusterDim.y = grid.y;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   if (p.n_split > 1) decode_combine_kernel<D><<<p.c.batch * p.Hq, D, 0, stream>>>(p);
   return cudaGetLastError();
 }

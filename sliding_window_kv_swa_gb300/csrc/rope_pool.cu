@@ -28,9 +28,12 @@ struct Freqs {
 };
 
 __device__ __forceinline__ float2 rot_cs(double pos, double freq) {
-  const double two_pi = 6.283185307179586476925286766559;
+  const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
   double a = pos * freq;
-  a -= rint(a / two_pi) * two_pi;
+  // the quotient only picks the multiple of 2 pi to subtract: multiplying by
+  // 1 / (2 pi) instead of dividing can move it by one at a half-turn, which
+  // still leaves |a| <= pi (+ one ulp)
+  a = fma(-rint(a * inv_two_pi), two_pi, a);
   float s, c;
   sincosf(float(a), &s, &c);
   return make_float2(c, s);
