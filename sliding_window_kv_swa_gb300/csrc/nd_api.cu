@@ -298,7 +298,9 @@ size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int 
   const size_t esz = dtype == ND_F32 ? 4 : 2;
   size_t bytes = 0;
   if (rope_theta != 0.f) {
-    bytes += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
+    // rotated q (fp32 path only: the bf16 kernel rotates q as it stages it),
+    // rotated k, the angle table
+    if (dtype == ND_F32) bytes += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
     bytes += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
     bytes += round_up(rope_table_bytes(T, head_dim), 256);
   }
@@ -356,16 +358,21 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
   char *ws = static_cast<char *>(workspace);
   const size_t esz = dtype == ND_F32 ? 4 : 2;
   if (rope_theta != 0.f) {
-    void *qr = ws;
-    ws += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
+    const bool f32 = dtype == ND_F32;
+    void *qr = nullptr;
+    if (f32) {
+      qr = ws;
+      ws += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
+    }
     void *kr = ws;
     ws += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
     void *table = ws;
     ws += round_up(rope_table_bytes(T, head_dim), 256);
-    cudaError_t e = launch_rope_qk(q, qr, n_q_heads, k, kr, n_kv_heads, batch, T, head_dim,
-                                   rope_theta, dtype == ND_F32, table, s);
+    cudaError_t e = launch_rope_qk(f32 ? q : nullptr, qr, f32 ? n_q_heads : 0, k, kr, n_kv_heads,
+                                   batch, T, head_dim, rope_theta, f32, table, s);
     if (e != cudaSuccess) return fail_cuda(e);
-    a.q = qr;
+    if (f32) a.q = qr;
+    else a.rope_cs = table;
     a.k = kr;
   }
   if (dtype == ND_F32) return finish(launch_prefill_f32(a, s));

@@ -88,6 +88,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// One rotate-half pair (x_i, x_{i+d/2}) turned by the angle with cosine c and
+// sine s.  The rounding order is fixed here (products rounded, then one
+// fused add) so every kernel that rotates q or k produces the same bits.
+__device__ __forceinline__ void rope_pair(float a, float b, float c, float s, float &ya, float &yb) {
+  ya = __fmaf_rn(a, c, -__fmul_rn(b, s));
+  yb = __fmaf_rn(b, c, __fmul_rn(a, s));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);

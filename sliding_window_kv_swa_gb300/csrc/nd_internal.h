@@ -43,6 +43,8 @@ cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, i
                         float theta, cudaStream_t stream);
 
 size_t rope_table_bytes(int T, int head_dim);
+// Builds the (cos, sin) table of positions 0..T-1 into `table` (float2
+// [T][head_dim/2]) and rotates q (Hq heads; q may be NULL with Hq = 0) and k.
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
                            int batch, int T, int head_dim, float theta, bool f32, void *table,
                            cudaStream_t stream);
@@ -62,6 +64,9 @@ struct PrefillArgs {
   int block;                        // 0 = no pooled columns
   void *out;
   float *lse;  // may be NULL
+  // bf16 path: (cos, sin) table float2 [T][d/2] of the rotation; q is then
+  // rotated inside the attention kernel (k arrives rotated).  NULL: q as is.
+  const void *rope_cs = nullptr;
 };
 
 size_t prefill_plan_bytes(int batch, int T, int block);

@@ -89,6 +89,7 @@ struct TcParams {
   uint16_t *out;
   float *lse;
   int *err;
+  const float2 *rope_cs;  // (cos, sin) [T][D/2]: rotate Q while staging it; NULL: Q as given
 };
 
 // ------------------------------------------------------------------ plan
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
       m_full[NM], m_empty[NM], s_full[2][NS], p_full[2][NS], pv_done[2][NS], o_free[2], epi_full[2],
-      epi_empty[2];
+      epi_empty[2], q_rot[2];
   __shared__ float s_inv[2][BM];  // 1 / row sum, from the softmax warps to the epilogue warps
   __shared__ __align__(128) uint8_t s_stage[4][32 * 64];  // epilogue staging, one block per warp
   __shared__ uint32_t s_tmem;
@@ -502,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = 0; u < 2; ++u) {
       mbar_init(&q_full[u], 1);
       mbar_init(&q_empty[u], 2);  // committed by both issuers after an item's last S MMA
+      mbar_init(&q_rot[u], BM);   // the epilogue threads have rotated the buffer's rows
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
@@ -674,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item I = In;
       if (w + int(gridDim.x) < n_items) In = item_at(w + gridDim.x);
       const int qb = it & 1;
-      ok = warp_wait(&q_full[qb], (it >> 1) & 1, p.err, abort_flag);
+      ok = warp_wait(p.rope_cs ? &q_rot[qb] : &q_full[qb], (it >> 1) & 1, p.err, abort_flag);
       for (int j = 0; j < I.n && ok; ++j) {
         const int g = gt + j, st = g % NK;
         // the buffer holds P(g - NS) until PV(g - NS) has read it
@@ -723,9 +725,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage = smem_u32(&s_stage[qd][0]);
     bool ok = true;
     int gt = 0;
+    // Rotary embedding of an item's Q, in place in shared memory, once its
+    // TMA load has landed: rotate-half pairs (i, i + D/2) at the row's own
+    // position t, from the (cos, sin) table.  In the 128-byte swizzle a row's
+    // 16-byte chunk c sits at chunk c ^ (row & 7); at D = 128 the partner of
+    // column i is column i of the second 64-column box (the same offset), at
+    // D = 64 it is chunk c + 4 of the same row.  Lane -> (row, chunk) so a
+    // warp reads whole table rows.  Rows at or past T (zero-filled) stay zero.
+    auto rotate_q = [&](int w, int it) {
+      const Item I = item_at(w);
+      const int qb = it & 1;
+      if (!warp_wait(&q_full[qb], (it >> 1) & 1, p.err, abort_flag)) return false;
+      constexpr int kPairChunks = D / 16, kRowsPerPass = 32 / kPairChunks;
+      const int c = lane % kPairChunks;
+#pragma unroll 1
+      for (int pass = 0; pass < 32 / kRowsPerPass; ++pass) {
+        const int rr = qd * 32 + pass * kRowsPerPass + lane / kPairChunks;
+#pragma unroll
+        for (int rb = 0; rb < 2; ++rb) {
+          const int t = (rb ? I.row01 : I.row00) + rr;
+          if (t >= p.T) continue;
+          const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope_cs + size_t(t) * (D / 2) + 8 * c);
+          float cc[8], ss[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 v = __ldg(cs4 + i);
+            cc[2 * i] = v.x, ss[2 * i] = v.y, cc[2 * i + 1] = v.z, ss[2 * i + 1] = v.w;
+          }
+          const uint32_t row = sQ(qb, rb) + rr * 128;
+          const uint32_t lo = row + ((c ^ (rr & 7)) << 4);
+          const uint32_t hi = D == 128 ? lo + BM * 128 : row + (((c + 4) ^ (rr & 7)) << 4);
+          uint32_t a[4], b[4], ya[4], yb[4];
+          ld_shared_v4(lo, a[0], a[1], a[2], a[3]);
+          ld_shared_v4(hi, b[0], b[1], b[2], b[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float x0, x1, y0, y1;
+            rope_pair(bf16_lo(a[i]), bf16_lo(b[i]), cc[2 * i], ss[2 * i], x0, y0);
+            rope_pair(bf16_hi(a[i]), bf16_hi(b[i]), cc[2 * i + 1], ss[2 * i + 1], x1, y1);
+            ya[i] = pack_bf16x2(x0, x1);
+            yb[i] = pack_bf16x2(y0, y1);
+          }
+          st_shared_v4(lo, ya[0], ya[1], ya[2], ya[3]);
+          st_shared_v4(hi, yb[0], yb[1], yb[2], yb[3]);
+        }
+      }
+      // the MMA reads Q through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&q_rot[qb]);
+      return true;
+    };
+    // Q(it + 1) is rotated before item it's epilogue: it lands early in item
+    // it, and the issuer wants it as soon as item it's last S has gone out.
+    if (p.rope_cs && blockIdx.x < n_items) ok = rotate_q(blockIdx.x, 0);
     for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
       const Item I = item_at(w);
       const int n = I.n;
+      if (p.rope_cs && w + int(gridDim.x) < n_items && !rotate_q(w + gridDim.x, it + 1)) {
+        ok = false;
+        break;
+      }
       for (int rb = 0; rb < 2 && ok; ++rb) {
         ok = warp_wait(&epi_full[rb], it & 1, p.err, abort_flag);
         if (!ok) break;
@@ -1081,6 +1140,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.out = static_cast<uint16_t *>(a.out);
   p.lse = a.lse;
   p.err = err;
+  p.rope_cs = static_cast<const float2 *>(a.rope_cs);
 
   CUtensorMap tq, tk, tv, tpk, tpv;
   if (!make_map(&tq, a.q, a.batch, a.T, a.Hq, D, BM) || !make_map(&tk, a.k, a.batch, a.T, a.Hkv, D, BN) ||

@@ -76,8 +76,10 @@ __global__ void __launch_bounds__(128) rope_kernel(const E *x1, E *y1, int H1, c
     const size_t row = (size_t(bt) * H + h) * D;
     const float a = Elem<E>::ld(x, row + i), b = Elem<E>::ld(x, row + i + half);
     const float2 c = cs[i];
-    Elem<E>::st(y, row + i, a * c.x - b * c.y);
-    Elem<E>::st(y, row + i + half, b * c.x + a * c.y);
+    float ya, yb;
+    rope_pair(a, b, c.x, c.y, ya, yb);
+    Elem<E>::st(y, row + i, ya);
+    Elem<E>::st(y, row + i + half, yb);
   }
 }
 
@@ -146,10 +148,7 @@ __global__ void __launch_bounds__(256) rope_vec_kernel(const E *x1, E *y1, int H
   }
   float ya[8], yb[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    ya[i] = a[i] * c[i] - b[i] * s_[i];
-    yb[i] = b[i] * c[i] + a[i] * s_[i];
-  }
+  for (int i = 0; i < 8; ++i) rope_pair(a[i], b[i], c[i], s_[i], ya[i], yb[i]);
   st8(y + row + i0, ya);
   st8(y + row + i0 + half, yb);
 }
@@ -185,8 +184,7 @@ __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint
     float ko = ka, ko2 = kb;
     if (apply_rope) {
       const float2 c = cs[i];
-      ko = ka * c.x - kb * c.y;
-      ko2 = kb * c.x + ka * c.y;
+      rope_pair(ka, kb, c.x, c.y, ko, ko2);
     }
     const size_t orow = ((size_t(b) * nblk + j) * H + h) * D;
     pk[orow + i] = __bfloat16_as_ushort(__float2bfloat16_rn(ko));

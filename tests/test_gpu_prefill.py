@@ -267,3 +267,27 @@ def test_compressed_prefill_small_all_rows(T, W, block):
                                    pooled_k=pk, pooled_v=pv, block=block)
     want, _ = oracle.compressed_prefill(q, k, v, W, block, 10000.0)
     assert_close_bf16(host(out), want, f"compressed T={T}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (3, 1)])
+def test_bf16_rotation_in_kernel_matches_separate_rope(d, Hq, Hkv):
+    # q is rotated inside the attention kernel as its tile is staged; the
+    # result must carry the same bits as rotating q and k with the stand-alone
+    # rotary call and running the product without rotation.  T spans a ragged
+    # last row block; (3, 1) takes the unpaired-head path (two row blocks).
+    rng = philox(1700 + d + Hq)
+    B, T, W = 2, 389, 96
+    qb, _ = normal_bf16(rng, (B, T, Hq, d))
+    kb, _ = normal_bf16(rng, (B, T, Hkv, d))
+    vb, _ = normal_bf16(rng, (B, T, Hkv, d))
+    seg, sink = packed_segments(rng, B, T, 2, 3, T // 4, 3, T // 8)
+    lib = nd()
+    fused = lib.nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), dev(sink), W,
+                                    rope_theta=10000.0)
+    qr = lib.nd_rope_apply(dev_bf16(qb), rope_theta=10000.0)
+    kr = lib.nd_rope_apply(dev_bf16(kb), rope_theta=10000.0)
+    sep = lib.nd_swa_sink_prefill(qr, kr, dev_bf16(vb), dev(seg), dev(sink), W, rope_theta=0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), sep.view(torch.int16))
