@@ -357,25 +357,32 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
 
   char *ws = static_cast<char *>(workspace);
   const size_t esz = dtype == ND_F32 ? 4 : 2;
+  const bool f32 = dtype == ND_F32;
+  void *qr = nullptr, *kr = nullptr, *table = nullptr;
   if (rope_theta != 0.f) {
-    const bool f32 = dtype == ND_F32;
-    void *qr = nullptr;
-    if (f32) {
+    if (f32) {  // the bf16 kernel rotates q as it stages it
       qr = ws;
       ws += round_up(size_t(batch) * T * n_q_heads * head_dim * esz, 256);
     }
-    void *kr = ws;
+    kr = ws;
     ws += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
-    void *table = ws;
+    table = ws;
     ws += round_up(rope_table_bytes(T, head_dim), 256);
-    cudaError_t e = launch_rope_qk(f32 ? q : nullptr, qr, f32 ? n_q_heads : 0, k, kr, n_kv_heads,
-                                   batch, T, head_dim, rope_theta, f32, table, s);
-    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  // bf16: the tile records and plan go first (an ordinary launch), the
+  // rotation table beside them, then K's rotation and the attention kernel,
+  // each a dependent launch that waits for the kernel before it
+  cudaError_t e = cudaSuccess;
+  if (!f32) e = launch_prefill_tc_prep(a, ws, s);
+  if (e == cudaSuccess && table) {
+    e = launch_rope_qk(f32 ? q : nullptr, qr, f32 ? n_q_heads : 0, k, kr, n_kv_heads, batch, T, head_dim,
+                       rope_theta, f32, table, /*chained=*/!f32, s);
+    a.k = kr;
     if (f32) a.q = qr;
     else a.rope_cs = table;
-    a.k = kr;
   }
-  if (dtype == ND_F32) return finish(launch_prefill_f32(a, s));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (f32) return finish(launch_prefill_f32(a, s));
   return finish(launch_prefill_tc(a, ws, device_error_word(), s));
 }
 

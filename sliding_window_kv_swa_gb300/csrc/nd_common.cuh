@@ -79,6 +79,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
   return false;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels launched with programmatic stream serialization may start while the
+// previous kernel on the stream runs.  pdl_wait() returns once that kernel has
+// completed and its writes are visible (a no-op for an ordinary launch);
+// pdl_trigger() lets the next such kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- conversions
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -42,12 +42,35 @@ bool decode_step_fuses(int batch, int n_kv_heads, int max_slots, int head_dim);
 cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                         float theta, cudaStream_t stream);
 
+// Launch with programmatic stream serialization allowed: the kernel may be
+// scheduled while the previous one on the stream runs, and must call
+// pdl_wait() (nd_common.cuh) before it touches memory that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 size_t rope_table_bytes(int T, int head_dim);
 // Builds the (cos, sin) table of positions 0..T-1 into `table` (float2
 // [T][head_dim/2]) and rotates q (Hq heads; q may be NULL with Hq = 0) and k.
+// chained: the previous kernel on the stream is an ordinary launch of the
+// same call that does not touch `table`; the table kernel then runs beside it
+// and waits for it only before it exits (so its completion still implies that
+// kernel's).  Otherwise the table kernel waits before it starts.
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
                            int batch, int T, int head_dim, float theta, bool f32, void *table,
-                           cudaStream_t stream);
+                           bool chained, cudaStream_t stream);
 
 cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T, int n_heads,
                                  int head_dim, int block, float theta, void *pk, void *pv,
@@ -71,6 +94,10 @@ struct PrefillArgs {
 
 size_t prefill_plan_bytes(int batch, int T, int block);
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
+// The tensor-core path in two launches: the tile records and plan (an
+// ordinary launch, first of the call), then the attention kernel (a dependent
+// launch: it waits for the kernel before it, which may be the rotation pass).
+cudaError_t launch_prefill_tc_prep(const PrefillArgs &a, void *plan_ws, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream);
 
 }  // namespace nd

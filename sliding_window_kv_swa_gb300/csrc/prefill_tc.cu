@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(1024) tile_prep_kernel(TcParams p, TileMeta *m
   extern __shared__ int s_tile[];  // [3][n_kt]: seg_lo, seg_hi, any_sink
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   int *t_lo = s_tile, *t_hi = s_tile + p.n_kt, *t_any = s_tile + 2 * p.n_kt;
+  pdl_trigger();  // the next kernel reads nothing written here before it waits
   for (int j = warp; j < p.n_kt; j += nw) {
     int lo, hi, any;
     build_tile_meta(p.seg, p.sink, p.T, b, j, lane, meta[size_t(b) * p.n_kt + j], lo, hi, any);
@@ -544,6 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  // dependent launch: the setup above overlapped the kernel before this one;
+  // every global read below (plan, tile records, Q, K, V, table) follows it
+  pdl_wait();
   auto tS = [&](int rb, int buf) { return tmem + L::cS + (NS * rb + buf) * BN; };
   auto tO = [&](int rb) { return tmem + L::cO + rb * D; };
   bool fail = false;
@@ -1111,14 +1115,21 @@ PlanDims plan_dims(int B, int T, int block, int span) {
   return d;
 }
 
-template <int D>
-cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t stream) {
+struct TcSetup {
+  PlanDims pd;
+  TcParams p;
+  TileMeta *meta;
+  int32_t *plan;
+};
+
+TcSetup tc_setup(const PrefillArgs &a, void *ws, int *err) {
+  TcSetup S;
   const int G = a.Hq / a.Hkv;
   const bool pair_heads = G % 2 == 0;
-  PlanDims pd = plan_dims(a.batch, a.T, a.block, pair_heads ? BM : 2 * BM);
-  TileMeta *meta = static_cast<TileMeta *>(ws);
-  int32_t *plan = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pd.sum_bytes);
-  TcParams p;
+  S.pd = plan_dims(a.batch, a.T, a.block, pair_heads ? BM : 2 * BM);
+  S.meta = static_cast<TileMeta *>(ws);
+  S.plan = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + S.pd.sum_bytes);
+  TcParams &p = S.p;
   p.B = a.batch;
   p.T = a.T;
   p.Hq = a.Hq;
@@ -1127,21 +1138,27 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   p.W = a.window;
   p.block = a.block;
   p.nb = a.block > 0 ? a.T / a.block : 0;
-  p.n_span = pd.n_span;
-  p.span = pd.span;
-  p.n_kt = pd.n_kt;
-  p.plan_stride = pd.stride;
+  p.n_span = S.pd.n_span;
+  p.span = S.pd.span;
+  p.n_kt = S.pd.n_kt;
+  p.plan_stride = S.pd.stride;
   p.pair_heads = pair_heads ? 1 : 0;
   p.n_pairs = pair_heads ? a.Hq / 2 : a.Hq;
   p.seg = a.seg_ids;
   p.sink = a.sink;
-  p.plan = plan;
-  p.meta = meta;
+  p.plan = S.plan;
+  p.meta = S.meta;
   p.out = static_cast<uint16_t *>(a.out);
   p.lse = a.lse;
   p.err = err;
   p.rope_cs = static_cast<const float2 *>(a.rope_cs);
+  return S;
+}
 
+template <int D>
+cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t stream) {
+  const TcSetup S = tc_setup(a, ws, err);
+  const TcParams &p = S.p;
   CUtensorMap tq, tk, tv, tpk, tpv;
   if (!make_map(&tq, a.q, a.batch, a.T, a.Hq, D, BM) || !make_map(&tk, a.k, a.batch, a.T, a.Hkv, D, BN) ||
       !make_map(&tv, a.v, a.batch, a.T, a.Hkv, D, BN))
@@ -1154,25 +1171,17 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
     tpk = tk;
     tpv = tv;
   }
-  // tile records and plan: one block per sequence
-  const size_t prep_smem = size_t(3) * pd.n_kt * sizeof(int);
-  cudaError_t e = cudaSuccess;
-  if (prep_smem > 48 * 1024)
-    e = cudaFuncSetAttribute(tile_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(prep_smem));
-  if (e != cudaSuccess) return e;
-  tile_prep_kernel<<<a.batch, 1024, prep_smem, stream>>>(p, meta, plan);
   auto kern = a.block > 0 ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kBytes);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (or per item, when there are fewer items)
   int sms = 0, dev = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long n_items = long(a.batch) * pd.n_span * p.n_pairs;
-  dim3 grid(unsigned(n_items < sms ? n_items : sms));
-  kern<<<grid, kThreads, Lay<D>::kBytes, stream>>>(tq, tk, tv, tpk, tpv, p);
-  return cudaGetLastError();
+  const long n_items = long(a.batch) * S.pd.n_span * p.n_pairs;
+  const dim3 grid(unsigned(n_items < sms ? n_items : sms));
+  return launch_pdl(kern, grid, dim3(kThreads), size_t(Lay<D>::kBytes), stream, tq, tk, tv, tpk, tpv, p);
 }
 
 }  // namespace
@@ -1180,6 +1189,20 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
 size_t prefill_plan_bytes(int batch, int T, int block) {
   PlanDims pd = plan_dims(batch, T, block, BM);  // the 128-row span has the most plan rows
   return pd.sum_bytes + pd.plan_bytes;
+}
+
+cudaError_t launch_prefill_tc_prep(const PrefillArgs &a, void *plan_ws, cudaStream_t stream) {
+  if (size_t(a.batch) * a.T == 0) return cudaSuccess;
+  const TcSetup S = tc_setup(a, plan_ws, nullptr);
+  // tile records and plan: one block per sequence
+  const size_t prep_smem = size_t(3) * S.pd.n_kt * sizeof(int);
+  if (prep_smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(tile_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(prep_smem));
+    if (e != cudaSuccess) return e;
+  }
+  tile_prep_kernel<<<a.batch, 1024, prep_smem, stream>>>(S.p, S.meta, S.plan);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream) {

@@ -86,10 +86,14 @@ __global__ void __launch_bounds__(128) rope_kernel(const E *x1, E *y1, int H1, c
 // Prefill path: the (cos, sin) table of every position and channel pair is
 // built once per call (double-precision reduction as above), then one thread
 // rotates 8 channel pairs of one (b, t, head) with 16-byte loads and stores.
-__global__ void rope_table_kernel(float2 *cs, int T, int half, Freqs fr) {
+__global__ void rope_table_kernel(float2 *cs, int T, int half, Freqs fr, int wait_first) {
+  // wait_first == 0: the kernel before this one writes nothing read or
+  // written here; the wait before exit keeps the chain of completions intact
+  if (wait_first) pdl_wait();
+  pdl_trigger();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= T * half) return;
-  cs[idx] = rot_cs(double(idx / half), fr.f[idx % half]);
+  if (idx < T * half) cs[idx] = rot_cs(double(idx / half), fr.f[idx % half]);
+  if (!wait_first) pdl_wait();
 }
 
 __device__ __forceinline__ void ld8(const uint16_t *p, float *x) {
@@ -124,6 +128,10 @@ template <typename E>
 __global__ void __launch_bounds__(256) rope_vec_kernel(const E *x1, E *y1, int H1, const E *x2, E *y2,
                                                        int H2, int T, int D, const float2 *cs,
                                                        size_t n_items) {
+  // The table is in.  No early trigger: this grid runs many waves, and an
+  // attention grid scheduled early takes whole SMs from its later waves
+  // (measured 14% slower on the packed step).
+  pdl_wait();
   const size_t item = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (item >= n_items) return;
   const int half = D / 2, groups = half / 8;
@@ -194,6 +202,76 @@ __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint
   }
 }
 
+// Vector form of the pooling (head_dim a multiple of 16, 16-byte aligned
+// rows): a CTA takes kPoolJ consecutive pooled blocks of one sequence, builds
+// their midpoint angles in shared memory, and each thread pools 8 channel
+// pairs (i0..i0+7 and i0+half..) of one (block, head) with 16-byte loads --
+// the sums, the mean and the rotation in the same order as pool_kernel.
+constexpr int kPoolJ = 4;
+__global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const uint16_t *v,
+                                                       uint16_t *pk, uint16_t *pv, int T, int H,
+                                                       int D, int block, int apply_rope, Freqs fr) {
+  __shared__ float2 cs[kPoolJ][kMaxHalf];
+  const int nblk = T / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
+  const int b = blockIdx.x / n_grp, j0 = (blockIdx.x % n_grp) * kPoolJ;
+  const int nj = min(kPoolJ, nblk - j0);
+  const int half = D / 2, groups = half / 8;
+  if (apply_rope)
+    for (int idx = threadIdx.x; idx < nj * half; idx += blockDim.x) {
+      const int jj = idx / half, i = idx % half;
+      const int mid = min((j0 + jj) * block + block / 2, T - 1);
+      cs[jj][i] = rot_cs(double(mid), fr.f[i]);
+    }
+  __syncthreads();
+  const float fblock = float(block);
+  for (int idx = threadIdx.x; idx < nj * H * groups; idx += blockDim.x) {
+    const int g = idx % groups, rest = idx / groups;
+    const int h = rest % H, jj = rest / H;
+    const int i0 = g * 8, j = j0 + jj;
+    float ka[8], kb[8], va[8], vb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ka[e] = kb[e] = va[e] = vb[e] = 0.f;
+    const size_t row0 = ((size_t(b) * T + size_t(j) * block) * H + h) * D;
+    const size_t rstride = size_t(H) * D;
+#pragma unroll 4
+    for (int r = 0; r < block; ++r) {
+      const size_t row = row0 + r * rstride;
+      float x[8];
+      ld8(k + row + i0, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ka[e] += x[e];
+      ld8(k + row + i0 + half, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) kb[e] += x[e];
+      ld8(v + row + i0, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) va[e] += x[e];
+      ld8(v + row + i0 + half, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vb[e] += x[e];
+    }
+    float ko[8], ko2[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ka[e] /= fblock;
+      kb[e] /= fblock;
+      va[e] /= fblock;
+      vb[e] /= fblock;
+      ko[e] = ka[e];
+      ko2[e] = kb[e];
+      if (apply_rope) {
+        const float2 c = cs[jj][i0 + e];
+        rope_pair(ka[e], kb[e], c.x, c.y, ko[e], ko2[e]);
+      }
+    }
+    const size_t orow = ((size_t(b) * nblk + j) * H + h) * D;
+    st8(pk + orow + i0, ko);
+    st8(pk + orow + i0 + half, ko2);
+    st8(pv + orow + i0, va);
+    st8(pv + orow + i0 + half, vb);
+  }
+}
+
 Freqs make_freqs(int D, float theta) {
   Freqs fr;
   for (int i = 0; i < kMaxHalf; ++i)
@@ -220,23 +298,23 @@ size_t rope_table_bytes(int T, int head_dim) { return size_t(T) * (head_dim / 2)
 // head_dim must be a multiple of 16.
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
                            int batch, int T, int head_dim, float theta, bool f32, void *table,
-                           cudaStream_t stream) {
+                           bool chained, cudaStream_t stream) {
   if (size_t(batch) * T == 0) return cudaSuccess;
   Freqs fr = make_freqs(head_dim, theta);
   float2 *cs = static_cast<float2 *>(table);
   const int half = head_dim / 2;
-  rope_table_kernel<<<(T * half + 255) / 256, 256, 0, stream>>>(cs, T, half, fr);
+  cudaError_t e = launch_pdl(rope_table_kernel, dim3((T * half + 255) / 256), dim3(256), 0, stream, cs, T,
+                             half, fr, chained ? 0 : 1);
+  if (e != cudaSuccess) return e;
   const size_t n = size_t(batch) * T * (Hq + Hkv) * (half / 8);
-  const unsigned grid = unsigned((n + 255) / 256);
+  const dim3 grid(unsigned((n + 255) / 256));
   if (f32)
-    rope_vec_kernel<float><<<grid, 256, 0, stream>>>(
-        static_cast<const float *>(q), static_cast<float *>(q_out), Hq, static_cast<const float *>(k),
-        static_cast<float *>(k_out), Hkv, T, head_dim, cs, n);
-  else
-    rope_vec_kernel<uint16_t><<<grid, 256, 0, stream>>>(
-        static_cast<const uint16_t *>(q), static_cast<uint16_t *>(q_out), Hq,
-        static_cast<const uint16_t *>(k), static_cast<uint16_t *>(k_out), Hkv, T, head_dim, cs, n);
-  return cudaGetLastError();
+    return launch_pdl(rope_vec_kernel<float>, grid, dim3(256), 0, stream, static_cast<const float *>(q),
+                      static_cast<float *>(q_out), Hq, static_cast<const float *>(k),
+                      static_cast<float *>(k_out), Hkv, T, head_dim, static_cast<const float2 *>(cs), n);
+  return launch_pdl(rope_vec_kernel<uint16_t>, grid, dim3(256), 0, stream, static_cast<const uint16_t *>(q),
+                    static_cast<uint16_t *>(q_out), Hq, static_cast<const uint16_t *>(k),
+                    static_cast<uint16_t *>(k_out), Hkv, T, head_dim, static_cast<const float2 *>(cs), n);
 }
 
 cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T, int n_heads,
@@ -245,6 +323,16 @@ cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T,
   const int nblk = T / block;
   if (size_t(batch) * nblk == 0) return cudaSuccess;
   Freqs fr = make_freqs(head_dim, theta);
+  const bool vec = head_dim % 16 == 0 && ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+                                           reinterpret_cast<uintptr_t>(pk) | reinterpret_cast<uintptr_t>(pv)) &
+                                          15) == 0;
+  if (vec) {
+    const int n_grp = (nblk + kPoolJ - 1) / kPoolJ;
+    pool_vec_kernel<<<batch * n_grp, 256, 0, stream>>>(
+        static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), static_cast<uint16_t *>(pk),
+        static_cast<uint16_t *>(pv), T, n_heads, head_dim, block, theta != 0.f ? 1 : 0, fr);
+    return cudaGetLastError();
+  }
   pool_kernel<<<batch * nblk, 128, 0, stream>>>(
       static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
       static_cast<uint16_t *>(pk), static_cast<uint16_t *>(pv), T, n_heads, head_dim, block,

@@ -224,10 +224,13 @@ def test_rope_matches_oracle(d):
     assert np.all(err <= np.abs(want) * 2 ** -8 + 1e-6)   # one bf16 rounding per element
 
 
-@pytest.mark.parametrize("block,T", [(4, 4096), (1, 100), (3, 101), (8, 64)])
-def test_compress_pool_matches_oracle(block, T):
-    rng = philox(1100 + block)
-    B, H, d = 2, 4, 64
+@pytest.mark.parametrize("block,T,d", [(4, 4096, 64), (1, 100, 64), (3, 101, 64), (8, 64, 64), (4, 1000, 128),
+                                       (5, 203, 48), (64, 4096, 64), (2, 50, 62)])
+def test_compress_pool_matches_oracle(block, T, d):
+    # d = 62 (not a multiple of 16) takes the scalar pooling kernel, the rest
+    # the 16-byte one; T % block leaves a dropped tail in several cases
+    rng = philox(1100 + block + d)
+    B, H = 2, 4
     kb, k = normal_bf16(rng, (B, T, H, d))
     vb, v = normal_bf16(rng, (B, T, H, d))
     pk, pv = nd().nd_kv_compress_pool(dev_bf16(kb), dev_bf16(vb), block, 10000.0)
