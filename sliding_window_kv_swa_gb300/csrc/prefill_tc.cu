@@ -16,23 +16,28 @@
 // consecutive row blocks of one head.  The kernel is persistent: one CTA per
 // SM walks work items (sequence, row span, block pair) with a stride of the
 // grid, and every role keeps running tile counts, so the next item's Q and
-// first tiles load while the current one finishes.  Its eleven warps
+// first tiles load while the current one finishes.  Its sixteen warps
 // specialise:
 //   warps 0-3, 4-7 : one softmax warpgroup per row block; thread i owns row i
 //                    (= TMEM lane i): exact mask, online softmax in the log2
-//                    domain; bf16 P goes into one of the block's two TMEM P
-//                    buffers, so P(g) is written while PV(g-1) still runs.
-//   warp 8         : TMA loader over three rings: K tiles
-//                    (freed as soon as both blocks' S MMAs have read them),
-//                    V tiles (freed after both blocks' PV) and the exact
-//                    tiles' segment / sink records (cp.async, freed once the
-//                    softmax warps have built their masks).
+//                    domain; bf16 P(g) goes back into TMEM over the front of
+//                    S(g)'s buffer (already read out).
+//   warp 8         : TMA loader: Q (two buffers), K tiles (freed as soon as
+//                    both blocks' S MMAs have read them) and the exact tiles'
+//                    segment / sink records (cp.async, freed once the
+//                    softmax warps have built their masks); at d = 64 also V.
 //   warps 9, 10    : one MMA issuer per row block: S(g) = Q K(g)^T (M128
-//                    N64) into the block's S buffer as soon as the softmax
-//                    has read S(g-1), then O += P(g-1) V(g-1) (M128, N=d,
-//                    P read from TMEM, V an MN-major shared operand), so
-//                    neither block waits behind the other's.
-// TMEM per CTA: S 2 x 64, P 2 x 2 x 32, O 2 x d fp32 columns (512 at d=128).
+//                    N64) into S buffer g % NS once PV(g - NS) has read the P
+//                    it held, then O += P(g-1) V(g-1) (M128, N=d, P read from
+//                    TMEM, V an MN-major shared operand), so neither block
+//                    waits behind the other's.
+//   warp 11        : V loader at d = 128 (V tiles, freed after both blocks'
+//                    PV); idle at d = 64.
+//   warps 12-15    : epilogue: rotate the next item's Q in shared memory
+//                    (when the call applies RoPE), read O out of TMEM and
+//                    write O / l.
+// TMEM per CTA: S 2 x NS x 64 (NS = 2 at d = 128, 3 at d = 64) and O 2 x d
+// fp32 columns: 512 either way.
 // O accumulates in TMEM; a row's O is rescaled (TMEM load / multiply / store)
 // only when its running max grows by more than 2^8, so most tiles touch O
 // only through the MMA.  Tiles every row of a warp fully sees skip the
