@@ -187,13 +187,13 @@ ND_API int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache,
 /*
  * nd_swa_sink_decode_step with the step's inputs and outputs in host memory,
  * for a caller whose token and query live on the host: the call enqueues on
- * `stream` the copies of q, k_new and v_new to the device (one
- * cudaMemcpyAsync each), the step exactly as nd_swa_sink_decode_step, and the
- * copies of out (and lse, when lse_host is not NULL) back to the host.  The
- * host results are valid once the stream has passed the call (synchronise
- * the stream, or an event recorded after the call).  Page-locked host
- * buffers let the copies run asynchronously; pageable ones are still
- * correct but make the copies synchronous.
+ * `stream` the copies of q, k_new and v_new to the device, the step exactly
+ * as nd_swa_sink_decode_step, and the copies of out (and lse, when lse_host
+ * is not NULL) back to the host.  The host results are valid once the stream
+ * has passed the call (synchronise the stream, or an event recorded after the
+ * call).  Page-locked, 16-byte aligned host buffers are copied by a kernel
+ * over the host link (one launch per direction); other host memory by one
+ * cudaMemcpyAsync per buffer, synchronous for pageable memory.
  *   q_host, out_host        bf16 [batch][n_q_heads][head_dim], host memory
  *   k_new_host, v_new_host  bf16 [batch][n_kv_heads][head_dim], host memory
  *   lse_host                fp32 [batch][n_q_heads], host memory, or NULL
@@ -212,6 +212,25 @@ ND_API int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *c
                                         int n_q_heads, int window, void *out_host,
                                         float *lse_host, void *workspace,
                                         size_t workspace_bytes, nd_stream_t stream);
+
+/*
+ * nd_swa_sink_decode_step_host with the step's host buffers packed, so each
+ * direction is one copy (each copy pays a fixed latency of a few
+ * microseconds, which dominates a step of this size):
+ *   in_host   one host allocation holding, back to back,
+ *             q     bf16 [batch][n_q_heads][head_dim],
+ *             k_new bf16 [batch][n_kv_heads][head_dim],
+ *             v_new bf16 [batch][n_kv_heads][head_dim]
+ *   out_host  one host allocation holding out bf16 [batch][n_q_heads][head_dim]
+ *             followed, when with_lse != 0, by lse fp32 [batch][n_q_heads]
+ * (one allocation each: a copy may not span two page-locked allocations that
+ * merely sit next to each other).  Workspace, stream semantics and errors as
+ * nd_swa_sink_decode_step_host; the workspace size is the same query.
+ */
+ND_API int nd_swa_sink_decode_step_host_packed(const void *in_host, const nd_kv_cache *cache,
+                                               int n_q_heads, int window, void *out_host,
+                                               int with_lse, void *workspace,
+                                               size_t workspace_bytes, nd_stream_t stream);
 
 /*
  * nd_swa_sink_decode without a workspace argument.  The pages have no

@@ -236,8 +236,9 @@ int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache, const void 
 }
 
 // Device staging for the host-buffer step, at the front of its workspace:
-// q, k_new, v_new, out, lse, each rounded to 256 bytes, then the decode's own
-// split scratch.
+// q, k_new, v_new back to back (each a multiple of 128 bytes: head_dim is 64
+// or 128), then out and lse back to back, then the decode's own split
+// scratch.  Back to back so the packed form moves each side in one copy.
 struct HostStepLayout {
   size_t q, kn, vn, out, lse, split, total;
 };
@@ -246,10 +247,10 @@ static HostStepLayout host_step_layout(int batch, int n_q_heads, int n_kv_heads,
   HostStepLayout L;
   const size_t qb = size_t(batch) * n_q_heads * head_dim * 2, kb = size_t(batch) * n_kv_heads * head_dim * 2;
   L.q = 0;
-  L.kn = L.q + round_up(qb, 256);
-  L.vn = L.kn + round_up(kb, 256);
-  L.out = L.vn + round_up(kb, 256);
-  L.lse = L.out + round_up(qb, 256);
+  L.kn = L.q + qb;
+  L.vn = L.kn + kb;
+  L.out = round_up(L.vn + kb, 256);
+  L.lse = L.out + qb;
   L.split = L.lse + round_up(size_t(batch) * n_q_heads * sizeof(float), 256);
   L.total = L.split + decode_workspace_bytes(batch, n_q_heads, head_dim, max_slots, n_kv_heads);
   return L;
@@ -261,14 +262,30 @@ size_t nd_swa_sink_decode_step_host_workspace_size(int batch, int n_q_heads, int
   return host_step_layout(batch, n_q_heads, n_kv_heads, head_dim, max_slots).total;
 }
 
-int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *cache, const void *k_new_host,
-                                 const void *v_new_host, int n_q_heads, int window, void *out_host,
-                                 float *lse_host, void *workspace, size_t workspace_bytes,
-                                 nd_stream_t stream) {
+// Device address of a page-locked host buffer, or NULL when `p` is not
+// page-locked memory the device can address.
+static void *mapped_host(const void *p) {
+  cudaPointerAttributes a;
+  if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// The host-buffer step.  packed_in: q_host holds q, k_new, v_new back to
+// back (one copy); packed_out: lse follows out in out_host (one copy).
+// Page-locked, 16-byte aligned host buffers move by copy kernels over the
+// host link (a few microseconds less per copy than a copy engine at these
+// sizes); any other host memory by cudaMemcpyAsync.
+static int decode_step_host(const void *q_host, const nd_kv_cache *cache, const void *k_new_host,
+                            const void *v_new_host, bool packed_in, int n_q_heads, int window,
+                            void *out_host, float *lse_host, bool packed_out, void *workspace,
+                            size_t workspace_bytes, nd_stream_t stream) {
   int st = check_step_args(cache, n_q_heads, window);
   if (st != ND_OK) return st;
   if (cache->batch == 0) return ND_OK;
-  if (!q_host || !k_new_host || !v_new_host || !out_host) return ND_ERR_INVALID_ARG;
+  if (!q_host || !out_host || (!packed_in && (!k_new_host || !v_new_host))) return ND_ERR_INVALID_ARG;
   const int B = cache->batch, Hkv = cache->n_kv_heads, d = cache->head_dim;
   const HostStepLayout L = host_step_layout(B, n_q_heads, Hkv, d, cache->sink_cap + cache->ring_cap);
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return ND_ERR_WORKSPACE;
@@ -276,19 +293,77 @@ int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *cache, c
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   const size_t qb = size_t(B) * n_q_heads * d * 2, kb = size_t(B) * Hkv * d * 2;
-  // one cudaMemcpyAsync per buffer
-  cudaError_t e = cudaMemcpyAsync(ws + L.q, q_host, qb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.kn, k_new_host, kb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.vn, v_new_host, kb, cudaMemcpyHostToDevice, s);
+  const size_t lb = size_t(B) * n_q_heads * sizeof(float);
+  cudaError_t e;
+  const void *src[3];
+  void *dst[3];
+  size_t nb[3];
+  int nseg = 0;
+  {
+    const void *hin[3] = {q_host, k_new_host, v_new_host};
+    const size_t off[3] = {L.q, L.kn, L.vn}, len[3] = {packed_in ? qb + 2 * kb : qb, kb, kb};
+    for (int i = 0; i < (packed_in ? 1 : 3); ++i) {
+      void *dp = mapped_host(hin[i]);
+      if (!dp || !aligned16(dp)) {
+        nseg = -1;
+        break;
+      }
+      src[nseg] = dp;
+      dst[nseg] = ws + off[i];
+      nb[nseg++] = len[i];
+    }
+  }
+  if (nseg > 0) {
+    e = launch_copy_segments(nseg, src, dst, nb, s);
+  } else if (packed_in) {
+    e = cudaMemcpyAsync(ws + L.q, q_host, qb + 2 * kb, cudaMemcpyHostToDevice, s);
+  } else {
+    e = cudaMemcpyAsync(ws + L.q, q_host, qb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.kn, k_new_host, kb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.vn, v_new_host, kb, cudaMemcpyHostToDevice, s);
+  }
   if (e != cudaSuccess) return finish(e);
-  float *lse_dev = lse_host ? reinterpret_cast<float *>(ws + L.lse) : nullptr;
+  const bool want_lse = packed_out || lse_host;
+  float *lse_dev = want_lse ? reinterpret_cast<float *>(ws + L.lse) : nullptr;
   st = decode_step_device(ws + L.q, cache, ws + L.kn, ws + L.vn, n_q_heads, window, ws + L.out, lse_dev,
                           ws + L.split, workspace_bytes - L.split, s);
   if (st != ND_OK) return st;
-  e = cudaMemcpyAsync(out_host, ws + L.out, qb, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && lse_host)
-    e = cudaMemcpyAsync(lse_host, lse_dev, size_t(B) * n_q_heads * sizeof(float), cudaMemcpyDeviceToHost, s);
+  nseg = 0;
+  {
+    void *hout[2] = {out_host, packed_out ? nullptr : lse_host};
+    const size_t off[2] = {L.out, L.lse}, len[2] = {packed_out ? qb + lb : qb, lb};
+    for (int i = 0; i < 2; ++i) {
+      if (!hout[i]) continue;
+      void *dp = mapped_host(hout[i]);
+      if (!dp || !aligned16(dp)) {
+        nseg = -1;
+        break;
+      }
+      src[nseg] = ws + off[i];
+      dst[nseg] = dp;
+      nb[nseg++] = len[i];
+    }
+  }
+  if (nseg > 0) return finish(launch_copy_segments(nseg, src, dst, nb, s));
+  e = cudaMemcpyAsync(out_host, ws + L.out, packed_out ? qb + lb : qb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && lse_host && !packed_out)
+    e = cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, s);
   return finish(e);
+}
+
+int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *cache, const void *k_new_host,
+                                 const void *v_new_host, int n_q_heads, int window, void *out_host,
+                                 float *lse_host, void *workspace, size_t workspace_bytes,
+                                 nd_stream_t stream) {
+  return decode_step_host(q_host, cache, k_new_host, v_new_host, false, n_q_heads, window, out_host, lse_host,
+                          false, workspace, workspace_bytes, stream);
+}
+
+int nd_swa_sink_decode_step_host_packed(const void *in_host, const nd_kv_cache *cache, int n_q_heads,
+                                        int window, void *out_host, int with_lse, void *workspace,
+                                        size_t workspace_bytes, nd_stream_t stream) {
+  return decode_step_host(in_host, cache, nullptr, nullptr, true, n_q_heads, window, out_host, nullptr,
+                          with_lse != 0, workspace, workspace_bytes, stream);
 }
 
 size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,

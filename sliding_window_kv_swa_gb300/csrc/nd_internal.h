@@ -61,6 +61,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Kernel copy of n (1..3) segments (16-byte aligned addresses; any byte
+// count), e.g. between page-locked host memory and device memory; a
+// dependent launch.
+cudaError_t launch_copy_segments(int n, const void *const *src, void *const *dst, const size_t *bytes,
+                                 cudaStream_t stream);
+
 size_t rope_table_bytes(int T, int head_dim);
 // Builds the (cos, sin) table of positions 0..T-1 into `table` (float2
 // [T][head_dim/2]) and rotates q (Hq heads; q may be NULL with Hq = 0) and k.

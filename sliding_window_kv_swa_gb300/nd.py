@@ -73,6 +73,7 @@ def _lib():
             "nd_swa_sink_decode_step": (I, [P, P, P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_decode_step_host_workspace_size": (S, [I, I, I, I, I]),
             "nd_swa_sink_decode_step_host": (I, [P, P, P, P, I, I, P, P, P, S, P]),
+            "nd_swa_sink_decode_step_host_packed": (I, [P, P, I, I, P, I, P, S, P]),
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
@@ -96,6 +97,7 @@ EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_e
             "nd_kv_append_quant", "nd_kv_quant_rows", "nd_swa_sink_decode_workspace_size",
             "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_decode_step",
             "nd_swa_sink_decode_step_host_workspace_size", "nd_swa_sink_decode_step_host",
+            "nd_swa_sink_decode_step_host_packed",
             "nd_swa_sink_prefill_workspace_size",
             "nd_swa_sink_prefill",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
@@ -267,6 +269,10 @@ def nd_swa_sink_decode_step_host(q_host: torch.Tensor, cache: KVCache, k_new_hos
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous host tensor")
     B, Hq, d = q_host.shape
+    nk = cache.batch * cache.n_kv_heads * cache.head_dim
+    if (B, d) != (cache.batch, cache.head_dim) or k_new_host.numel() != nk or v_new_host.numel() != nk or \
+            out_host.numel() != q_host.numel() or (lse_host is not None and lse_host.numel() != B * Hq):
+        raise ValueError("host buffer shapes do not match the cache")
     if workspace is None:
         nbytes = nd_swa_sink_decode_step_host_workspace_size(B, Hq, cache.n_kv_heads, d,
                                                              cache.sink_cap + cache.ring_cap)
@@ -276,6 +282,32 @@ def nd_swa_sink_decode_step_host(q_host: torch.Tensor, cache: KVCache, k_new_hos
         q_host.data_ptr(), ctypes.byref(s), k_new_host.data_ptr(), v_new_host.data_ptr(), Hq, int(window),
         out_host.data_ptr(), None if lse_host is None else lse_host.data_ptr(), workspace.data_ptr(),
         workspace.numel(), _stream(stream)))
+    return out_host
+
+
+def nd_swa_sink_decode_step_host_packed(in_host: torch.Tensor, cache: KVCache, n_q_heads: int, window: int,
+                                        out_host: torch.Tensor, with_lse: bool = False,
+                                        workspace: Optional[torch.Tensor] = None, stream=None,
+                                        cache_struct=None) -> torch.Tensor:
+    """nd_swa_sink_decode_step_host with packed host buffers: in_host one
+    contiguous host tensor holding q | k_new | v_new (bf16, back to back),
+    out_host one contiguous host tensor holding out (bf16) followed, with
+    with_lse, by lse (fp32).  One copy each way.  Returns out_host."""
+    B, Hkv, d = cache.batch, cache.n_kv_heads, cache.head_dim
+    nin = (B * n_q_heads * d + 2 * B * Hkv * d) * 2
+    nout = B * n_q_heads * d * 2 + (B * n_q_heads * 4 if with_lse else 0)
+    for t, name, need in ((in_host, "in_host", nin), (out_host, "out_host", nout)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+        if t.numel() * t.element_size() < need:
+            raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs {need}")
+    if workspace is None:
+        nbytes = nd_swa_sink_decode_step_host_workspace_size(B, n_q_heads, Hkv, d, cache.sink_cap + cache.ring_cap)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=cache.k_codes.device)
+    s = cache_struct if cache_struct is not None else cache.struct()
+    _check("nd_swa_sink_decode_step_host_packed", _lib().nd_swa_sink_decode_step_host_packed(
+        in_host.data_ptr(), ctypes.byref(s), int(n_q_heads), int(window), out_host.data_ptr(),
+        1 if with_lse else 0, workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return out_host
 
 

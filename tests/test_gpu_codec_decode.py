@@ -261,14 +261,17 @@ def test_decode_step_matches_append_then_decode(B, Hq, Hkv, d, S, W, fill):
     np.testing.assert_array_equal(host(cache.v_scale), ref.v_scale)
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,d,S,W", [
-    (64, 8, 2, 64, 64, 256),     # fused step
-    (10, 32, 8, 128, 64, 32),    # append and decode as two launches
+@pytest.mark.parametrize("B,Hq,Hkv,d,S,W,packed", [
+    (64, 8, 2, 64, 64, 256, False),   # fused step
+    (64, 8, 2, 64, 64, 256, True),    # packed host buffers: one copy each way
+    (10, 32, 8, 128, 64, 32, False),  # append and decode as two launches
+    (10, 32, 8, 128, 64, 32, True),
 ])
-def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W):
-    """nd_swa_sink_decode_step_host: q, the new token and the output (and lse)
-    in page-locked host memory, copies enqueued by the call; same results as
-    the oracle's append + decode, cache bit-exact."""
+def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W, packed):
+    """nd_swa_sink_decode_step_host (separate host buffers) and
+    nd_swa_sink_decode_step_host_packed (q | k_new | v_new in one host
+    allocation, out | lse in another): the copies are enqueued by the call;
+    same results as the oracle's append + decode, cache bit-exact."""
     w = decode_cache(B, Hq, Hkv, d, S, W, seed=760 + B + d, full=True)
     ref = oracle_cache(w, S, W)
     cache = device_cache(ref)
@@ -276,15 +279,26 @@ def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W):
     ws = torch.empty(nd().nd_swa_sink_decode_step_host_workspace_size(B, Hq, Hkv, d, S + W),
                      dtype=torch.uint8, device="cuda")
     rng = philox(761 + B)
-    out_h = torch.empty((B, Hq, d), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    nq, nk = B * Hq * d, B * Hkv * d
+    if packed:
+        obuf = torch.empty(nq * 2 + B * Hq * 4, dtype=torch.uint8).pin_memory()
+        out_h = obuf[:nq * 2].view(torch.bfloat16).view(B, Hq, d)
+        lse_h = obuf[nq * 2:].view(torch.float32).view(B, Hq)
+    else:
+        out_h = torch.empty((B, Hq, d), dtype=torch.bfloat16).pin_memory()
+        lse_h = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
     for step in range(3):
         kb, kf = normal_bf16(rng, (B, Hkv, d))
         vb, vf = normal_bf16(rng, (B, Hkv, d))
         qb, qf = normal_bf16(rng, (B, Hq, d))
-        pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
-        nd().nd_swa_sink_decode_step_host(pin(qb), cache, pin(kb), pin(vb), W, out_h, lse_host=lse_h,
-                                          workspace=ws, cache_struct=st)
+        if packed:
+            inp = pin(np.concatenate([np.ascontiguousarray(x).view(np.int16).reshape(-1) for x in (qb, kb, vb)]))
+            nd().nd_swa_sink_decode_step_host_packed(inp, cache, Hq, W, obuf, with_lse=True, workspace=ws,
+                                                     cache_struct=st)
+        else:
+            nd().nd_swa_sink_decode_step_host(pin(qb), cache, pin(kb), pin(vb), W, out_h, lse_host=lse_h,
+                                              workspace=ws, cache_struct=st)
         torch.cuda.current_stream().synchronize()
         oracle.kv_append(ref, kf, vf, False)
         want, wlse = oracle.decode(qf, ref, W)
