@@ -38,7 +38,6 @@ namespace nd {
 namespace {
 
 constexpr int kStep = 16;    // slots per warp step (one MMA k-step)
-constexpr int kStages = 4;   // copies in flight per warp: kStages - 1 steps ahead
 constexpr int kTargetCtas = 152;
 constexpr float kLazyLog2 = 8.f;  // p is taken against a max at most 2^8 below the true one
 // Largest cluster the fused step uses.  Clusters are co-scheduled on one GPC;
@@ -156,8 +155,13 @@ __device__ __forceinline__ float ldsf(uint32_t a) {
   return v;
 }
 
-template <int D, int NW>
-__global__ void __launch_bounds__(NW * 32, D == 128 ? 3 : 1) decode_kernel(const DecodeParams p) {
+// ST: cp.async stages per warp (ST - 1 steps in flight).  d = 128 has two
+// builds: 4 stages at three CTAs per SM, and 5 stages at two CTAs per SM for
+// grids of at most four CTAs per SM, where the bytes each CTA keeps in flight
+// matter more than how many CTAs an SM holds.
+template <int D, int NW, int ST>
+__global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : 1) decode_kernel(const DecodeParams p) {
+  constexpr int kStages = ST;
   constexpr int NG = D / 32;  // scale groups per row
   using S = Stage<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -576,18 +580,18 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 // sequence in one or two steps per warp), 4 at head_dim 128 (three CTAs per SM).
 constexpr int warps_for(int D) { return D == 64 ? 20 : 4; }
 
-template <int D, int NW>
+template <int D, int NW, int ST>
 size_t decode_smem_bytes() {
-  const size_t stages = size_t(NW) * kStages * Stage<D>::kBytes;
+  const size_t stages = size_t(NW) * ST * Stage<D>::kBytes;
   const size_t merge = size_t(NW) * 8 * D * 4 + 2 * size_t(NW) * 8 * 4;
   return stages > merge ? stages : merge;
 }
 
-template <int D>
+template <int D, int ST>
 cudaError_t launch_d(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
   constexpr int NW = warps_for(D);
-  const size_t smem = decode_smem_bytes<D, NW>();
-  auto kern = decode_kernel<D, NW>;
+  const size_t smem = decode_smem_bytes<D, NW, ST>();
+  auto kern = decode_kernel<D, NW, ST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -676,8 +680,13 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
     p.ws_ml = p.ws_o + parts * c.head_dim;
   }
   dim3 grid(pl.n_split, c.n_kv_heads, c.batch);
-  if (c.head_dim == 128) return launch_d<128>(p, grid, stream);
-  if (c.head_dim == 64) return launch_d<64>(p, grid, stream);
+  if (c.head_dim == 128) {
+    // deeper rings when the grid is small (at most four CTAs per SM):
+    // measured +4 points of HBM at 256 and 512 CTAs, -2 to -4 at 1024 and up
+    const long ctas = long(grid.x) * grid.y * grid.z;
+    return ctas <= 4L * kTargetCtas ? launch_d<128, 5>(p, grid, stream) : launch_d<128, 4>(p, grid, stream);
+  }
+  if (c.head_dim == 64) return launch_d<64, 4>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 
