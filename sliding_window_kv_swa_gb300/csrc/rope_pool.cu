@@ -203,11 +203,13 @@ __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint
 }
 
 // Vector form of the pooling (head_dim a multiple of 16, 16-byte aligned
-// rows): a CTA takes kPoolJ consecutive pooled blocks of one sequence, builds
-// their midpoint angles in shared memory, and each thread pools 8 channel
-// pairs (i0..i0+7 and i0+half..) of one (block, head) with 16-byte loads --
-// the sums, the mean and the rotation in the same order as pool_kernel.
-constexpr int kPoolJ = 4;
+// rows): a CTA takes kPoolJ consecutive pooled blocks of one sequence and
+// builds their midpoint angles in shared memory; each thread pools 8 channel
+// pairs (i0..i0+7 and i0+half..) of one (block, head) of K or of V with
+// 16-byte loads -- K and V on separate threads, so a thread holds 16 sums
+// and an SM keeps more loads in flight.  The sums, the mean and the rotation
+// follow pool_kernel's order.
+constexpr int kPoolJ = 2;
 __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const uint16_t *v,
                                                        uint16_t *pk, uint16_t *pv, int T, int H,
                                                        int D, int block, int apply_rope, Freqs fr) {
@@ -224,51 +226,47 @@ __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const 
     }
   __syncthreads();
   const float fblock = float(block);
-  for (int idx = threadIdx.x; idx < nj * H * groups; idx += blockDim.x) {
-    const int g = idx % groups, rest = idx / groups;
+  const int per_kv = nj * H * groups;
+  for (int idx = threadIdx.x; idx < 2 * per_kv; idx += blockDim.x) {
+    const bool is_v = idx >= per_kv;
+    const int w = is_v ? idx - per_kv : idx;
+    const int g = w % groups, rest = w / groups;
     const int h = rest % H, jj = rest / H;
     const int i0 = g * 8, j = j0 + jj;
-    float ka[8], kb[8], va[8], vb[8];
+    const uint16_t *x = is_v ? v : k;
+    float sa[8], sb[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ka[e] = kb[e] = va[e] = vb[e] = 0.f;
+    for (int e = 0; e < 8; ++e) sa[e] = sb[e] = 0.f;
     const size_t row0 = ((size_t(b) * T + size_t(j) * block) * H + h) * D;
     const size_t rstride = size_t(H) * D;
 #pragma unroll 4
     for (int r = 0; r < block; ++r) {
       const size_t row = row0 + r * rstride;
-      float x[8];
-      ld8(k + row + i0, x);
+      float xa[8], xb[8];
+      ld8(x + row + i0, xa);
+      ld8(x + row + i0 + half, xb);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ka[e] += x[e];
-      ld8(k + row + i0 + half, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) kb[e] += x[e];
-      ld8(v + row + i0, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) va[e] += x[e];
-      ld8(v + row + i0 + half, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) vb[e] += x[e];
-    }
-    float ko[8], ko2[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      ka[e] /= fblock;
-      kb[e] /= fblock;
-      va[e] /= fblock;
-      vb[e] /= fblock;
-      ko[e] = ka[e];
-      ko2[e] = kb[e];
-      if (apply_rope) {
-        const float2 c = cs[jj][i0 + e];
-        rope_pair(ka[e], kb[e], c.x, c.y, ko[e], ko2[e]);
+      for (int e = 0; e < 8; ++e) {
+        sa[e] += xa[e];
+        sb[e] += xb[e];
       }
     }
+    float ya[8], yb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sa[e] /= fblock;
+      sb[e] /= fblock;
+      ya[e] = sa[e];
+      yb[e] = sb[e];
+      if (apply_rope && !is_v) {
+        const float2 c = cs[jj][i0 + e];
+        rope_pair(sa[e], sb[e], c.x, c.y, ya[e], yb[e]);
+      }
+    }
+    uint16_t *y = is_v ? pv : pk;
     const size_t orow = ((size_t(b) * nblk + j) * H + h) * D;
-    st8(pk + orow + i0, ko);
-    st8(pk + orow + i0 + half, ko2);
-    st8(pv + orow + i0, va);
-    st8(pv + orow + i0 + half, vb);
+    st8(y + orow + i0, ya);
+    st8(y + orow + i0 + half, yb);
   }
 }
 
