@@ -308,3 +308,68 @@ def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W, packed):
     np.testing.assert_array_equal(host(cache.v_scale), ref.v_scale)
     for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
         np.testing.assert_array_equal(host(getattr(cache, f)), getattr(ref, f), err_msg=f)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,S,W", [
+    (64, 8, 2, 64, 64, 256),    # fused step, one CTA per SM (early trigger of the next step)
+    (10, 32, 8, 128, 64, 32),   # append, then the decode as a dependent launch
+    (1, 16, 8, 128, 64, 192),   # split decode + combine after the append
+])
+def test_decode_steps_back_to_back(B, Hq, Hkv, d, S, W):
+    """Steps enqueued back to back with every input already on the device and
+    no synchronisation in between, so each step's kernels are scheduled while
+    the previous step's run (dependent launches): every step must still see
+    the token the step before appended.  Outputs are kept per step and
+    checked against the oracle's sequence afterwards."""
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=790 + B + d, full=True)
+    ref = oracle_cache(w, S, W)
+    cache = device_cache(ref)
+    rng = philox(791 + B)
+    n = 6
+    toks = [(normal_bf16(rng, (B, Hkv, d)), normal_bf16(rng, (B, Hkv, d)), normal_bf16(rng, (B, Hq, d)))
+            for _ in range(n)]
+    dev_in = [(dev_bf16(kb), dev_bf16(vb), dev_bf16(qb)) for (kb, _), (vb, _), (qb, _) in toks]
+    outs = [torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    ws = torch.empty(max(nd().nd_swa_sink_decode_workspace_size(B, Hq, Hkv, d, S + W), 16), dtype=torch.uint8,
+                     device="cuda")
+    torch.cuda.synchronize()
+    for i in range(n):
+        k_d, v_d, q_d = dev_in[i]
+        nd().nd_swa_sink_decode_step(q_d, cache, k_d, v_d, W, out=outs[i], workspace=ws)
+    torch.cuda.synchronize()
+    for i, ((_, kf), (_, vf), (_, qf)) in enumerate(toks):
+        oracle.kv_append(ref, kf, vf, False)
+        want, _ = oracle.decode(qf, ref, W)
+        assert_close_bf16(host(outs[i]), want, f"step {i}")
+    np.testing.assert_array_equal(host(cache.k_codes), ref.k_codes)
+    for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
+        np.testing.assert_array_equal(host(getattr(cache, f)), getattr(ref, f), err_msg=f)
+
+
+def test_decode_steps_host_packed_back_to_back():
+    """The packed host-buffer step (copy kernels, the step, copy kernels) for
+    several steps without synchronisation in between: the staging area in
+    the workspace is reused by every step."""
+    B, Hq, Hkv, d, S, W = 64, 8, 2, 64, 64, 256
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=795, full=True)
+    ref = oracle_cache(w, S, W)
+    cache = device_cache(ref)
+    st = cache.struct()
+    ws = torch.empty(nd().nd_swa_sink_decode_step_host_workspace_size(B, Hq, Hkv, d, S + W),
+                     dtype=torch.uint8, device="cuda")
+    rng = philox(796)
+    n = 5
+    toks = [(normal_bf16(rng, (B, Hkv, d)), normal_bf16(rng, (B, Hkv, d)), normal_bf16(rng, (B, Hq, d)))
+            for _ in range(n)]
+    ins = [torch.from_numpy(np.concatenate([np.ascontiguousarray(x).view(np.int16).reshape(-1)
+                                            for x in (qb, kb, vb)])).view(torch.bfloat16).pin_memory()
+           for (kb, _), (vb, _), (qb, _) in toks]
+    outs = [torch.empty((B, Hq, d), dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        nd().nd_swa_sink_decode_step_host_packed(ins[i], cache, Hq, W, outs[i], workspace=ws, cache_struct=st)
+    torch.cuda.synchronize()
+    for i, ((_, kf), (_, vf), (_, qf)) in enumerate(toks):
+        oracle.kv_append(ref, kf, vf, False)
+        want, _ = oracle.decode(qf, ref, W)
+        assert_close_bf16(outs[i].float().numpy(), want, f"step {i}")

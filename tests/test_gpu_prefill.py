@@ -294,3 +294,35 @@ def test_bf16_rotation_in_kernel_matches_separate_rope(d, Hq, Hkv):
     sep = lib.nd_swa_sink_prefill(qr, kr, dev_bf16(vb), dev(seg), dev(sink), W, rope_theta=0.0)
     torch.cuda.synchronize()
     assert torch.equal(fused.view(torch.int16), sep.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_prefill_calls_back_to_back_share_a_workspace():
+    """Prefill calls enqueued back to back on one workspace with no
+    synchronisation (each call's tile records, angle table, rotated K and the
+    attention kernel are chained dependent launches): every output must carry
+    the same bits as the same call run alone."""
+    rng = philox(1800)
+    lib = nd()
+    B, T, Hq, Hkv, d = 2, 700, 4, 2, 128
+    calls = []
+    for i in range(3):
+        qb, _ = normal_bf16(rng, (B, T, Hq, d))
+        kb, _ = normal_bf16(rng, (B, T, Hkv, d))
+        vb, _ = normal_bf16(rng, (B, T, Hkv, d))
+        seg, sink = packed_segments(rng, B, T, 2, 3, T // 4, 3, T // 8)
+        calls.append((dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(seg), dev(sink), [64, 17, 256][i],
+                      [10000.0, 0.0, 500000.0][i]))
+    nbytes = max(lib.nd_swa_sink_prefill_workspace_size(lib.ND_BF16, B, T, Hq, Hkv, d, th, 0)
+                 for *_, th in calls)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    alone = []
+    for q, k, v, seg, sink, W, th in calls:
+        alone.append(lib.nd_swa_sink_prefill(q, k, v, seg, sink, W, rope_theta=th, workspace=ws))
+        torch.cuda.synchronize()
+    chained = [torch.empty_like(a) for a in alone]
+    for (q, k, v, seg, sink, W, th), o in zip(calls, chained):
+        lib.nd_swa_sink_prefill(q, k, v, seg, sink, W, rope_theta=th, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    for i, (a, c) in enumerate(zip(alone, chained)):
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16)), f"call {i}"
