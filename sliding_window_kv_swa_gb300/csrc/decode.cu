@@ -30,6 +30,8 @@
 //          shuffles.
 //   merge: the warps of a CTA merge through shared memory; split CTAs write
 //          (max, sum, O) partials that a combine kernel merges.
+#include <atomic>
+
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -592,8 +594,18 @@ cudaError_t launch_d(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
   constexpr int NW = warps_for(D);
   const size_t smem = decode_smem_bytes<D, NW, ST>();
   auto kern = decode_kernel<D, NW, ST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  // the shared-memory opt-in once per device (a per-launch call is host
+  // time on every decode step)
+  static std::atomic<unsigned long long> smem_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (!bit || !(smem_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    smem_set.fetch_or(bit, std::memory_order_release);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NW * 32);

@@ -293,21 +293,21 @@ def nd_swa_sink_decode_step_host_packed(in_host: torch.Tensor, cache: KVCache, n
     contiguous host tensor holding q | k_new | v_new (bf16, back to back),
     out_host one contiguous host tensor holding out (bf16) followed, with
     with_lse, by lse (fp32).  One copy each way.  Returns out_host."""
-    B, Hkv, d = cache.batch, cache.n_kv_heads, cache.head_dim
+    s = cache_struct if cache_struct is not None else cache.struct()
+    B, Hkv, d = s.batch, s.n_kv_heads, s.head_dim
     nin = (B * n_q_heads * d + 2 * B * Hkv * d) * 2
     nout = B * n_q_heads * d * 2 + (B * n_q_heads * 4 if with_lse else 0)
-    for t, name, need in ((in_host, "in_host", nin), (out_host, "out_host", nout)):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous host tensor")
-        if t.numel() * t.element_size() < need:
-            raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs {need}")
+    # (this call sits on a per-token path: one cheap check per tensor)
+    if in_host.is_cuda or not in_host.is_contiguous() or in_host.nbytes < nin:
+        raise ValueError(f"in_host must be a contiguous host tensor of at least {nin} bytes")
+    if out_host.is_cuda or not out_host.is_contiguous() or out_host.nbytes < nout:
+        raise ValueError(f"out_host must be a contiguous host tensor of at least {nout} bytes")
     if workspace is None:
-        nbytes = nd_swa_sink_decode_step_host_workspace_size(B, n_q_heads, Hkv, d, cache.sink_cap + cache.ring_cap)
+        nbytes = nd_swa_sink_decode_step_host_workspace_size(B, n_q_heads, Hkv, d, s.sink_cap + s.ring_cap)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=cache.k_codes.device)
-    s = cache_struct if cache_struct is not None else cache.struct()
     _check("nd_swa_sink_decode_step_host_packed", _lib().nd_swa_sink_decode_step_host_packed(
-        in_host.data_ptr(), ctypes.byref(s), int(n_q_heads), int(window), out_host.data_ptr(),
-        1 if with_lse else 0, workspace.data_ptr(), workspace.numel(), _stream(stream)))
+        in_host.data_ptr(), ctypes.byref(s), n_q_heads, window, out_host.data_ptr(),
+        1 if with_lse else 0, workspace.data_ptr(), workspace.nbytes, _stream(stream)))
     return out_host
 
 
