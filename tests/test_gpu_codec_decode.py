@@ -373,3 +373,38 @@ def test_decode_steps_host_packed_back_to_back():
         oracle.kv_append(ref, kf, vf, False)
         want, _ = oracle.decode(qf, ref, W)
         assert_close_bf16(outs[i].float().numpy(), want, f"step {i}")
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_decode_step_host_pageable_and_no_lse(packed):
+    """Host buffers that are not page-locked take the copy-engine path
+    (cudaMemcpyAsync) instead of the copy kernels; the packed form without
+    lse copies the output alone.  Same results as the oracle either way."""
+    B, Hq, Hkv, d, S, W = 8, 8, 2, 64, 16, 48
+    w = decode_cache(B, Hq, Hkv, d, S, W, seed=798 + packed, full=True)
+    ref = oracle_cache(w, S, W)
+    cache = device_cache(ref)
+    ws = torch.empty(nd().nd_swa_sink_decode_step_host_workspace_size(B, Hq, Hkv, d, S + W),
+                     dtype=torch.uint8, device="cuda")
+    rng = philox(799 + packed)
+    for step in range(2):
+        kb, kf = normal_bf16(rng, (B, Hkv, d))
+        vb, vf = normal_bf16(rng, (B, Hkv, d))
+        qb, qf = normal_bf16(rng, (B, Hq, d))
+        as_t = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        if packed:
+            inp = as_t(np.concatenate([np.ascontiguousarray(x).view(np.int16).reshape(-1) for x in (qb, kb, vb)]))
+            out_h = torch.empty((B, Hq, d), dtype=torch.bfloat16)
+            nd().nd_swa_sink_decode_step_host_packed(inp, cache, Hq, W, out_h, with_lse=False, workspace=ws)
+        else:
+            out_h = torch.empty((B, Hq, d), dtype=torch.bfloat16)
+            lse_h = torch.empty((B, Hq), dtype=torch.float32)
+            nd().nd_swa_sink_decode_step_host(as_t(qb), cache, as_t(kb), as_t(vb), W, out_h, lse_host=lse_h,
+                                              workspace=ws)
+        torch.cuda.current_stream().synchronize()
+        oracle.kv_append(ref, kf, vf, False)
+        want, wlse = oracle.decode(qf, ref, W)
+        assert_close_bf16(out_h.float().numpy(), want, f"step {step}")
+        if not packed:
+            np.testing.assert_allclose(lse_h.numpy(), wlse, atol=2e-3, rtol=0)
+    np.testing.assert_array_equal(host(cache.k_codes), ref.k_codes)
