@@ -332,7 +332,7 @@ def bench_decode(torch, nd, B, Hq, Hkv, d, S, W, steps, warmup, seed, pk, dist=N
         replicas=replicas, launches=launches_per_step * steps, kernel=kernel, _state=(reps, ws))
 
 
-def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
+def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8, cpu_budget=None):
     from workloads import packed_prefill
     w = packed_prefill(B=batch)
     B, T, Hq, d = w["q"].shape
@@ -364,7 +364,14 @@ def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
     tiles = performed_tiles_packed(w["seg_ids"], w["sink"], w["window"])
     tile_flops = 4.0 * 128 * 64 * d * tiles * Hq
     t, ta = ms / steps * 1e-3, ms_attn / steps * 1e-3
+    oracle_row = None
+    if int(os.environ.get("RANK", "0")) == 0 and cpu_budget is not None:
+        try:
+            oracle_row = oracle_prefill_sample("packed", w, 4, 1, cpu_budget)
+        except Exception as ex:  # the product path never depends on it
+            oracle_row = {"tok_s": None, "sample": f"unavailable: {ex}"}
     return dict(config=f"packed prefill B{B} T{T} Hq{Hq} Hkv{Hkv} d{d} W256 RoPE, 3-6 segments with 64-512 sink prefixes",
+                oracle=oracle_row,
                 ms_per_step=ms / steps, tok_s=B * T / t, tflops=flops / t / 1e12,
                 frac=flops / t / 1e12 / pk["bf16"], visible_pairs=pairs, flops_per_step=flops,
                 attn_ms=ms_attn / steps, tiles=tiles * Hq, tile_flops=tile_flops,
@@ -372,7 +379,7 @@ def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8):
                 launches=4 * steps)
 
 
-def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
+def bench_compressed(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None):
     from workloads import compressed
     w = compressed()
     B, T, H, d = w["q"].shape
@@ -406,7 +413,14 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None):
     tiles = performed_tiles_compressed(T, w["window"], w["block"]) * B * H
     tile_flops = 4.0 * 128 * 64 * d * tiles
     t, ta = ms / steps * 1e-3, ms_attn / steps * 1e-3
-    return dict(config="compressed prefill B4 T4096 H16 d64 W256 b4 RoPE", ms_per_step=ms / steps,
+    oracle_row = None
+    if int(os.environ.get("RANK", "0")) == 0 and cpu_budget is not None:
+        try:
+            oracle_row = oracle_prefill_sample("compressed", w, 2, 2, cpu_budget)
+        except Exception as ex:  # the product path never depends on it
+            oracle_row = {"tok_s": None, "sample": f"unavailable: {ex}"}
+    return dict(config="compressed prefill B4 T4096 H16 d64 W256 b4 RoPE", oracle=oracle_row,
+                ms_per_step=ms / steps,
                 tok_s=B * T / t, tflops=flops / t / 1e12, frac=flops / t / 1e12 / pk["bf16"],
                 visible_pairs=pairs, attn_ms=ms_attn / steps, tiles=tiles, tile_flops=tile_flops,
                 tile_tflops=tile_flops / ta / 1e12, tile_frac=tile_flops / ta / 1e12 / pk["bf16"],
@@ -464,6 +478,29 @@ def e2e_decode(torch, nd, state, B, Hq, Hkv, d, S, W, steps, warmup):
     return dict(value=(cache_b + qo_b + app_b) / (ms / steps * 1e-3) / 1e9, unit="GB/s",
                 h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, ms_per_step=ms / steps,
                 host_enqueue_ms_per_step=host_s * 1e3 / steps)
+
+
+def oracle_prefill_sample(kind, w, heads, kv_heads, budget_s):
+    """Times the oracle's prefill on the host beside a prefill row: one
+    sequence of the row's workload with its first `heads` query heads (and
+    their `kv_heads` KV heads), repeated until budget_s elapses (at least
+    once); tok/s scaled to the whole row: tokens x heads/Hq per run time."""
+    import oracle
+    B, T, Hq, d = w["q"].shape
+    q, k, v = w["q"][:1, :, :heads], w["k"][:1, :, :kv_heads], w["v"][:1, :, :kv_heads]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        if kind == "packed":
+            oracle.swa_sink_prefill(q, k, v, w["seg_ids"][:1], w["sink"][:1], w["window"], w["rope_theta"])
+        else:
+            oracle.compressed_prefill(q, k, v, w["window"], w["block"], w["rope_theta"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return dict(tok_s=T * heads / Hq * n / el, cores=min(oracle.num_threads(), heads * T), kind="oracle",
+                sample=f"{n} run(s) of one sequence (T{T}) x {heads} of {Hq} query heads in {el:.1f} s "
+                       f"(fp64 dense oracle, OpenMP over rows and heads), scaled by heads to the row")
 
 
 def oracle_decode_sample(B, Hq, Hkv, d, S, W, seed, budget_s):
@@ -572,10 +609,12 @@ def main():
         rows["decode_sweep"] = dict(config="decode + fused append, Hq32 Hkv8 d128, 1024 sinks + 256 ring", **sweep)
     if "packed" in want:
         rows["packed_prefill"] = bench_packed_prefill(torch, nd, max(10, steps // 10), warmup, pk, dist,
-                                                      batch=args.packed_batch)
+                                                      batch=args.packed_batch,
+                                                      cpu_budget=min(5.0, args.cpu_budget))
         torch.cuda.empty_cache()
     if "compressed" in want:
-        rows["compressed_prefill"] = bench_compressed(torch, nd, max(10, steps // 10), warmup, pk, dist)
+        rows["compressed_prefill"] = bench_compressed(torch, nd, max(10, steps // 10), warmup, pk, dist,
+                                                      cpu_budget=min(5.0, args.cpu_budget))
         torch.cuda.empty_cache()
 
     value = job_throughput(head["bytes_per_step"], steps, world, head["ms_per_step"] * steps)
