@@ -266,6 +266,8 @@ def test_decode_step_matches_append_then_decode(B, Hq, Hkv, d, S, W, fill):
     (64, 8, 2, 64, 64, 256, True),    # packed host buffers: one copy each way
     (10, 32, 8, 128, 64, 32, False),  # append and decode as two launches
     (10, 32, 8, 128, 64, 32, True),
+    (3, 3, 1, 64, 8, 16, False),      # lse of 36 bytes: the copy kernels' byte tail
+    (3, 3, 1, 64, 8, 16, True),
 ])
 def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W, packed):
     """nd_swa_sink_decode_step_host (separate host buffers) and
