@@ -12,7 +12,7 @@
 // KV head) -- or a slice of its visible slots when there are too few sequences
 // to fill the GPU -- and each warp walks 16-slot steps of it:
 //   copy : every lane issues 16-byte cp.async copies of K codes, V codes and
-//          scales for the step three steps ahead into the warp's own shared
+//          scales for the step three (or four) steps ahead into the warp's own shared
 //          stages (XOR-swizzled 16-byte chunks, so the fragment reads below
 //          are bank-conflict free); no registers are tied up by loads in
 //          flight, and the warp never waits on other warps.
@@ -30,6 +30,10 @@
 //          shuffles.
 //   merge: the warps of a CTA merge through shared memory; split CTAs write
 //          (max, sum, O) partials that a combine kernel merges.
+// The kernel is a dependent launch: it may be scheduled while the previous
+// kernel on the stream runs, and waits for it before its first global read.
+// Also here: the copy kernel the host-buffer step uses to move its inputs and
+// outputs between page-locked host memory and the device.
 #include <atomic>
 
 #include "nd_common.cuh"
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : 1) dec
   cp_async_wait<0>();
 
   // At d = 64 (one CTA per SM) the next kernel's CTAs may be scheduled from
-  // here on; at d = 128 three CTAs share an SM and early-placed CTAs of the
+  // here on; at d = 128 two or three CTAs share an SM and early-placed CTAs of the
   // next step crowd unevenly, so there the trigger stays implicit (exit).
   if (D == 64) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- merge: quad-sum l, then the warps through shared memory (the stage
@@ -579,7 +583,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 }
 
 // Warps per CTA: 16 at head_dim 64 (one CTA per SM covers a whole short
-// sequence in one or two steps per warp), 4 at head_dim 128 (three CTAs per SM).
+// sequence in one or two steps per warp), 4 at head_dim 128 (two or three CTAs
+// per SM, by ring depth).
 constexpr int warps_for(int D) { return D == 64 ? 20 : 4; }
 
 template <int D, int NW, int ST>
