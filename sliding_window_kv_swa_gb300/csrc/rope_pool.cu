@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(128) rope_kernel(const E *x1, E *y1, int H1, c
 // Prefill path: the (cos, sin) table of every position and channel pair is
 // built once per call (double-precision reduction as above), then one thread
 // rotates 8 channel pairs of one (b, t, head) with 16-byte loads and stores.
+// The bf16 prefill passes K alone through it; its attention kernel rotates q
+// from the same table with the same rounding (rope_pair) as it stages q.
 __global__ void rope_table_kernel(float2 *cs, int T, int half, Freqs fr, int wait_first) {
   // wait_first == 0: the kernel before this one writes nothing read or
   // written here; the wait before exit keeps the chain of completions intact
@@ -291,9 +293,9 @@ cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, i
 
 size_t rope_table_bytes(int T, int head_dim) { return size_t(T) * (head_dim / 2) * sizeof(float2); }
 
-// Rotate q and k of a prefill into separate output buffers: the angle table
-// into `table` (rope_table_bytes), then one vectorised pass over q and k.
-// head_dim must be a multiple of 16.
+// Rotate q (when Hq > 0) and k of a prefill into separate output buffers: the
+// angle table into `table` (rope_table_bytes), then one vectorised pass;
+// both are dependent launches.  head_dim must be a multiple of 16.
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
                            int batch, int T, int head_dim, float theta, bool f32, void *table,
                            bool chained, cudaStream_t stream) {
