@@ -115,3 +115,47 @@ def test_workspace_sizes():
     # prefill with rotation keeps rotated copies of q and k
     n = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, 1, 512, 4, 1, 64, 10000.0, 0)
     assert n >= 512 * 4 * 64 * 4 + 512 * 1 * 64 * 4
+
+
+def test_host_step_validation_before_any_device_work():
+    """The host-buffer step forms reject missing buffers, a bad window and a
+    missing or short workspace on the host, before touching a device."""
+    import sliding_window_kv_swa_gb300 as nd
+    lib = ctypes.CDLL(nd.library_path())
+    P, Z = ctypes.c_void_p, ctypes.c_size_t
+    for fn in ("nd_swa_sink_decode_step_host", "nd_swa_sink_decode_step_host_packed",
+               "nd_swa_sink_decode_step_host_workspace_size"):
+        getattr(lib, fn).restype = ctypes.c_size_t if fn.endswith("size") else ctypes.c_int
+    lib.nd_swa_sink_decode_step_host_workspace_size.argtypes = [ctypes.c_int] * 5
+    cache = nd.nd._Cache(2, 1, 64, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
+    need = lib.nd_swa_sink_decode_step_host_workspace_size(2, 4, 1, 64, 12)
+    # q, k_new, v_new (128 x 2 B each ...) then out and lse, 16-byte multiples
+    assert need >= 2 * 4 * 64 * 2 + 2 * (2 * 1 * 64 * 2) + 2 * 4 * 64 * 2
+    packed = lambda inp, win, out, ws, n: lib.nd_swa_sink_decode_step_host_packed(
+        inp, ctypes.byref(cache), 4, win, out, 1, ws, Z(n), None)
+    assert packed(None, 8, P(16), P(16), need) == 1          # no input buffer
+    assert packed(P(16), 8, None, P(16), need) == 1          # no output buffer
+    assert packed(P(16), 0, P(16), P(16), need) == 1         # window < 1
+    assert packed(P(16), 8, P(16), None, need) == 4          # no workspace
+    assert packed(P(16), 8, P(16), P(16), need - 16) == 4    # short workspace
+    assert packed(P(16), 8, P(16), P(24), need) == 4         # misaligned workspace
+    sep = lambda q, k, v: lib.nd_swa_sink_decode_step_host(
+        q, ctypes.byref(cache), k, v, 4, 8, P(16), None, P(16), Z(need), None)
+    assert sep(P(16), None, P(16)) == 1
+    assert sep(P(16), P(16), None) == 1
+    assert sep(None, P(16), P(16)) == 1
+
+
+def test_bf16_prefill_workspace_holds_no_rotated_q():
+    """The bf16 prefill rotates q inside its attention kernel: with rotation
+    its workspace adds only the rotated K and the angle table."""
+    import sliding_window_kv_swa_gb300 as nd
+    B, T, Hq, Hkv, d = 1, 512, 4, 1, 64
+    with_rope = nd.nd_swa_sink_prefill_workspace_size(nd.ND_BF16, B, T, Hq, Hkv, d, 10000.0, 0)
+    no_rope = nd.nd_swa_sink_prefill_workspace_size(nd.ND_BF16, B, T, Hq, Hkv, d, 0.0, 0)
+    k_bytes = B * T * Hkv * d * 2            # rotated K, bf16 (a multiple of 256 here)
+    table_bytes = T * (d // 2) * 8           # (cos, sin) fp32 per position and pair
+    assert with_rope - no_rope == k_bytes + table_bytes
+    # the fp32 path still keeps rotated copies of both q and k
+    f32 = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, B, T, Hq, Hkv, d, 10000.0, 0)
+    assert f32 == B * T * Hq * d * 4 + B * T * Hkv * d * 4 + table_bytes
