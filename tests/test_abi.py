@@ -159,3 +159,34 @@ def test_bf16_prefill_workspace_holds_no_rotated_q():
     # the fp32 path still keeps rotated copies of both q and k
     f32 = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, B, T, Hq, Hkv, d, 10000.0, 0)
     assert f32 == B * T * Hq * d * 4 + B * T * Hkv * d * 4 + table_bytes
+
+
+def test_empty_problems_return_ok_without_a_device():
+    """Every compute entry point returns ND_OK for an empty problem (no
+    sequences, no tokens, no rows, no whole pooled block) before touching a
+    device: on a machine without a GPU any device call would fail instead."""
+    import sliding_window_kv_swa_gb300 as nd
+    lib = ctypes.CDLL(nd.library_path())
+    P, Z, F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+    empty = nd.nd._Cache(0, 2, 64, 4, 8, None, None, None, None, None, None, None, None)
+    e = ctypes.byref(empty)
+    calls = {
+        "nd_kv_append_quant": (e, None, None, 0, None),
+        "nd_kv_quant_rows": (None, ctypes.c_int64(0), 64, None, None, None),
+        "nd_swa_sink_decode": (None, e, 4, 8, None, None, None, Z(0), None),
+        "nd_swa_sink_decode_step": (None, e, None, None, 4, 8, None, None, None, Z(0), None),
+        "nd_swa_sink_decode_step_host": (None, e, None, None, 4, 8, None, None, None, Z(0), None),
+        "nd_swa_sink_decode_step_host_packed": (None, e, 4, 8, None, 0, None, Z(0), None),
+        "nd_swa_sink_decode_noalloc": (None, e, 4, 8, None, None, None),
+        "nd_swa_sink_prefill": (None, None, None, 1, 0, 16, 4, 2, 64, None, None, 0, F(10000.0),
+                                None, None, 0, None, None, None, Z(0), None),
+        "nd_rope_apply": (None, None, 0, 16, 2, 64, F(10000.0), None),
+        "nd_kv_compress_pool": (None, None, 1, 3, 2, 64, 4, F(10000.0), None, None, None),
+    }
+    for fn, args in calls.items():
+        f = getattr(lib, fn)
+        f.restype = ctypes.c_int
+        assert f(*args) == 0, fn
+    # T = 0 with sequences present
+    assert lib.nd_swa_sink_prefill(None, None, None, 1, 2, 0, 4, 2, 128, None, None, 0, F(0.0),
+                                   None, None, 0, None, None, None, Z(0), None) == 0
