@@ -232,36 +232,16 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : 1) dec
     s_meta[3] = new_slot;
   }
 
-  // ---- q fragments while the metadata read is in flight.  Thread t owns
-  //      channels 32*grp + 8t .. +7 of head g; k-step s uses 4s .. 4s+3.
-  uint32_t qa[NG][2][2];
-  float head_coef;  // 2^-Eq * log2(e) / sqrt(D), for head g
+  // ---- q: its loads go out now, its fragments are built once the cache
+  //      copies below are on their way.  Thread t owns channels
+  //      32*grp + 8t .. +7 of head g; k-step s uses 4s .. 4s+3.
+  uint4 w[NG];
   {
     const bool row_ok = g < G;
     const uint16_t *qh = p.q + (size_t(b) * p.Hq + hkv * G + (row_ok ? g : 0)) * D;
-    uint4 w[NG];
-    float qm = 0.f;
 #pragma unroll
-    for (int grp = 0; grp < NG; ++grp) {
+    for (int grp = 0; grp < NG; ++grp)
       w[grp] = row_ok ? *reinterpret_cast<const uint4 *>(qh + 32 * grp + 8 * t) : make_uint4(0, 0, 0, 0);
-      const uint32_t ws[4] = {w[grp].x, w[grp].y, w[grp].z, w[grp].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(ws[i])), fabsf(bf16_hi(ws[i]))));
-    }
-    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
-    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
-    const int eq = qm > 0.f ? 14 - ilog2_floor(qm) : 0;
-    const float up = exp2i(eq);
-    head_coef = exp2i(-eq) * (1.4426950408889634f * rsqrtf(float(D)));
-#pragma unroll
-    for (int grp = 0; grp < NG; ++grp) {
-      const uint32_t ws[4] = {w[grp].x, w[grp].y, w[grp].z, w[grp].w};
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        qa[grp][s][0] = pack_half2(bf16_lo(ws[2 * s]) * up, bf16_hi(ws[2 * s]) * up);
-        qa[grp][s][1] = pack_half2(bf16_lo(ws[2 * s + 1]) * up, bf16_hi(ws[2 * s + 1]) * up);
-      }
-    }
   }
   // The CTA walks physical slots [v_begin, v_end) of the pair -- sink region,
   // then ring -- in storage order: the softmax does not depend on slot order,
@@ -316,6 +296,31 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : 1) dec
 
 #pragma unroll
   for (int n = 0; n < kStages - 1; ++n) issue(n);
+  uint32_t qa[NG][2][2];
+  float head_coef;  // 2^-Eq * log2(e) / sqrt(D), for head g
+  {
+    float qm = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp) {
+      const uint32_t ws[4] = {w[grp].x, w[grp].y, w[grp].z, w[grp].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(ws[i])), fabsf(bf16_hi(ws[i]))));
+    }
+    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
+    qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
+    const int eq = qm > 0.f ? 14 - ilog2_floor(qm) : 0;
+    const float up = exp2i(eq);
+    head_coef = exp2i(-eq) * (1.4426950408889634f * rsqrtf(float(D)));
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp) {
+      const uint32_t ws[4] = {w[grp].x, w[grp].y, w[grp].z, w[grp].w};
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        qa[grp][s][0] = pack_half2(bf16_lo(ws[2 * s]) * up, bf16_hi(ws[2 * s]) * up);
+        qa[grp][s][1] = pack_half2(bf16_lo(ws[2 * s + 1]) * up, bf16_hi(ws[2 * s + 1]) * up);
+      }
+    }
+  }
   __syncthreads();  // the metadata is in
   const int sink_len = s_meta[0], rs_eff = s_meta[1], n_vis = s_meta[2], new_slot = s_meta[3];
   if (fused) cluster_arrive();  // this CTA is done reading the sequence's metadata
