@@ -23,6 +23,12 @@
  *    error code of the failing call on the calling thread.
  *  - No exception crosses the ABI.  The library is thread-safe as long as
  *    concurrent calls do not share output or workspace buffers.
+ *  - Kernels after the first of a call are programmatic dependent launches
+ *    (each waits for the kernel before it), and some kernels let the next
+ *    kernel on the stream be scheduled before they finish.  Ordinary
+ *    launches, copies and events after a call see all of its results; a
+ *    caller kernel launched with programmatic stream serialization must wait
+ *    for its prerequisite grid (griddepcontrol.wait) before it reads them.
  */
 #ifndef ND_H_
 #define ND_H_
