@@ -23,9 +23,10 @@
  *    error code of the failing call on the calling thread.
  *  - No exception crosses the ABI.  The library is thread-safe as long as
  *    concurrent calls do not share output or workspace buffers.
- *  - Kernels after the first of a call are programmatic dependent launches
- *    (each waits for the kernel before it), and some kernels let the next
- *    kernel on the stream be scheduled before they finish.  Ordinary
+ *  - Most kernels are programmatic dependent launches (each waits for the
+ *    kernel before it on the stream, the caller's included, before it reads
+ *    memory), and some let the next kernel on the stream be scheduled before
+ *    they finish.  Ordinary
  *    launches, copies and events after a call see all of its results; a
  *    caller kernel launched with programmatic stream serialization must wait
  *    for its prerequisite grid (griddepcontrol.wait) before it reads them.
