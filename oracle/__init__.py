@@ -325,6 +325,86 @@ def compress(q, k, v, block: int, theta: float, table_len: Optional[int] = None)
     return q_out, k_out, v_out
 
 
+def round_bf16(x) -> np.ndarray:
+    """Storage rounding to bf16 (round to nearest even), returned as fp64:
+    fp64 -> fp32 (numpy's rounding) -> bf16 on the bit pattern."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = ((b + (((b >> 16) & 1) + np.uint32(0x7FFF))) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def compressed_cache(k, v, pos: int, window: int, block: int, theta: float,
+                     n_pinned: int = 0, sink_cap: Optional[int] = None,
+                     ring_cap: Optional[int] = None) -> Cache:
+    """The int8 cache compressed attention decodes from after positions
+    0..pos of k, v ([B, T, Hkv, d], before rotation), per "Compressed
+    attention and the copy probe" ("Two kinds of columns", "Pool before
+    rotating, not after"; priced in "So what happened ?"), in the library's
+    layout:
+      sink slot s < n_pinned   token s, key rotated at s (pinned prefix,
+                               an exact key visible at any distance)
+      sink slot n_pinned + j   block j of the positions after the prefix:
+                               mean of its keys before rotation, rotated at
+                               n_pinned + j*block + block//2; mean of values
+      ring                     the newest non-pinned tokens, keys rotated at
+                               their positions, in append order
+    Every stored row is rounded to bf16 and quantised with quant_g32.
+    sink_len counts the pinned tokens plus the pooled blocks visible to a
+    query at pos: (j+1)*block <= pos - window + 1 - n_pinned."""
+    k = _c(k, np.float64)
+    v = _c(v, np.float64)
+    B, T, Hkv, d = k.shape
+    n_tok = pos + 1
+    n_pin = min(n_tok, n_pinned)
+    n_rest = n_tok - n_pin
+    n_blk = n_rest // block if n_tok > n_pinned else 0
+    lim = pos - window + 1 - n_pinned
+    n_vis = lim // block if lim >= block else 0
+    S = sink_cap if sink_cap is not None else n_pinned + max(n_blk, 1)
+    W = ring_cap if ring_cap is not None else window
+    c = Cache(B, Hkv, d, S, W)
+    kr = rope(k[:, :n_tok], np.arange(n_tok), theta) if theta else k[:, :n_tok]
+
+    def put(slot, kk, vv):  # kk, vv [B, Hkv, d]
+        c.k_codes[:, :, slot], c.k_scale[:, :, slot] = quant_g32(round_bf16(kk))
+        c.v_codes[:, :, slot], c.v_scale[:, :, slot] = quant_g32(round_bf16(vv))
+
+    for s_ in range(n_pin):
+        put(s_, kr[:, s_], v[:, s_])
+    if n_blk:
+        seg_k = k[:, n_pinned:n_pinned + n_blk * block]
+        seg_v = v[:, n_pinned:n_pinned + n_blk * block]
+        pk = pool_blocks(seg_k, block)
+        pv = pool_blocks(seg_v, block)
+        if theta:
+            mids = n_pinned + np.arange(n_blk) * block + block // 2
+            pk = rope(pk, mids, theta)
+        for j in range(n_blk):
+            put(n_pinned + j, pk[:, j], pv[:, j])
+    for i in range(max(0, n_rest - W), n_rest):  # ring index i holds token n_pinned + i
+        put(S + i % W, kr[:, n_pinned + i], v[:, n_pinned + i])
+    c.sink_len[:] = n_pin + n_vis
+    c.ring_len[:] = min(n_rest, W)
+    c.ring_start[:] = n_rest % W if n_rest > W else 0
+    c.seq_len[:] = n_tok
+    return c
+
+
+def compressed_decode(q, k, v, pos: int, window: int, block: int, theta: float,
+                      n_pinned: int = 0, sink_cap: Optional[int] = None,
+                      ring_cap: Optional[int] = None):
+    """Compressed attention for the query at position pos (q [B, Hq, d] before
+    rotation) over compressed_cache(...): one softmax over the visible pooled
+    blocks, the pinned tokens and the exact keys of the window.  Returns
+    (out [B, Hq, d], lse [B, Hq], the cache)."""
+    c = compressed_cache(k, v, pos, window, block, theta, n_pinned, sink_cap, ring_cap)
+    qq = _c(q, np.float64)[:, None]
+    if theta:
+        qq = rope(qq, np.array([pos]), theta)
+    out, lse = decode(qq[:, 0], c, window)
+    return out, lse, c
+
+
 # --------------------------------------------------------------------------
 # KV budget window
 # --------------------------------------------------------------------------

@@ -352,12 +352,16 @@ void ndo_decode(int B, int Hq, int Hkv, int d, int sink_cap, int ring_cap,
                 double *out, double *lse) {
   int ng = d / 32;
   int nslot = sink_cap + ring_cap;
-  int64_t *kpos = (int64_t *)malloc(sizeof(int64_t) * nslot);
-  uint8_t *is_sink = (uint8_t *)malloc(nslot);
-  uint8_t *keep = (uint8_t *)malloc(nslot);
-  double *kd = (double *)malloc(sizeof(double) * (size_t)nslot * Hkv * d);
-  double *vd = (double *)malloc(sizeof(double) * (size_t)nslot * Hkv * d);
+  /* Sequences are independent: with more than one, each thread takes whole
+   * sequences (the attention inside then runs on that thread alone); every
+   * sequence's arithmetic is the same either way. */
+#pragma omp parallel for schedule(dynamic, 1) if (B > 1)
   for (int b = 0; b < B; ++b) {
+    int64_t *kpos = (int64_t *)malloc(sizeof(int64_t) * nslot);
+    uint8_t *is_sink = (uint8_t *)malloc(nslot);
+    uint8_t *keep = (uint8_t *)malloc(nslot);
+    double *kd = (double *)malloc(sizeof(double) * (size_t)nslot * Hkv * d);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)nslot * Hkv * d);
     ndo_slot_positions(sink_cap, ring_cap, sink_len[b], ring_start[b],
                        ring_len[b], seq_len[b], kpos, is_sink);
     int64_t qpos = (int64_t)seq_len[b] - 1;
@@ -378,12 +382,12 @@ void ndo_decode(int B, int Hq, int Hkv, int d, int sink_cap, int ring_cap,
     ndo_attention(1, 1, nslot, Hq, Hkv, d, q + (size_t)b * Hq * d, kd, vd, keep,
                   0, 0, NULL, out + (size_t)b * Hq * d,
                   lse ? lse + (size_t)b * Hq : NULL);
+    free(kpos);
+    free(is_sink);
+    free(keep);
+    free(kd);
+    free(vd);
   }
-  free(kpos);
-  free(is_sink);
-  free(keep);
-  free(kd);
-  free(vd);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -143,6 +143,27 @@ def test_pooled_key_rotated_at_block_midpoint():
             assert abs(math.remainder(ang - t, 2 * math.pi)) < 1e-9
 
 
+@pytest.mark.parametrize("b,table_len", [(4, 10), (3, 7), (8, 1), (2, 24)])
+def test_pooled_midpoint_clamped_to_rotary_table(b, table_len):
+    # [C3] "Pool before rotating, not after" clamps each block midpoint to the
+    # last row of the rotary table.  With a table shorter than T, blocks whose
+    # midpoint j*b + b//2 lies past it are rotated at table_len - 1 instead;
+    # d = 2 again, so the angle read back is the position used.
+    B, T, H, d = 1, 24, 1, 2
+    k = np.zeros((B, T, H, d))
+    k[..., 0] = 1.0
+    z = np.zeros_like(k)
+    _, kk, _ = oracle.compress(z, k, z, b, theta=10.0, table_len=table_len)
+    clamped = 0
+    for j in range(T // b):
+        mid = j * b + b // 2
+        want = mid if mid <= table_len - 1 else table_len - 1
+        clamped += want != mid
+        ang = math.atan2(kk[0, j, 0, 1], kk[0, j, 0, 0])
+        assert abs(math.remainder(ang - want, 2 * math.pi)) < 1e-9, (b, j, want)
+    assert clamped == sum(1 for j in range(T // b) if j * b + b // 2 > table_len - 1)
+
+
 def test_pool_happens_before_rotation():
     # Two keys of opposite angle offsets around the midpoint would shrink if
     # rotated first; pooling first keeps the mean of the raw keys, rotated once.
@@ -181,3 +202,87 @@ def test_compressed_attention_matches_sdpa_on_concatenated_columns():
     tq, tk, tv = (torch.from_numpy(a).permute(0, 2, 1, 3) for a in (qr, kk, vv))
     want = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=m)
     np.testing.assert_allclose(out, want.permute(0, 2, 1, 3).numpy(), atol=1e-12, rtol=0)
+
+
+# ---------------------------------------------------------------- compressed decode cache
+# The oracle's compressed-attention decode (compressed_cache / compressed_decode)
+# stores every key and value as int8 group-32 codes; these pins tie it to the
+# dense definition above.  Tolerance: int8 quantisation moves each stored
+# element by at most scale/2 = amax/254 (about 1e-2 for N(0,1) groups), plus one
+# bf16 rounding; the attention output of these small cases stays within 3e-2
+# max / 6e-3 mean of the unquantised result, while one pooled column too many
+# or too few (a visibility rule off by one) moves it by ~1/(columns) ~ 1e-1.
+QMAX, QMEAN = 3e-2, 6e-3
+
+
+@pytest.mark.parametrize("T,W,b", [(48, 8, 4), (40, 4, 4), (37, 5, 3), (30, 6, 1)])
+def test_compressed_cache_columns_follow_the_mask(T, W, b):
+    """At every query position the cache holds exactly the columns of that
+    row of compressed_mask: the visible pooled blocks (sink_len) and the
+    exact keys (ring positions)."""
+    rng = philox(60 + T)
+    k, v = (rng.standard_normal((1, T, 2, 32)) for _ in range(2))
+    m = oracle.compressed_mask(T, W, b)
+    for pos in range(T):
+        c = oracle.compressed_cache(k, v, pos, W, b, 1e4, sink_cap=T // b + 1)
+        assert int(c.sink_len[0]) == int(m[pos, :T // b].sum()), pos
+        kpos, _ = oracle.slot_positions(c, 0)
+        ring = sorted(int(x) for x in kpos[c.sink_cap:] if x >= 0)
+        assert ring == [int(t) for t in np.nonzero(m[pos, T // b:])[0]], pos
+
+
+@pytest.mark.parametrize("T,W,b", [(48, 8, 4), (40, 4, 4), (37, 5, 3)])
+def test_compressed_decode_matches_compressed_prefill_rows(T, W, b):
+    """Decode at every position equals the row of the dense compressed
+    attention, up to the int8 storage."""
+    rng = philox(70 + T)
+    B, H, d = 2, 2, 64
+    q, k, v = (rng.standard_normal((B, T, H, d)) for _ in range(3))
+    want, _ = oracle.compressed_prefill(q, k, v, W, b, 1e4)
+    errs = []
+    for pos in range(T):
+        out, _, _ = oracle.compressed_decode(q[:, pos], k, v, pos, W, b, 1e4)
+        errs.append(np.abs(out - want[:, pos]))
+    errs = np.stack(errs)
+    assert errs.max() <= QMAX and errs.mean() <= QMEAN, (errs.max(), errs.mean())
+
+
+def test_compressed_decode_with_pinned_prefix_block_one_is_causal_attention():
+    """Pinned prefix + compressed attention with block 1: every token is kept
+    (pinned, pooled singly at its own position, or in the window), so the
+    decode equals plain causal attention up to the int8 storage; and a
+    window as long as the sequence never pools."""
+    rng = philox(80)
+    B, T, H, d, P, W = 1, 30, 2, 32, 5, 4
+    q, k, v = (rng.standard_normal((B, T, H, d)) for _ in range(3))
+    pos_all = np.arange(T)
+    qr, kr = oracle.rope(q, pos_all, 1e4), oracle.rope(k, pos_all, 1e4)
+    tq, tk, tv = (torch.from_numpy(a).permute(0, 2, 1, 3) for a in (qr, kr, v))
+    full = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True).permute(0, 2, 1, 3).numpy()
+    for pos in range(T):
+        out, _, c = oracle.compressed_decode(q[:, pos], k, v, pos, W, 1, 1e4, n_pinned=P, sink_cap=T)
+        assert np.abs(out - full[:, pos]).max() <= QMAX, pos
+        assert int(c.sink_len[0]) == min(pos + 1, P) + max(0, pos - W + 1 - P)
+    out, _, c = oracle.compressed_decode(q[:, T - 1], k, v, T - 1, T, 4, 1e4, n_pinned=P, ring_cap=T)
+    assert int(c.sink_len[0]) == P and int(c.ring_len[0]) == T - P
+    assert np.abs(out - full[:, T - 1]).max() <= QMAX
+
+
+def test_pinned_tokens_are_seen_at_any_distance():
+    """A pinned token's value reaches a query far past the window; the same
+    token unpinned reaches it only through its block's mean (a quarter of
+    the weight at block 4), and not at all before its block is visible."""
+    rng = philox(81)
+    B, T, H, d, W, b = 1, 64, 1, 32, 8, 4
+    q, k, v = (rng.standard_normal((B, T, H, d)) for _ in range(3))
+    v2 = v.copy()
+    v2[:, 0] += 10.0
+    pos = T - 1
+    for P in (1, 0):
+        a, _, _ = oracle.compressed_decode(q[:, pos], k, v, pos, W, b, 1e4, n_pinned=P)
+        c_, _, _ = oracle.compressed_decode(q[:, pos], k, v2, pos, W, b, 1e4, n_pinned=P)
+        assert np.abs(c_ - a).max() > 1e-2, P
+    # token 0 unpinned, query at pos W + 1: block 0 (tokens 0..3) not yet visible
+    a, _, _ = oracle.compressed_decode(q[:, W + 1], k, v, W + 1, W, b, 1e4)
+    c_, _, _ = oracle.compressed_decode(q[:, W + 1], k, v2, W + 1, W, b, 1e4)
+    np.testing.assert_array_equal(a, c_)
