@@ -149,6 +149,38 @@ ND_API int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim,
                      int8_t *codes, float *scales, nd_stream_t stream);
 
 /*
+ * Prefill -> cache handoff: fills cache rows from the keys and values a
+ * prefill computed, so decoding can continue after a packed prefill.  The
+ * bounded cache of [N2] "KV Sinks for Tools" / [N1] "KV sink 如何「钉住」工具"
+ * keeps a segment's pinned sink prefix and only its most recent positions;
+ * cache row e receives the tokens of segment src_seg[e] of batch row
+ * src_row[e] exactly as appending them one at a time, in position order, to
+ * an empty cache row would (nd_kv_append_quant with to_sink = sink[b][t]):
+ *   - while the ring is empty, a sink token goes to the next sink slot
+ *     (rejected once sink_cap slots are used);
+ *   - every other token goes to the ring, which keeps the newest ring_cap;
+ *   - once the ring holds a token, sink tokens are rejected.
+ * The row's codes, scales and metadata (sink_len, ring_start, ring_len,
+ * seq_len) are then those of that sequence of appends; its other slots keep
+ * whatever they held (they are not visible).  A rejected sink token is
+ * dropped (not counted in seq_len) and sets device error flag 2.
+ *   k, v     bf16 [batch][T][n_kv_heads][head_dim]: the keys as the decode
+ *            will read them (already rotated, if the model rotates keys) and
+ *            the values; n_kv_heads and head_dim are the cache's
+ *   seg_ids  int32 [batch][T], or NULL (every position in one segment)
+ *   sink     uint8 [batch][T], or NULL (no sink tokens)
+ *   src_row, src_seg  int32 [cache->batch] device arrays; src_seg may be NULL
+ *            when seg_ids is.  src_row[e] < 0 leaves cache row e untouched;
+ *            src_row[e] >= batch or src_seg[e] <= 0 (padding) sets device
+ *            error flag 2 and leaves it untouched.
+ * Requires ring_cap > 0; head_dim 32, 64, 128 or 256.
+ */
+ND_API int nd_kv_cache_from_prefill(const nd_kv_cache *cache, const void *k, const void *v,
+                                    int batch, int T, const int32_t *seg_ids,
+                                    const uint8_t *sink, const int32_t *src_row,
+                                    const int32_t *src_seg, nd_stream_t stream);
+
+/*
  * One decode step ([N1] "256-token 滑动窗口：源码走读"): each sequence's query
  * sits at position seq_len - 1 and attends to every sink slot and to the ring
  * entries within `window` positions of it (recent = qpos - kpos < window; a
@@ -242,22 +274,26 @@ ND_API int nd_swa_sink_decode_step_host_packed(const void *in_host, const nd_kv_
 /*
  * nd_swa_sink_decode without a workspace argument.  The pages have no
  * counterpart: this is a library convenience for callers that cannot
- * allocate device memory -- a thread recording a CUDA graph with a frozen
- * memory plan, a serving loop that must never call cudaMalloc (it may
- * synchronise the device), or a host runtime that owns all device memory and
- * passes a plugin only its inputs and outputs.
+ * allocate device memory -- a serving loop that must never call cudaMalloc
+ * (it may synchronise the device and stall every stream), or a host runtime
+ * that owns all device memory and passes a plugin only its inputs and
+ * outputs.
  *
  * Computes exactly what nd_swa_sink_decode computes, with the same arguments
- * and results.  Its split-K scratch is one fixed device array of
- * ND_NOALLOC_SCRATCH_BYTES inside libnd, present on every device that loads
- * the library until the process exits.  The call allocates nothing and calls
- * no allocating routine.
+ * and results, and refuses what it refuses with the same status.  Its
+ * split-K scratch is one fixed device array of ND_NOALLOC_SCRATCH_BYTES
+ * (512 KiB) inside libnd, present on every device that loads the library
+ * until the process exits.  The call allocates nothing and calls no
+ * allocating routine.
  *  - Returns ND_ERR_WORKSPACE when the decode would need more scratch than
  *    ND_NOALLOC_SCRATCH_BYTES (nd_swa_sink_decode_workspace_size tells how
  *    much a shape needs); use nd_swa_sink_decode with a caller workspace then.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress); make that first call before any stream capture
- *    on that device.
+ *    (cudaGetSymbolAddress) and keeps it for later calls; make that first
+ *    call before any stream capture on that device.  A failed lookup returns
+ *    ND_ERR_CUDA (nd_last_cuda_error() has the code).  The kept address does
+ *    not survive cudaDeviceReset: do not reset a device while the library is
+ *    in use on it.
  *  - All calls on a device share the one array and each overwrites it, so
  *    calls whose kernels may overlap on the GPU (different streams without
  *    ordering between them) race; order them on one stream or use
@@ -267,6 +303,75 @@ ND_API int nd_swa_sink_decode_step_host_packed(const void *in_host, const nd_kv_
 ND_API int nd_swa_sink_decode_noalloc(const void *q, const nd_kv_cache *cache,
                                       int n_q_heads, int window, void *out,
                                       float *lse, nd_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Compressed-attention decode                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The cache of compressed attention ([C3] "Two kinds of columns, pooled
+ * blocks and exact recent keys", "Pool before rotating, not after"; priced
+ * at inference in "So what happened ?": W exact positions plus one pooled
+ * entry per block of `block` positions outside the window).  It is an
+ * nd_kv_cache in the same int8 group-32 layout:
+ *   sink slots [0, n_pinned)        pinned tokens 0 .. n_pinned-1, exact keys
+ *                                   visible at any distance (the sink prefix
+ *                                   of [N2] "KV Sinks for Tools"; 0 = the
+ *                                   pages' compressed attention)
+ *   sink slot n_pinned + j          pooled block j: positions
+ *                                   n_pinned + j*block .. + block-1; key =
+ *                                   mean of the unrotated keys rotated at
+ *                                   n_pinned + j*block + block/2, value =
+ *                                   mean of the values, each rounded to bf16
+ *                                   and quantised with the cache codec
+ *   ring (ring_cap >= window)       the exact keys (rotated at their
+ *                                   positions) and values of the newest
+ *                                   positions
+ *   sink_len                        pinned tokens seen + pooled blocks
+ *                                   visible to the newest query: block j is
+ *                                   visible at query position p iff
+ *                                   (j+1)*block <= p - window + 1 - n_pinned
+ *   k_sum, v_sum  fp32 [batch][n_kv_heads][head_dim]: the running sums
+ *                 (before rotation, in position order) of the block being
+ *                 filled; nothing needs to be initialised
+ * sink_cap must hold n_pinned + the number of blocks the sequence will
+ * close; an empty cache has all four metadata arrays 0.
+ */
+typedef struct {
+  nd_kv_cache kv;
+  float *k_sum;
+  float *v_sum;
+  int block;     /* >= 1 */
+  int n_pinned;  /* 0 .. kv.sink_cap */
+} nd_compressed_cache;
+
+/*
+ * One decode step of compressed attention for every sequence: the token at
+ * position p = seq_len (q, k_new, v_new before rotation, bf16) is appended --
+ * pinned slot p while p < n_pinned, else the ring (nd_kv_append_quant's rule)
+ * plus its block's sums, and when p is the last position of block j that
+ * block is written to its pooled slot -- and the query, rotated at p, then
+ * attends one softmax over [visible pooled blocks, pinned tokens, the ring
+ * entries within `window` of p] (nd_swa_sink_decode on the cache).  With
+ * n_pinned = 0 this is row p of the compressed attention of [C3], read from
+ * int8 storage.  rope_theta 0 = no rotation.
+ *   q        bf16 [batch][n_q_heads][head_dim]   (before rotation)
+ *   k_new, v_new bf16 [batch][n_kv_heads][head_dim] (before rotation)
+ *   out      bf16 [batch][n_q_heads][head_dim];  lse fp32 [batch][n_q_heads] or NULL
+ * The rotated q and the decode's split scratch live in `workspace` (device,
+ * 16-byte aligned) of nd_compressed_decode_step_workspace_size(batch,
+ * n_q_heads, n_kv_heads, head_dim, sink_cap + ring_cap) bytes.  Requires
+ * window >= 1, ring_cap >= window, head_dim 64 or 128, n_q_heads /
+ * n_kv_heads 1..8.  A block that does not fit sink_cap, or a pinned token
+ * beyond it, is not written and sets device error flag 2.
+ */
+ND_API size_t nd_compressed_decode_step_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                                       int head_dim, int max_slots);
+ND_API int nd_compressed_decode_step(const void *q, const nd_compressed_cache *cache,
+                                     const void *k_new, const void *v_new, int n_q_heads,
+                                     int window, float rope_theta, void *out, float *lse,
+                                     void *workspace, size_t workspace_bytes,
+                                     nd_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Prefill                                                                   */
@@ -315,10 +420,25 @@ ND_API int nd_swa_sink_prefill(const void *q, const void *k, const void *v,
                         size_t workspace_bytes, nd_stream_t stream);
 
 /*
+ * Work the bf16 prefill's attention kernel performed: after an
+ * nd_swa_sink_prefill call with dtype ND_BF16 and these arguments has run on
+ * `workspace` (the call's own workspace, not yet reused), writes to
+ * *tiles_out the number of products of a 128-row query block with a 64-key
+ * tile the kernel computed -- the tiles its plan kept, read from the plan in
+ * the workspace (so this synchronises with the device).  Each such product
+ * is 4 * 128 * 64 * head_dim flops (QK^T and PV).
+ */
+ND_API int nd_swa_sink_prefill_tiles(const void *workspace, int batch, int T, int n_q_heads,
+                                     int n_kv_heads, int head_dim, float rope_theta, int block,
+                                     long long *tiles_out);
+
+/*
  * Rotary embedding (rotate-half) of x at positions 0..T-1 of each row, the
  * rotation [C3] "Pool before rotating, not after" applies to q and k.
  *   x, y  bf16 [batch][T][n_heads][head_dim]  (y may equal x: in place)
- * Angles are computed in fp32: angle = t * theta^(-2i/head_dim).
+ * Angles: theta^(-2i/head_dim) and t * theta^(-2i/head_dim) reduced modulo
+ * 2*pi are computed in double; the sine and cosine of the reduced angle and
+ * the rotation itself in fp32, rounded once to bf16.
  */
 ND_API int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads,
                   int head_dim, float rope_theta, nd_stream_t stream);

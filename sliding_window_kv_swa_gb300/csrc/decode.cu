@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
   if (ch == 0 && p.lse) p.lse[row] = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
-// Warps per CTA: 16 at head_dim 64 (one CTA per SM covers a whole short
+// Warps per CTA: 20 at head_dim 64 (one CTA per SM covers a whole short
 // sequence in one or two steps per warp), 4 at head_dim 128 (two or three CTAs
 // per SM, by ring depth).
 constexpr int warps_for(int D) { return D == 64 ? 20 : 4; }

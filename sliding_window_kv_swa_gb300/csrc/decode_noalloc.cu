@@ -2,8 +2,7 @@
 // that cannot hand the library a workspace buffer.
 //
 // Who needs it: code that runs where allocating device memory is not
-// allowed or not possible -- a host thread that is recording a CUDA graph
-// whose memory plan is frozen, a real-time serving loop that must not call
+// allowed or not possible -- a real-time serving loop that must not call
 // cudaMalloc (it can synchronise the device and stall every stream), or an
 // embedding host (another runtime, a plugin ABI) that owns all device memory
 // and gives the plugin only its input and output buffers.
@@ -19,6 +18,7 @@
 #include <mutex>
 
 #include "nd.h"
+#include "nd_internal.h"
 
 namespace {
 
@@ -31,17 +31,14 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up on the
-// first call per device).  Returns the CUDA error of the lookup, if any.
-cudaError_t scratch_address(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+// Device address of the scratch array on device `dev`, which is current (set
+// up on the first call per device).  Returns the CUDA error of the lookup.
+cudaError_t scratch_address(int dev, void **out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = p;
   }
@@ -53,16 +50,20 @@ cudaError_t scratch_address(void **out) {
 
 extern "C" int nd_swa_sink_decode_noalloc(const void *q, const nd_kv_cache *cache, int n_q_heads,
                                           int window, void *out, float *lse, nd_stream_t stream) {
-  if (!cache || window < 1 || n_q_heads <= 0 || cache->n_kv_heads <= 0 || cache->batch < 0)
-    return ND_ERR_INVALID_ARG;
-  if (cache->batch == 0) return ND_OK;
+  // the same argument checks, in the same order, as nd_swa_sink_decode, so a
+  // shape it refuses is refused here for the same reason
+  int st = nd::validate_decode(q, cache, n_q_heads, window, out);
+  if (st != ND_OK || cache->batch == 0) return st;
   const size_t need = nd_swa_sink_decode_workspace_size(cache->batch, n_q_heads, cache->n_kv_heads,
                                                         cache->head_dim, cache->sink_cap + cache->ring_cap);
   if (need > ND_NOALLOC_SCRATCH_BYTES) return ND_ERR_WORKSPACE;
+  int dev = 0;
+  if ((st = nd::check_device(&dev)) != ND_OK) return st;
   void *scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) {
-    cudaGetLastError();  // the lookup error is reported as ND_ERR_CUDA, not left sticky
-    return ND_ERR_CUDA;
+  const cudaError_t e = scratch_address(dev, &scratch);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // reported through the status, not left sticky
+    return nd::fail_cuda(e);
   }
   return nd_swa_sink_decode(q, cache, n_q_heads, window, out, lse, scratch, ND_NOALLOC_SCRATCH_BYTES,
                             stream);

@@ -163,7 +163,210 @@ __global__ void __launch_bounds__(256) kv_quant_rows_kernel(const uint16_t *x, i
     quant_row<CPL>(x + r * D, codes + r * D, scales + r * (D / 32), lane);
 }
 
+// ------------------------------------------------------------------ prefill -> cache
+// Quantise RPI = 256/D rows of D channels per warp-iteration: lane l holds 8
+// channels (16 bytes) of row l / (D/8); a 32-channel group spans 4 lanes (a
+// group never straddles two rows, so every lane of a group has the same row).
+// Same arithmetic as quant_row (IEEE divides, rint, clamp), so the same codes.
+// Every lane of the warp must call it (the group absmax is a shuffle).
+__device__ __forceinline__ uint2 quant8(const uint4 w, float &scale) {
+  float x[8];
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16_lo(u[i]);
+    x[2 * i + 1] = bf16_hi(u[i]);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  scale = __fdiv_rn(amax, 127.0f);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float r = 0.f;
+    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    const uint32_t cb = uint32_t(int(r)) & 0xffu;
+    if (i < 4) lo |= cb << (8 * i);
+    else hi |= cb << (8 * (i - 4));
+  }
+  return make_uint2(lo, hi);
+}
+
+constexpr int kFillTokens = 16;   // kept tokens per CTA
+constexpr int kFillThreads = 256;
+
+struct FillParams {
+  nd_kv_cache c;
+  const uint16_t *k, *v;  // [batch][T][Hkv][D]
+  int batch, T;
+  const int32_t *seg_ids;  // may be NULL
+  const uint8_t *sink;     // may be NULL
+  const int32_t *src_row, *src_seg;
+  int *err;
+};
+
+// Cache row e = blockIdx.y takes the tokens of segment src_seg[e] of batch row
+// src_row[e], in position order, under the append rule: while the ring is
+// empty a sink token goes to the next sink slot (rejected once the sink
+// region is full); every other token goes to the ring, and once the ring has
+// a token, sink tokens are rejected.  Every CTA ranks the segment's tokens
+// (two block-wide prefix counts over the batch row) and then quantises the
+// kept tokens [16*blockIdx.x, +16) into their slots; CTA 0 of the row writes
+// the metadata.
+template <int D>
+__global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams p) {
+  constexpr int NW = kFillThreads / 32;
+  __shared__ int s_wsum[NW][2];
+  __shared__ int s_first_r;
+  __shared__ int s_src[kFillTokens], s_slot[kFillTokens];
+  const nd_kv_cache &c = p.c;
+  const int e = blockIdx.y, c0 = blockIdx.x * kFillTokens;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  const int b = p.src_row[e];
+  const int seg = p.seg_ids ? p.src_seg[e] : 1;
+  if (b < 0) return;  // row left untouched
+  if (b >= p.batch || seg <= 0) {
+    if (blockIdx.x == 0 && tid == 0) raise_device_error(p.err, ND_DEVERR_METADATA);
+    return;
+  }
+  if (tid == 0) s_first_r = 0x7fffffff;
+  if (tid < kFillTokens) s_src[tid] = -1;
+  // this thread's positions [t0, t1) of the batch row
+  const int per = (p.T + kFillThreads - 1) / kFillThreads;
+  const int t0 = min(p.T, tid * per), t1 = min(p.T, t0 + per);
+  const int32_t *sg = p.seg_ids ? p.seg_ids + size_t(b) * p.T : nullptr;
+  const uint8_t *sk = p.sink ? p.sink + size_t(b) * p.T : nullptr;
+  int n_seg = 0, n_snk = 0, first_r = -1;
+  for (int t = t0; t < t1; ++t) {
+    if (sg && sg[t] != seg) continue;
+    const bool is_sink = sk && sk[t];
+    if (!is_sink && first_r < 0) first_r = n_seg;
+    n_seg += 1;
+    n_snk += is_sink;
+  }
+  // block-wide exclusive prefix of (n_seg, n_snk)
+  int a = n_seg, s = n_snk;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, a, off), ys = __shfl_up_sync(0xffffffffu, s, off);
+    if (lane >= off) a += ya, s += ys;
+  }
+  if (lane == 31) s_wsum[warp][0] = a, s_wsum[warp][1] = s;
+  __syncthreads();
+  int ex_seg = a - n_seg, ex_snk = s - n_snk, tot_seg = 0, tot_snk = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    if (w < warp) ex_seg += s_wsum[w][0], ex_snk += s_wsum[w][1];
+    tot_seg += s_wsum[w][0], tot_snk += s_wsum[w][1];
+  }
+  if (first_r >= 0) atomicMin(&s_first_r, ex_seg + first_r);
+  __syncthreads();
+  const int f = s_first_r == 0x7fffffff ? tot_seg : s_first_r;  // rank of the first ring token
+  const int n_sink = min(f, c.sink_cap);                         // accepted sink tokens
+  const int n_ring = tot_seg - tot_snk;                          // ring tokens
+  const int kept_ring = min(n_ring, c.ring_cap);
+  const int i0 = n_ring - kept_ring;                             // oldest ring token kept
+  if (blockIdx.x == 0 && tid == 0) {
+    c.sink_len[e] = n_sink;
+    c.ring_len[e] = kept_ring;
+    c.ring_start[e] = n_ring > c.ring_cap ? n_ring % c.ring_cap : 0;
+    c.seq_len[e] = n_sink + n_ring;
+    if (tot_snk > n_sink) raise_device_error(p.err, ND_DEVERR_METADATA);  // rejected sink tokens
+  }
+  const int n_kept = n_sink + kept_ring;
+  if (c0 >= n_kept) return;
+  // second walk: place the kept tokens that fall into this CTA's chunk
+  {
+    int rank = ex_seg, rsnk = ex_snk;
+    for (int t = t0; t < t1; ++t) {
+      if (sg && sg[t] != seg) continue;
+      const bool is_sink = sk && sk[t];
+      int kept = -1, slot = 0;
+      if (rank < n_sink) {
+        kept = rank;
+        slot = rank;
+      } else if (!is_sink) {
+        const int i = rank - rsnk;  // ring index of this token
+        if (i >= i0) {
+          kept = n_sink + i - i0;
+          slot = c.sink_cap + i % c.ring_cap;
+        }
+      }
+      if (kept >= c0 && kept < c0 + kFillTokens) {
+        s_src[kept - c0] = t;
+        s_slot[kept - c0] = slot;
+      }
+      rank += 1;
+      rsnk += is_sink;
+    }
+  }
+  __syncthreads();
+  // rows of this chunk: (token j, head h, K or V); RPI rows per warp-iteration
+  constexpr int RPI = 256 / D, kUnroll = 4;
+  const int n_tok = min(kFillTokens, n_kept - c0), Hkv = c.n_kv_heads;
+  const int n_rows = n_tok * Hkv * 2, nslot = c.sink_cap + c.ring_cap;
+  const int sub = lane / (D / 8);
+  for (int r0 = warp * RPI * kUnroll; r0 < n_rows; r0 += NW * RPI * kUnroll) {
+    uint4 w[kUnroll];
+    int rows[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = r0 + u * RPI + sub;
+      rows[u] = r;
+      w[u] = make_uint4(0, 0, 0, 0);
+      if (r < n_rows) {
+        const int j = r / (2 * Hkv), h = (r >> 1) % Hkv;
+        const uint16_t *src = ((r & 1) ? p.v : p.k) + ((size_t(b) * p.T + s_src[j]) * Hkv + h) * D;
+        w[u] = *reinterpret_cast<const uint4 *>(src + (lane % (D / 8)) * 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      // every lane takes part in the shuffles; rows past the end are not stored
+      float scale;
+      const uint2 q8 = quant8(w[u], scale);
+      const int r = rows[u];
+      if (r < n_rows) {
+        const int j = r / (2 * Hkv), h = (r >> 1) % Hkv, ch = (lane % (D / 8)) * 8;
+        const bool is_v = r & 1;
+        const size_t row = (size_t(e) * Hkv + h) * nslot + s_slot[j];
+        *reinterpret_cast<uint2 *>((is_v ? c.v_codes : c.k_codes) + row * D + ch) = q8;
+        if ((lane & 3) == 0) (is_v ? c.v_scale : c.k_scale)[row * (D / 32) + ch / 32] = scale;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_fill(const nd_kv_cache &c, const void *k, const void *v, int batch, int T,
+                           const int32_t *seg_ids, const uint8_t *sink, const int32_t *src_row,
+                           const int32_t *src_seg, int *err, cudaStream_t stream) {
+  FillParams p;
+  p.c = c;
+  p.k = static_cast<const uint16_t *>(k);
+  p.v = static_cast<const uint16_t *>(v);
+  p.batch = batch;
+  p.T = T;
+  p.seg_ids = seg_ids;
+  p.sink = sink;
+  p.src_row = src_row;
+  p.src_seg = src_seg;
+  p.err = err;
+  const int slots = c.sink_cap + c.ring_cap;
+  const dim3 grid((slots + kFillTokens - 1) / kFillTokens, c.batch);
+  switch (c.head_dim) {
+    case 32: return launch_pdl(kv_fill_kernel<32>, grid, dim3(kFillThreads), 0, stream, p);
+    case 64: return launch_pdl(kv_fill_kernel<64>, grid, dim3(kFillThreads), 0, stream, p);
+    case 128: return launch_pdl(kv_fill_kernel<128>, grid, dim3(kFillThreads), 0, stream, p);
+    case 256: return launch_pdl(kv_fill_kernel<256>, grid, dim3(kFillThreads), 0, stream, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_kv_append_quant(const nd_kv_cache &c, const void *k_new, const void *v_new,
                                    int to_sink, int *err, cudaStream_t stream) {

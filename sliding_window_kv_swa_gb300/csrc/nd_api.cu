@@ -25,6 +25,8 @@ std::mutex g_mu;
 int *g_err_ptr[kMaxDevices] = {};
 int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 
+}  // namespace
+
 int fail_cuda(cudaError_t e) {
   t_last_cuda_error = int(e);
   return ND_ERR_CUDA;
@@ -50,6 +52,8 @@ int check_device(int *dev_out) {
   return ok == 1 ? ND_OK : ND_ERR_UNSUPPORTED;
 }
 
+namespace {
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -72,6 +76,19 @@ int validate_cache(const nd_kv_cache *c) {
 }
 
 }  // namespace
+
+int validate_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, int window, const void *out) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return ND_ERR_INVALID_ARG;
+  const int G = n_q_heads / cache->n_kv_heads;
+  if (G > 8) return ND_ERR_UNSUPPORTED;
+  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
+  if (cache->batch == 0) return ND_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  if (cache->sink_cap + cache->ring_cap <= 0) return ND_ERR_INVALID_ARG;
+  return ND_OK;
+}
 
 int *device_error_word() {
   int dev = 0;
@@ -156,6 +173,23 @@ int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim, int8_t *codes,
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nd_kv_cache_from_prefill(const nd_kv_cache *cache, const void *k, const void *v, int batch, int T,
+                             const int32_t *seg_ids, const uint8_t *sink, const int32_t *src_row,
+                             const int32_t *src_seg, nd_stream_t stream) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (batch < 0 || T < 0) return ND_ERR_INVALID_ARG;
+  if (cache->ring_cap <= 0) return ND_ERR_INVALID_ARG;
+  const int d = cache->head_dim;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return ND_ERR_UNSUPPORTED;
+  if (cache->batch == 0) return ND_OK;
+  if (!src_row || (seg_ids && !src_seg)) return ND_ERR_INVALID_ARG;
+  if (size_t(batch) * T > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return ND_ERR_INVALID_ARG;
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  return finish(launch_kv_fill(*cache, k, v, batch, T, seg_ids, sink, src_row, src_seg, device_error_word(),
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t nd_swa_sink_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                          int max_slots) {
   if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || max_slots <= 0) return 0;
@@ -165,16 +199,9 @@ size_t nd_swa_sink_decode_workspace_size(int batch, int n_q_heads, int n_kv_head
 int nd_swa_sink_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, int window,
                        void *out, float *lse, void *workspace, size_t workspace_bytes,
                        nd_stream_t stream) {
-  int st = validate_cache(cache);
-  if (st != ND_OK) return st;
-  if (window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads) return ND_ERR_INVALID_ARG;
-  const int G = n_q_heads / cache->n_kv_heads;
-  if (G > 8) return ND_ERR_UNSUPPORTED;
-  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
-  if (cache->batch == 0) return ND_OK;
-  if (!q || !out || !aligned16(q) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  int st = validate_decode(q, cache, n_q_heads, window, out);
+  if (st != ND_OK || cache->batch == 0) return st;
   const int max_slots = cache->sink_cap + cache->ring_cap;  // every physical slot is walked
-  if (max_slots <= 0) return ND_ERR_INVALID_ARG;
   DecodePlan pl = plan_decode(cache->batch, cache->n_kv_heads, max_slots, cache->head_dim);
   if (pl.n_split > 1) {
     size_t need = size_t(cache->batch) * n_q_heads * pl.n_split * (cache->head_dim + 2) * sizeof(float);
@@ -366,10 +393,51 @@ int nd_swa_sink_decode_step_host_packed(const void *in_host, const nd_kv_cache *
                           with_lse != 0, workspace, workspace_bytes, stream);
 }
 
-size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,
-                                          int n_kv_heads, int head_dim, float rope_theta,
-                                          int block) {
-  if (batch <= 0 || T <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return 0;
+// Compressed decode step: rotated q at the front of the workspace, then the
+// decode's split scratch.
+static size_t compressed_q_bytes(int batch, int n_q_heads, int head_dim) {
+  return round_up(size_t(batch) * n_q_heads * head_dim * 2, 256);
+}
+
+size_t nd_compressed_decode_step_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                                int max_slots) {
+  if (batch <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || max_slots <= 0) return 0;
+  return compressed_q_bytes(batch, n_q_heads, head_dim) +
+         decode_workspace_bytes(batch, n_q_heads, head_dim, max_slots, n_kv_heads);
+}
+
+int nd_compressed_decode_step(const void *q, const nd_compressed_cache *cache, const void *k_new,
+                              const void *v_new, int n_q_heads, int window, float rope_theta, void *out,
+                              float *lse, void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+  if (!cache) return ND_ERR_INVALID_ARG;
+  const nd_kv_cache *kv = &cache->kv;
+  int st = validate_decode(q, kv, n_q_heads, window, out);
+  if (st != ND_OK) return st;
+  if (cache->block < 1 || cache->n_pinned < 0 || cache->n_pinned > kv->sink_cap) return ND_ERR_INVALID_ARG;
+  if (kv->ring_cap < window) return ND_ERR_INVALID_ARG;  // the exact window must fit the ring
+  if (kv->batch == 0) return ND_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ND_ERR_INVALID_ARG;
+  if (!cache->k_sum || !cache->v_sum || !aligned16(cache->k_sum) || !aligned16(cache->v_sum))
+    return ND_ERR_INVALID_ARG;
+  const int B = kv->batch, d = kv->head_dim, max_slots = kv->sink_cap + kv->ring_cap;
+  const size_t qb = compressed_q_bytes(B, n_q_heads, d);
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < qb + decode_workspace_bytes(B, n_q_heads, d, max_slots, kv->n_kv_heads))
+    return ND_ERR_WORKSPACE;
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int *err = device_error_word();
+  char *ws = static_cast<char *>(workspace);
+  cudaError_t e = launch_compressed_append(*kv, cache->k_sum, cache->v_sum, cache->block, cache->n_pinned,
+                                           window, q, n_q_heads, k_new, v_new, ws, rope_theta, err, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return finish(launch_decode(ws, *kv, n_q_heads, window, out, lse, ws + qb, workspace_bytes - qb, err, s));
+}
+
+// Prefill workspace: the rotation buffers (when rope_theta != 0), then the
+// tile records and plan (bf16 path).  Returns the offset of the plan.
+static size_t prefill_rotation_bytes(nd_dtype dtype, int batch, int T, int n_q_heads, int n_kv_heads,
+                                     int head_dim, float rope_theta) {
   const size_t esz = dtype == ND_F32 ? 4 : 2;
   size_t bytes = 0;
   if (rope_theta != 0.f) {
@@ -379,8 +447,42 @@ size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int 
     bytes += round_up(size_t(batch) * T * n_kv_heads * head_dim * esz, 256);
     bytes += round_up(rope_table_bytes(T, head_dim), 256);
   }
+  return bytes;
+}
+
+size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,
+                                          int n_kv_heads, int head_dim, float rope_theta,
+                                          int block) {
+  if (batch <= 0 || T <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return 0;
+  size_t bytes = prefill_rotation_bytes(dtype, batch, T, n_q_heads, n_kv_heads, head_dim, rope_theta);
   if (dtype == ND_BF16) bytes += round_up(prefill_plan_bytes(batch, T, block), 256);
   return bytes;
+}
+
+int nd_swa_sink_prefill_tiles(const void *workspace, int batch, int T, int n_q_heads, int n_kv_heads,
+                              int head_dim, float rope_theta, int block, long long *tiles_out) {
+  if (!tiles_out || batch < 0 || T < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || block < 0)
+    return ND_ERR_INVALID_ARG;
+  if (n_q_heads % n_kv_heads || (head_dim != 64 && head_dim != 128)) return ND_ERR_INVALID_ARG;
+  *tiles_out = 0;
+  if (size_t(batch) * T == 0) return ND_OK;
+  if (!workspace || !aligned16(workspace)) return ND_ERR_WORKSPACE;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  PrefillArgs a = {};
+  a.dtype = ND_BF16;
+  a.batch = batch;
+  a.T = T;
+  a.Hq = n_q_heads;
+  a.Hkv = n_kv_heads;
+  a.d = head_dim;
+  a.block = block;
+  const size_t off = prefill_rotation_bytes(ND_BF16, batch, T, n_q_heads, n_kv_heads, head_dim, rope_theta);
+  long long n = 0;
+  cudaError_t e = prefill_tile_count(a, static_cast<const char *>(workspace) + off, &n);
+  if (e != cudaSuccess) return fail_cuda(e);
+  *tiles_out = n;
+  return ND_OK;
 }
 
 int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dtype, int batch,

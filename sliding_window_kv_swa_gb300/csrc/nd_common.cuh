@@ -106,6 +106,50 @@ __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, fl
   yb = __fmaf_rn(b, c, __fmul_rn(a, s));
 }
 
+// (cos, sin) of the rotation angle pos * freq: the product and its reduction
+// modulo 2 pi in double, then sincosf of the reduced angle, so the angle
+// error stays ~1e-7 rad at any position.  Every kernel that rotates takes its
+// angles from here (and rounds with rope_pair), so all give the same bits.
+__device__ __forceinline__ float2 rot_cs(double pos, double freq) {
+  const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
+  double a = pos * freq;
+  // the quotient only picks the multiple of 2 pi to subtract: multiplying by
+  // 1 / (2 pi) instead of dividing can move it by one at a half-turn, which
+  // still leaves |a| <= pi (+ one ulp)
+  a = fma(-rint(a * inv_two_pi), two_pi, a);
+  float s, c;
+  sincosf(float(a), &s, &c);
+  return make_float2(c, s);
+}
+
+// The cache codec on one row of 32*CPL channels held by a full warp (lane l
+// has channels [l*CPL, l*CPL + CPL)): per 32-channel group amax = max |x|
+// (a shuffle over the group's 32/CPL lanes), scale = amax / 127 and
+// code = clamp(rint(x / scale), +-127), both divides IEEE fp32; amax == 0
+// gives scale 0 and zero codes.  Returns the scale of this lane's group.
+template <int CPL>
+__device__ __forceinline__ float quant_lanes(const float *x, int *code) {
+  constexpr int kLanesPerGroup = 32 / CPL;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int off = kLanesPerGroup / 2; off >= 1; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    float r = 0.f;
+    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    code[i] = int(r);
+  }
+  return scale;
+}
+
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);

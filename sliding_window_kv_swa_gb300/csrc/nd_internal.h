@@ -14,8 +14,22 @@ namespace nd {
 // Address of the current device's error word (see nd_device_errors()).
 int *device_error_word();
 
+// Records `e` as the calling thread's last CUDA error; returns ND_ERR_CUDA.
+int fail_cuda(cudaError_t e);
+// ND_OK if the current device is an sm_103 part, else ND_ERR_UNSUPPORTED (or
+// ND_ERR_CUDA when the device query fails).
+int check_device(int *dev_out);
+// The argument checks of nd_swa_sink_decode (cache, heads, window, q, out),
+// in its order; ND_OK also for an empty batch.
+int validate_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, int window, const void *out);
+
 cudaError_t launch_kv_append_quant(const nd_kv_cache &c, const void *k_new, const void *v_new,
                                    int to_sink, int *err, cudaStream_t stream);
+
+// Prefill -> cache handoff (nd_kv_cache_from_prefill); a dependent launch.
+cudaError_t launch_kv_fill(const nd_kv_cache &c, const void *k, const void *v, int batch, int T,
+                           const int32_t *seg_ids, const uint8_t *sink, const int32_t *src_row,
+                           const int32_t *src_seg, int *err, cudaStream_t stream);
 
 cudaError_t launch_kv_quant_rows(const void *x, int64_t n_rows, int head_dim, int8_t *codes,
                                  float *scales, cudaStream_t stream);
@@ -38,6 +52,13 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
                           cudaStream_t stream, const void *k_new = nullptr,
                           const void *v_new = nullptr);
 bool decode_step_fuses(int batch, int n_kv_heads, int max_slots, int head_dim);
+
+// Per sequence: rotate q into q_rot, append the token to the compressed
+// cache (pinned slot or ring, block sums, a pooled slot when the token closes
+// its block) and advance the metadata; a dependent launch.
+cudaError_t launch_compressed_append(const nd_kv_cache &c, float *k_sum, float *v_sum, int block, int n_pinned,
+                                     int window, const void *q, int Hq, const void *k_new, const void *v_new,
+                                     void *q_rot, float theta, int *err, cudaStream_t stream);
 
 cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                         float theta, cudaStream_t stream);
@@ -66,6 +87,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // dependent launch.
 cudaError_t launch_copy_segments(int n, const void *const *src, void *const *dst, const size_t *bytes,
                                  cudaStream_t stream);
+
+// theta^(-2i/head_dim) for i < head_dim/2, in double (head_dim <= 256).
+constexpr int kMaxHalf = 128;
+struct Freqs {
+  double f[kMaxHalf];
+};
+Freqs make_freqs(int head_dim, float theta);
 
 size_t rope_table_bytes(int T, int head_dim);
 // Builds the (cos, sin) table of positions 0..T-1 into `table` (float2
@@ -105,5 +133,8 @@ cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 // launch: it waits for the kernel before it, which may be the rotation pass).
 cudaError_t launch_prefill_tc_prep(const PrefillArgs &a, void *plan_ws, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream);
+// Products of a 128-row block with a 64-key tile that the attention kernel
+// performs for the plan in plan_ws (synchronous read of the plan's counts).
+cudaError_t prefill_tile_count(const PrefillArgs &a, const void *plan_ws, long long *tiles);
 
 }  // namespace nd

@@ -196,13 +196,12 @@ cudaError_t launch_simt(const PrefillArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-// fp32 inputs, or bf16 inputs on CUDA cores (used for shapes the tensor-core
-// kernel does not take).
+// fp32 inputs on CUDA cores (bf16 inputs always take the tensor-core kernel).
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream) {
   if (size_t(a.batch) * a.T == 0) return cudaSuccess;
-  const bool f32 = a.dtype == ND_F32;
-  if (a.d == 64) return f32 ? launch_simt<float, 64>(a, stream) : launch_simt<uint16_t, 64>(a, stream);
-  if (a.d == 128) return f32 ? launch_simt<float, 128>(a, stream) : launch_simt<uint16_t, 128>(a, stream);
+  if (a.dtype != ND_F32) return cudaErrorInvalidValue;
+  if (a.d == 64) return launch_simt<float, 64>(a, stream);
+  if (a.d == 128) return launch_simt<float, 128>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -49,6 +49,8 @@
 
 #include <climits>
 
+#include <vector>
+
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -1242,6 +1244,25 @@ cudaError_t launch_prefill_tc_prep(const PrefillArgs &a, void *plan_ws, cudaStre
   }
   tile_prep_kernel<<<a.batch, 1024, prep_smem, stream>>>(S.p, S.meta, S.plan);
   return cudaGetLastError();
+}
+
+// Every work item (sequence, span, head pair) multiplies each tile of its
+// span's plan entry with both of its 128-row blocks (two heads of a GQA pair,
+// or two row blocks of one head): per (sequence, span) the plan's count times
+// Hq (pairs) or 2 Hq (row-block pairs) products of a 128 x 64 tile.
+cudaError_t prefill_tile_count(const PrefillArgs &a, const void *plan_ws, long long *tiles) {
+  *tiles = 0;
+  if (size_t(a.batch) * a.T == 0) return cudaSuccess;
+  const TcSetup S = tc_setup(a, const_cast<void *>(plan_ws), nullptr);
+  const size_t rows = size_t(a.batch) * S.pd.n_span;
+  std::vector<int32_t> n(rows);
+  cudaError_t e = cudaMemcpy2D(n.data(), sizeof(int32_t), S.plan, size_t(S.pd.stride) * sizeof(int32_t),
+                               sizeof(int32_t), rows, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  long long total = 0;
+  for (size_t i = 0; i < rows; ++i) total += n[i];
+  *tiles = total * (S.p.pair_heads ? a.Hq : 2LL * a.Hq);
+  return cudaSuccess;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream) {

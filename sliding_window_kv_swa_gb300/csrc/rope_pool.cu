@@ -21,24 +21,6 @@ namespace nd {
 
 namespace {
 
-constexpr int kMaxHalf = 128;  // head_dim <= 256
-
-struct Freqs {
-  double f[kMaxHalf];
-};
-
-__device__ __forceinline__ float2 rot_cs(double pos, double freq) {
-  const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
-  double a = pos * freq;
-  // the quotient only picks the multiple of 2 pi to subtract: multiplying by
-  // 1 / (2 pi) instead of dividing can move it by one at a half-turn, which
-  // still leaves |a| <= pi (+ one ulp)
-  a = fma(-rint(a * inv_two_pi), two_pi, a);
-  float s, c;
-  sincosf(float(a), &s, &c);
-  return make_float2(c, s);
-}
-
 template <typename E>
 struct Elem;
 template <>
@@ -272,14 +254,14 @@ __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const 
   }
 }
 
+}  // namespace
+
 Freqs make_freqs(int D, float theta) {
   Freqs fr;
   for (int i = 0; i < kMaxHalf; ++i)
     fr.f[i] = (i < D / 2) ? pow(double(theta), -2.0 * double(i) / double(D)) : 0.0;
   return fr;
 }
-
-}  // namespace
 
 cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                         float theta, cudaStream_t stream) {

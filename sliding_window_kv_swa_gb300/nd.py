@@ -42,6 +42,11 @@ class _Cache(ctypes.Structure):
                 ("ring_len", ctypes.c_void_p), ("seq_len", ctypes.c_void_p)]
 
 
+class _CompressedCache(ctypes.Structure):
+    _fields_ = [("kv", _Cache), ("k_sum", ctypes.c_void_p), ("v_sum", ctypes.c_void_p),
+                ("block", ctypes.c_int), ("n_pinned", ctypes.c_int)]
+
+
 class _ModelCfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("d_model", "attn_dim", "num_heads", "num_kv_heads",
                                              "num_layers", "n_engram_sites", "max_seq_len",
@@ -67,6 +72,7 @@ def _lib():
             "nd_device_errors": (I, [P, I]),
             "nd_kv_append_quant": (I, [P, P, P, I, P]),
             "nd_kv_quant_rows": (I, [P, L, I, P, P, P]),
+            "nd_kv_cache_from_prefill": (I, [P, P, P, I, I, P, P, P, P, P]),
             "nd_swa_sink_decode_workspace_size": (S, [I, I, I, I, I]),
             "nd_swa_sink_decode": (I, [P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_decode_noalloc": (I, [P, P, I, I, P, P, P]),
@@ -74,8 +80,11 @@ def _lib():
             "nd_swa_sink_decode_step_host_workspace_size": (S, [I, I, I, I, I]),
             "nd_swa_sink_decode_step_host": (I, [P, P, P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_decode_step_host_packed": (I, [P, P, I, I, P, I, P, S, P]),
+            "nd_compressed_decode_step_workspace_size": (S, [I, I, I, I, I]),
+            "nd_compressed_decode_step": (I, [P, P, P, P, I, I, F, P, P, P, S, P]),
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
+            "nd_swa_sink_prefill_tiles": (I, [P, I, I, I, I, I, F, I, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
             "nd_kv_compress_pool": (I, [P, P, I, I, I, I, I, F, P, P, P]),
             "nd_kv_budget_window": (I, [P, P, P]),
@@ -94,12 +103,13 @@ def library_path() -> str:
 
 
 EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_errors",
-            "nd_kv_append_quant", "nd_kv_quant_rows", "nd_swa_sink_decode_workspace_size",
+            "nd_kv_append_quant", "nd_kv_quant_rows", "nd_kv_cache_from_prefill", "nd_swa_sink_decode_workspace_size",
             "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_decode_step",
             "nd_swa_sink_decode_step_host_workspace_size", "nd_swa_sink_decode_step_host",
             "nd_swa_sink_decode_step_host_packed",
+            "nd_compressed_decode_step_workspace_size", "nd_compressed_decode_step",
             "nd_swa_sink_prefill_workspace_size",
-            "nd_swa_sink_prefill",
+            "nd_swa_sink_prefill", "nd_swa_sink_prefill_tiles",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
 
 
@@ -176,6 +186,28 @@ class KVCache:
                                                self.seq_len)))
 
 
+@dataclass
+class CompressedCache:
+    """A compressed-attention cache (nd_compressed_cache): kv's sink region
+    holds n_pinned pinned tokens then the pooled blocks, its ring the exact
+    window; k_sum / v_sum fp32 [B, Hkv, d] hold the open block's sums."""
+    kv: KVCache
+    k_sum: torch.Tensor
+    v_sum: torch.Tensor
+    block: int
+    n_pinned: int = 0
+
+    @classmethod
+    def empty(cls, batch, n_kv_heads, head_dim, max_blocks, ring_cap, block, n_pinned=0, device="cuda"):
+        kv = KVCache.empty(batch, n_kv_heads, head_dim, n_pinned + max_blocks, ring_cap, device)
+        z = lambda: torch.zeros((batch, n_kv_heads, head_dim), dtype=torch.float32, device=device)
+        return cls(kv, z(), z(), block, n_pinned)
+
+    def struct(self) -> _CompressedCache:
+        return _CompressedCache(self.kv.struct(), self.k_sum.data_ptr(), self.v_sum.data_ptr(), self.block,
+                                self.n_pinned)
+
+
 # --------------------------------------------------------------------------
 # Entry points
 # --------------------------------------------------------------------------
@@ -186,6 +218,10 @@ def nd_version() -> str:
 
 def nd_status_string(status: int) -> str:
     return _lib().nd_status_string(status).decode()
+
+
+def nd_last_cuda_error() -> int:
+    return int(_lib().nd_last_cuda_error())
 
 
 def nd_device_errors(clear: bool = True) -> int:
@@ -206,6 +242,19 @@ def nd_kv_quant_rows(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
     n = x.numel() // d if d else 0
     _check("nd_kv_quant_rows", _lib().nd_kv_quant_rows(_ptr(x), n, d, _ptr(codes), _ptr(scales),
                                                        _stream(stream)))
+
+
+def nd_kv_cache_from_prefill(cache: KVCache, k: torch.Tensor, v: torch.Tensor, src_row: torch.Tensor,
+                             seg_ids: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
+                             src_seg: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Fill cache row e from segment src_seg[e] of batch row src_row[e] of a
+    prefill's k / v (bf16 [B, T, Hkv, d]) as appending its tokens in order
+    would; src_row / src_seg int32 [cache.batch] on the device."""
+    B, T = k.shape[:2]
+    s = cache.struct()
+    _check("nd_kv_cache_from_prefill", _lib().nd_kv_cache_from_prefill(
+        ctypes.byref(s), _ptr(k), _ptr(v), B, T, _ptr(seg_ids), _ptr(sink), _ptr(src_row), _ptr(src_seg),
+        _stream(stream)))
 
 
 def nd_swa_sink_decode_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
@@ -326,6 +375,31 @@ def nd_swa_sink_decode_noalloc(q: torch.Tensor, cache: KVCache, window: int, out
     return out
 
 
+def nd_compressed_decode_step_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                                             max_slots: int) -> int:
+    return int(_lib().nd_compressed_decode_step_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, max_slots))
+
+
+def nd_compressed_decode_step(q: torch.Tensor, cache: CompressedCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                              window: int, rope_theta: float = 0.0, out: Optional[torch.Tensor] = None,
+                              lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                              stream=None, cache_struct=None) -> torch.Tensor:
+    """Append the token at position seq_len (q, k_new, v_new before rotation)
+    to the compressed cache and attend with it; returns out."""
+    B, Hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    kv = cache.kv
+    if workspace is None:
+        nbytes = nd_compressed_decode_step_workspace_size(B, Hq, kv.n_kv_heads, d, kv.sink_cap + kv.ring_cap)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    s = cache_struct if cache_struct is not None else cache.struct()
+    _check("nd_compressed_decode_step", _lib().nd_compressed_decode_step(
+        _ptr(q), ctypes.byref(s), _ptr(k_new), _ptr(v_new), Hq, int(window), float(rope_theta), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
 def nd_swa_sink_prefill_workspace_size(dtype: int, batch: int, T: int, n_q_heads: int, n_kv_heads: int,
                                        head_dim: int, rope_theta: float = 0.0, block: int = 0) -> int:
     return int(_lib().nd_swa_sink_prefill_workspace_size(dtype, batch, T, n_q_heads, n_kv_heads, head_dim,
@@ -352,6 +426,16 @@ def nd_swa_sink_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         float(rope_theta), _ptr(pooled_k), _ptr(pooled_v), int(block), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def nd_swa_sink_prefill_tiles(workspace: torch.Tensor, batch: int, T: int, n_q_heads: int, n_kv_heads: int,
+                              head_dim: int, rope_theta: float = 0.0, block: int = 0) -> int:
+    """128-row x 64-key tile products the bf16 prefill's attention kernel
+    performed in its last call on `workspace` (reads the plan; synchronises)."""
+    n = ctypes.c_longlong(0)
+    _check("nd_swa_sink_prefill_tiles", _lib().nd_swa_sink_prefill_tiles(
+        _ptr(workspace), batch, T, n_q_heads, n_kv_heads, head_dim, float(rope_theta), int(block), ctypes.byref(n)))
+    return n.value
 
 
 def nd_rope_apply(x: torch.Tensor, y: Optional[torch.Tensor] = None, rope_theta: float = 10000.0,

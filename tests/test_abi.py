@@ -100,6 +100,18 @@ def test_host_validation_before_any_device_work():
     # append: head_dim not a multiple of 32
     c2 = nd.nd._Cache(1, 1, 48, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
     assert lib.nd_kv_append_quant(ctypes.byref(c2), P(16), P(16), 0, None) == 1
+    # prefill -> cache handoff: a ring is required, the row map is required,
+    # src_seg is required with seg_ids, k / v aligned, head_dim 32..256
+    fill = lib.nd_kv_cache_from_prefill
+    fill.restype = ctypes.c_int
+    no_ring = nd.nd._Cache(1, 1, 64, 4, 0, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert fill(ctypes.byref(no_ring), P(16), P(16), 1, 8, None, None, P(16), None, None) == 1
+    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, None, None, None) == 1
+    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, P(16), None, P(16), None, None) == 1
+    assert fill(ctypes.byref(cache), P(18), P(16), 1, 8, None, None, P(16), None, None) == 1
+    assert fill(ctypes.byref(cache), P(16), P(16), -1, 8, None, None, P(16), None, None) == 1
+    wide = nd.nd._Cache(1, 1, 512, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert fill(ctypes.byref(wide), P(16), P(16), 1, 8, None, None, P(16), None, None) == 2
 
 
 def test_workspace_sizes():
@@ -173,6 +185,7 @@ def test_empty_problems_return_ok_without_a_device():
     calls = {
         "nd_kv_append_quant": (e, None, None, 0, None),
         "nd_kv_quant_rows": (None, ctypes.c_int64(0), 64, None, None, None),
+        "nd_kv_cache_from_prefill": (e, None, None, 1, 16, None, None, None, None, None),
         "nd_swa_sink_decode": (None, e, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step": (None, e, None, None, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step_host": (None, e, None, None, 4, 8, None, None, None, Z(0), None),

@@ -184,30 +184,35 @@ def test_bf16_many_segments_per_tile():
         assert_close_bf16(out, want, f"many segments W={window}")
 
 
-def test_packed_prefill_full_size_sampled():
+def test_packed_prefill_full_size_planes():
     """Packed-segment prefill at full size (B8 T4096 Hq32 Hkv8 d128, W256,
-    RoPE) in the bench's launch configuration; sampled rows vs the oracle."""
+    RoPE) in the bench's launch configuration.  Batch rows 0 and 7 are
+    compared whole (every row and head, out and lse) with the oracle, so every
+    persistent work item of those rows -- and the barrier phases each CTA
+    carries from one item to the next -- is checked; the other rows on their
+    first and last positions, around segment starts and at random."""
     w = packed_prefill()
     B, T, Hq, d = w["q"].shape
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
     out = nd().nd_swa_sink_prefill(dev_bf16(w["q_bits"]), dev_bf16(w["k_bits"]), dev_bf16(w["v_bits"]),
                                    dev(w["seg_ids"]), dev(w["sink"]), w["window"], rope_theta=w["rope_theta"],
                                    lse=lse)
-    got = host(out)
+    got, got_lse = host(out), host(lse)
+    rows = [(b, t) for b in (0, B - 1) for t in range(T)]
     rng = philox(901)
-    rows = [(b, t) for b in range(B) for t in (0, T - 1)]
-    rows += [(int(rng.integers(0, B)), int(rng.integers(0, T))) for _ in range(48)]
-    # rows at segment and sink boundaries
-    for b in (0, B - 1):
+    for b in range(1, B - 1):
+        rows += [(b, 0), (b, T - 1)] + [(b, int(t)) for t in rng.integers(0, T, size=24)]
         starts = np.nonzero(np.diff(w["seg_ids"][b]))[0] + 1
-        for s in starts[:3]:
-            rows += [(b, int(s)), (b, int(s) - 1), (b, int(s) + 300)]
-    rows = [(b, min(t, T - 1)) for b, t in rows]
+        for s0 in starts:
+            rows += [(b, int(s0)), (b, int(s0) - 1), (b, min(int(s0) + 300, T - 1))]
     want, wlse = oracle_rows(w["q"], w["k"], w["v"], w["seg_ids"], w["sink"], w["window"], w["rope_theta"], rows)
     gr = np.stack([got[b, t] for b, t in rows])
-    assert_close_bf16(gr, want, "packed prefill sampled rows")
-    gl = np.stack([host(lse)[b, :, t] for b, t in rows])
+    assert_close_bf16(gr, want, "packed prefill rows")
+    gl = np.stack([got_lse[b, :, t] for b, t in rows])
     np.testing.assert_allclose(gl, wlse, atol=2e-2, rtol=0)
+    for b in (0, B - 1):   # each whole plane on its own as well
+        sel = [i for i, r in enumerate(rows) if r[0] == b]
+        assert_close_bf16(gr[sel], want[sel], f"packed prefill batch row {b}")
 
 
 # ---------------------------------------------------------------- rope / pool / compressed
@@ -243,19 +248,28 @@ def test_compress_pool_matches_oracle(block, T, d):
 
 def test_compressed_prefill_full_size():
     """Compressed-attention configuration at full size (B4 T4096 H16 d64, W256,
-    b4, RoPE): pool (GPU) + rotation + attention, every row vs the oracle."""
+    b4, RoPE): pool (GPU) + rotation + attention.  Batch row 0 is compared
+    whole (every row and head) with the oracle; the other rows at the window
+    edge and block-arrival rows (255-263), the last row and at random."""
     w = compressed()
     B, T, H, d = w["q"].shape
     pk, pv = nd().nd_kv_compress_pool(dev_bf16(w["k_bits"]), dev_bf16(w["v_bits"]), w["block"], w["rope_theta"])
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
     out = nd().nd_swa_sink_prefill(dev_bf16(w["q_bits"]), dev_bf16(w["k_bits"]), dev_bf16(w["v_bits"]),
                                    None, None, w["window"], rope_theta=w["rope_theta"], pooled_k=pk,
-                                   pooled_v=pv, block=w["block"])
-    got = host(out)
+                                   pooled_v=pv, block=w["block"], lse=lse)
+    got, got_lse = host(out), host(lse)
     rng = philox(1200)
-    rows = np.array([(b, t) for b in range(B) for t in (0, 255, 256, 258, 259, 262, 263, 1000, T - 1)]
-                    + [(int(rng.integers(0, B)), int(rng.integers(0, T))) for _ in range(64)])
-    want, _ = oracle.compressed_prefill(w["q"], w["k"], w["v"], w["window"], w["block"], w["rope_theta"], rows=rows)
-    assert_close_bf16(np.stack([got[b, t] for b, t in rows]), want, "compressed sampled rows")
+    rows = [(0, t) for t in range(T)]
+    rows += [(b, t) for b in range(1, B) for t in (0, 255, 256, 258, 259, 262, 263, 1000, T - 1)]
+    rows += [(int(rng.integers(1, B)), int(rng.integers(0, T))) for _ in range(64)]
+    rows = np.array(rows)
+    want, wlse = oracle.compressed_prefill(w["q"], w["k"], w["v"], w["window"], w["block"], w["rope_theta"],
+                                           rows=rows)
+    gr = np.stack([got[b, t] for b, t in rows])
+    assert_close_bf16(gr, want, "compressed rows")
+    assert_close_bf16(gr[:T], want[:T], "compressed batch row 0")
+    np.testing.assert_allclose(np.stack([got_lse[b, :, t] for b, t in rows]), wlse, atol=2e-2, rtol=0)
 
 
 @pytest.mark.parametrize("T,W,block", [(300, 16, 4), (129, 1, 2), (513, 64, 8), (64, 8, 1)])

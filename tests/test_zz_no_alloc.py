@@ -1,11 +1,11 @@
 """nd_swa_sink_decode_noalloc: the decode entry point for callers that cannot
-allocate device memory (a thread recording a CUDA graph with a frozen memory
-plan, a serving loop that must not call cudaMalloc, a host runtime that owns
-all device memory).  Its split-K scratch is a fixed device array inside the
-library; these tests call it through the C ABI and check it against
-nd_swa_sink_decode with a caller workspace, on two calls in a row (the second
-call reuses the scratch the first one left behind), and check that shapes
-needing more scratch than the array holds are refused.
+allocate device memory (a serving loop that must not call cudaMalloc, a host
+runtime that owns all device memory).  Its split-K scratch is a fixed device
+array inside the library; these tests call it through the C ABI and check it
+against nd_swa_sink_decode with a caller workspace and against the oracle, on
+two calls in a row (the second call reuses the scratch the first one left
+behind), and check that shapes needing more scratch than the array holds, and
+shapes the workspace entry point refuses, are refused with the same status.
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test."""
@@ -20,14 +20,14 @@ from workloads import decode_cache, normal_bf16, philox
 pytestmark = pytest.mark.gpu
 
 
-def _device_cache(nd, w, S, W):
+def _caches(nd, w, S, W):
     ref = oracle.Cache(*w["k"].shape[:2], w["k"].shape[3], S, W)
     ref.k_codes[...], ref.k_scale[...] = oracle.quant_g32(w["k"])
     ref.v_codes[...], ref.v_scale[...] = oracle.quant_g32(w["v"])
     for f in ("sink_len", "ring_start", "ring_len", "seq_len"):
         getattr(ref, f)[...] = w[f]
-    return nd.KVCache(dev(ref.k_codes), dev(ref.v_codes), dev(ref.k_scale), dev(ref.v_scale),
-                      dev(ref.sink_len), dev(ref.ring_start), dev(ref.ring_len), dev(ref.seq_len), S, W)
+    return ref, nd.KVCache(dev(ref.k_codes), dev(ref.v_codes), dev(ref.k_scale), dev(ref.v_scale),
+                           dev(ref.sink_len), dev(ref.ring_start), dev(ref.ring_len), dev(ref.seq_len), S, W)
 
 
 def test_noalloc_decode_matches_workspace_decode_on_two_calls():
@@ -39,12 +39,12 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
     # and needs scratch for the partials
     w = decode_cache(8, 8, 2, 64, S, W, seed=2023, full=True)
     B, Hq, d = w["q"].shape
-    cache = _device_cache(nd, w, S, W)
+    ref, cache = _caches(nd, w, S, W)
     need = nd.nd_swa_sink_decode_workspace_size(B, Hq, cache.n_kv_heads, d, S + W)
     assert 0 < need <= nd.nd.NOALLOC_SCRATCH_BYTES
     rng = philox(2024)
-    queries = [w["q_bits"], normal_bf16(rng, (B, Hq, d))[0]]
-    for call, q_bits in enumerate(queries):
+    queries = [(w["q_bits"], w["q"]), normal_bf16(rng, (B, Hq, d))]
+    for call, (q_bits, q_f32) in enumerate(queries):
         q = dev_bf16(q_bits)
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         want = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
@@ -56,7 +56,29 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
         torch.cuda.synchronize()
         assert_close_bf16(host(got), host(want), f"noalloc call {call}")
         np.testing.assert_allclose(host(got_lse), host(want_lse), atol=2e-3, rtol=0)
+        ref_out, ref_lse = oracle.decode(q_f32, ref, W)
+        assert_close_bf16(host(got), ref_out, f"noalloc call {call} vs oracle")
+        np.testing.assert_allclose(host(got_lse), ref_lse, atol=2e-3, rtol=0)
     assert nd.nd_device_errors(clear=True) == 0
+
+
+def test_noalloc_refuses_what_the_workspace_decode_refuses():
+    """Shapes the workspace entry point refuses get the same status here,
+    not ND_ERR_WORKSPACE, even when they are large."""
+    need_gpu()
+    import sliding_window_kv_swa_gb300 as nd
+    B, Hkv, d, S, W = 2, 8, 128, 1024, 256
+    cache = nd.KVCache.empty(B, Hkv, d, S, W)
+    for Hq, want in ((80, nd.nd.ND_ERR_UNSUPPORTED),   # 10 query heads per KV head (at most 8)
+                     (12, nd.nd.ND_ERR_INVALID_ARG)):  # not a multiple of the KV heads
+        q = torch.zeros((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty_like(q)
+        for fn in (lambda: nd.nd_swa_sink_decode_noalloc(q, cache, W, out=out),
+                   lambda: nd.nd_swa_sink_decode(q, cache, W, out=out,
+                                                 workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))):
+            with pytest.raises(nd.NDError) as ei:
+                fn()
+            assert ei.value.status == want
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
