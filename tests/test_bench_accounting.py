@@ -37,26 +37,20 @@ def test_decode_bytes():
     assert cache5 == 512 * 1280 * 2304
 
 
-def test_performed_tile_counts_bound_the_visible_tiles():
-    """The prefill tile count the bench reports sits between the tiles that
-    hold a visible pair (brute force on the oracle's mask) and all causal
-    tiles."""
-    import bench
-    import oracle
-    rng = philox(77)
-    B, T, W, span, bn = 2, 700, 100, 128, 64
-    seg, sink = packed_segments(rng, B, T, 2, 4, 120, 3, 40)
-    mask = oracle.causal_packing_mask(seg, sink, W)   # [B][T][T] bool
-    visible, causal = 0, 0
-    for b in range(B):
-        for q0 in range(0, T, span):
-            q1 = min(T, q0 + span)
-            for k0 in range(0, q1, bn):
-                causal += 1
-                visible += bool(mask[b, q0:q1, k0:k0 + bn].any())
-    got = bench.performed_tiles_packed(seg, sink, W, span, bn)
-    assert visible <= got <= causal, (visible, got, causal)
-    # one segment, no sinks, no window: every causal tile
-    seg1 = np.ones((1, T), np.int32)
-    assert bench.performed_tiles_packed(seg1, np.zeros((1, T), np.uint8), 0, span, bn) == \
-        sum((min(T, q0 + span) - 1) // bn + 1 for q0 in range(0, T, span))
+def test_fill_kept_tokens_matches_the_append_rule():
+    """The handoff row's algorithmic bytes count the tokens the append rule
+    keeps: the accepted sink prefix and the newest ring tokens."""
+    seg = np.array([[1] * 10 + [2] * 6 + [0] * 2 + [3] * 5], np.int32)
+    sink = np.zeros_like(seg, dtype=np.uint8)
+    sink[0, :4] = 1          # segment 1: 4 sinks, 6 ring tokens
+    sink[0, 10:16] = 1       # segment 2: sinks only
+    kept, n = bench.fill_kept_tokens(seg, sink, S=3, W=4)
+    assert n == 3
+    assert kept == (3 + 4) + (3 + 0) + (0 + 4)
+
+
+def test_rows_cover_every_measured_configuration():
+    assert set(bench.ALL_ROWS) >= {"step_b64", "sweep", "packed", "compressed", "compressed_b8", "tiny", "pool",
+                                   "append", "fill", "cdecode", "wsweep"}
+    r = bench.roofline("hbm", 6e9, 1.0, 6000.0, "GB/s", "k", "measured")
+    assert abs(r["achieved"] - 6000.0) < 1e-9 and abs(r["frac"] - 1.0) < 1e-12

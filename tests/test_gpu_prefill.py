@@ -340,3 +340,39 @@ def test_prefill_calls_back_to_back_share_a_workspace():
     torch.cuda.synchronize()
     for i, (a, c) in enumerate(zip(alone, chained)):
         assert torch.equal(a.view(torch.int16), c.view(torch.int16)), f"call {i}"
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 2, 64), (3, 1, 128)])
+def test_prefill_tile_count_reported_by_the_kernel_plan(Hq, Hkv, d):
+    """nd_swa_sink_prefill_tiles reads the plan the call built: at least
+    every (128-row block, 64-key tile) holding a visible pair (brute force on
+    the oracle's mask) times the query heads, at most every causal tile of
+    the span the plan covers; one segment without sinks or window: exactly
+    the causal tiles."""
+    rng = philox(1900 + d)
+    B, T, W = 2, 700, 100
+    qb, _ = normal_bf16(rng, (B, T, Hq, d))
+    kb, _ = normal_bf16(rng, (B, T, Hkv, d))
+    vb, _ = normal_bf16(rng, (B, T, Hkv, d))
+    seg, sink = packed_segments(rng, B, T, 2, 4, 120, 3, 40)
+    lib = nd()
+    pair = (Hq // Hkv) % 2 == 0
+    span = 128 if pair else 256
+    blocks = 1 if pair else 2
+    for segs, snk, win in ((seg, sink, W), (np.ones((B, T), np.int32), None, 0)):
+        ws = torch.empty(lib.nd_swa_sink_prefill_workspace_size(lib.ND_BF16, B, T, Hq, Hkv, d, 0.0, 0),
+                         dtype=torch.uint8, device="cuda")
+        lib.nd_swa_sink_prefill(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), dev(segs),
+                                None if snk is None else dev(snk), win, workspace=ws)
+        got = lib.nd_swa_sink_prefill_tiles(ws, B, T, Hq, Hkv, d, 0.0, 0)
+        mask = oracle.causal_packing_mask(segs, snk, win)
+        visible = causal = 0
+        for b in range(B):
+            for q0 in range(0, T, 128):
+                q1 = min(T, q0 + 128)
+                visible += sum(bool(mask[b, q0:q1, k0:k0 + 64].any()) for k0 in range(0, q1, 64))
+            for q0 in range(0, T, span):
+                causal += ((min(T, q0 + span) - 1) // 64 + 1) * blocks
+        assert visible * Hq <= got <= causal * Hq, (visible * Hq, got, causal * Hq)
+        if snk is None:
+            assert got == causal * Hq
