@@ -325,6 +325,40 @@ def compress(q, k, v, block: int, theta: float, table_len: Optional[int] = None)
     return q_out, k_out, v_out
 
 
+def chunk_prefill(q, k, v, cache: Cache, window: int):
+    """Chunked prefill against the bounded cache: the chunk's tokens sit at
+    positions p0 .. p0+Tc-1 (p0 = seq_len of each sequence) and each attends,
+    under the decode mask ("256-token 滑动窗口：源码走读": causal, and a sink at
+    any distance or qpos - kpos < window), to every occupied cache slot
+    (dequantised: code * scale) and to the chunk's own keys.  Afterwards the
+    chunk's tokens are appended to the ring, one kv_append each.
+    q [B,Tc,Hq,d], k / v [B,Tc,Hkv,d] (already rotated).  Returns
+    (out [B,Tc,Hq,d], lse [B,Tc,Hq], the cache after the appends)."""
+    q = _c(q, np.float64)
+    k = _c(k, np.float64)
+    v = _c(v, np.float64)
+    B, Tc, Hq, d = q.shape
+    out = np.empty((B, Tc, Hq, d))
+    lse = np.empty((B, Tc, Hq))
+    for b in range(B):
+        kpos, is_sink = slot_positions(cache, b)
+        occ = np.nonzero(kpos >= 0)[0]
+        p0 = int(cache.seq_len[b])
+        ck = dequant_g32(cache.k_codes[b][:, occ], cache.k_scale[b][:, occ]).transpose(1, 0, 2)
+        cv = dequant_g32(cache.v_codes[b][:, occ], cache.v_scale[b][:, occ]).transpose(1, 0, 2)
+        keys = np.concatenate([ck, k[b]], axis=0)[None]
+        vals = np.concatenate([cv, v[b]], axis=0)[None]
+        pos = np.concatenate([kpos[occ], p0 + np.arange(Tc)])
+        snk = np.concatenate([is_sink[occ], np.zeros(Tc, bool)])
+        mask = np.stack([decode_keep(p0 + t, pos, snk, window) for t in range(Tc)])
+        o, l = attention(q[b][None], keys, vals, mask)
+        out[b], lse[b] = o[0], l[0]
+    new = cache.copy()
+    for t in range(Tc):
+        kv_append(new, k[:, t], v[:, t], False)
+    return out, lse, new
+
+
 def round_bf16(x) -> np.ndarray:
     """Storage rounding to bf16 (round to nearest even), returned as fp64:
     fp64 -> fp32 (numpy's rounding) -> bf16 on the bit pattern."""

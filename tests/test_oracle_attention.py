@@ -279,3 +279,68 @@ def test_decode_window_smaller_than_ring_hides_oldest():
     vd = oracle.dequant_g32(cache.v_codes[0, :, keep], cache.v_scale[0, :, keep])
     o, _ = oracle.attention(w["q"][:, None], kd[None], vd[None], np.ones((1, len(keep)), bool))
     np.testing.assert_allclose(out_w3[0], o[0, 0], atol=1e-13, rtol=0)
+
+
+# ---------------------------------------------------------------- chunked prefill against the cache
+
+def _exact_int8_tokens(rng, shape):
+    """Token values the int8 group-32 codec stores exactly: per 32-channel
+    group, codes in [-127, 127] with one at +-127, times 2^-6 (so
+    amax/127 = 2^-6 and every x / scale is the integer code)."""
+    codes = rng.integers(-127, 128, size=shape).astype(np.float64)
+    g = codes.reshape(shape[:-1] + (shape[-1] // 32, 32))
+    g[..., 0] = np.where(rng.random(g.shape[:-1]) < 0.5, 127.0, -127.0)
+    return g.reshape(shape) / 64.0
+
+
+@pytest.mark.parametrize("S,W,ring_cap,Tc,n_sink,n_before", [
+    (8, 6, 6, 10, 5, 20),    # ring wrapped, window = ring
+    (4, 5, 9, 7, 4, 3),      # ring partly filled, window < ring
+    (6, 4, 4, 3, 0, 0),      # empty cache
+    (3, 50, 60, 12, 3, 30),  # window longer than what was seen
+])
+def test_chunk_prefill_equals_prefill_rows_of_the_whole_sequence(S, W, ring_cap, Tc, n_sink, n_before):
+    """With token values the codec stores exactly, prefilling a chunk against
+    the cache gives exactly rows p0.. of the prefill of the whole sequence
+    under make_causal_packing_mask (one segment, its first n_sink tokens
+    sinks, the window): what the ring dropped is outside every chunk row's
+    window, and the sinks are kept."""
+    rng = philox(500 + S + W + Tc)
+    B, Hq, Hkv, d = 2, 4, 2, 64
+    T = n_sink + n_before + Tc
+    k = _exact_int8_tokens(rng, (B, T, Hkv, d))
+    v = _exact_int8_tokens(rng, (B, T, Hkv, d))
+    q = rng.standard_normal((B, T, Hq, d))
+    cache = oracle.Cache(B, Hkv, d, S, ring_cap)
+    for t in range(n_sink + n_before):
+        oracle.kv_append(cache, k[:, t], v[:, t], t < n_sink)
+    p0 = n_sink + n_before
+    out, lse, after = oracle.chunk_prefill(q[:, p0:], k[:, p0:], v[:, p0:], cache, W)
+    seg = np.ones((B, T), np.int32)
+    sink = np.zeros((B, T), np.uint8)
+    sink[:, :n_sink] = 1
+    want, wlse = oracle.swa_sink_prefill(q, k, v, seg, sink, W)
+    np.testing.assert_allclose(out, want[:, p0:], atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, wlse[:, p0:], atol=1e-12, rtol=0)
+    # the cache after the chunk is the cache after appending it token by token
+    ref = cache.copy()
+    for t in range(p0, T):
+        oracle.kv_append(ref, k[:, t], v[:, t], False)
+    for f in ("k_codes", "v_codes", "k_scale", "v_scale", "sink_len", "ring_start", "ring_len", "seq_len"):
+        np.testing.assert_array_equal(getattr(after, f), getattr(ref, f))
+
+
+def test_chunk_of_one_token_is_the_decode_of_that_token():
+    """A one-token chunk is the decode step with the token's exact key: with
+    codec-exact values, the chunk's output equals decode() after appending it."""
+    rng = philox(510)
+    B, Hq, Hkv, d, S, W = 3, 8, 2, 64, 4, 8
+    cache = oracle.Cache(B, Hkv, d, S, W)
+    k = _exact_int8_tokens(rng, (B, 20, Hkv, d))
+    v = _exact_int8_tokens(rng, (B, 20, Hkv, d))
+    for t in range(19):
+        oracle.kv_append(cache, k[:, t], v[:, t], t < 3)
+    q = rng.standard_normal((B, 1, Hq, d))
+    out, _, after = oracle.chunk_prefill(q, k[:, 19:], v[:, 19:], cache, W)
+    want, _ = oracle.decode(q[:, 0], after, W)
+    np.testing.assert_allclose(out[:, 0], want, atol=1e-12, rtol=0)
