@@ -420,6 +420,36 @@ ND_API int nd_swa_sink_prefill(const void *q, const void *k, const void *v,
                         size_t workspace_bytes, nd_stream_t stream);
 
 /*
+ * Chunked prefill against the bounded cache: a chunk of `chunk` new tokens
+ * per sequence, at positions p0 .. p0+chunk-1 where p0 = seq_len, attends
+ * under the decode mask of [N1] "256-token 滑动窗口：源码走读" (causal, and a
+ * sink at any distance or qpos - kpos < window) to the cached sink and ring
+ * entries and to the chunk's own keys -- the rows p0.. of a prefill over the
+ * whole sequence, computed from the cache instead of the evicted prefix.
+ * Then the chunk's tokens are ring-appended to the cache (exactly as `chunk`
+ * calls of nd_kv_append_quant with to_sink = 0), so the next chunk or decode
+ * step continues from it.
+ *   q     bf16 [batch][chunk][n_q_heads][head_dim]  (rotated at their
+ *   k, v  bf16 [batch][chunk][n_kv_heads][head_dim]  positions, if the model
+ *                                                    rotates q and k)
+ *   out   bf16 [batch][chunk][n_q_heads][head_dim]
+ *   lse   fp32 [batch][n_q_heads][chunk], or NULL
+ * The cached keys are dequantised (code * scale) and rounded to bf16 for the
+ * tensor cores; the chunk's keys are used as given.  GQA as the prefill.
+ * Requires window >= 1, ring_cap > 0, head_dim 64 or 128; the workspace
+ * (device, 16-byte aligned) holds nd_swa_sink_chunk_prefill_workspace_size()
+ * bytes (the gathered bf16 keys and values of sink_cap + min(ring_cap,
+ * window-1) + chunk positions per sequence, and the tile plan).
+ */
+ND_API size_t nd_swa_sink_chunk_prefill_workspace_size(int batch, int chunk, int n_q_heads,
+                                                       int n_kv_heads, int head_dim, int sink_cap,
+                                                       int ring_cap, int window);
+ND_API int nd_swa_sink_chunk_prefill(const void *q, const void *k, const void *v, int chunk,
+                                     const nd_kv_cache *cache, int n_q_heads, int window,
+                                     void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, nd_stream_t stream);
+
+/*
  * Work the bf16 prefill's attention kernel performed: after an
  * nd_swa_sink_prefill call with dtype ND_BF16 and these arguments has run on
  * `workspace` (the call's own workspace, not yet reused), writes to

@@ -563,6 +563,83 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
   return finish(launch_prefill_tc(a, ws, device_error_word(), s));
 }
 
+// Chunked prefill workspace: gathered keys and values, segment ids, sink
+// flags, the metadata snapshot, then the prefill's tile records and plan.
+struct ChunkLayout {
+  int R, Tk;
+  size_t kk, vv, seg, sink, meta, plan, total;
+};
+static ChunkLayout chunk_layout(int batch, int chunk, int n_kv_heads, int head_dim, int sink_cap, int ring_cap,
+                                int window) {
+  ChunkLayout L;
+  L.R = chunk_ring_rows(ring_cap, window);
+  L.Tk = sink_cap + L.R + chunk;
+  const size_t rows = size_t(batch) * L.Tk;
+  L.kk = 0;
+  L.vv = L.kk + round_up(rows * n_kv_heads * head_dim * 2, 256);
+  L.seg = L.vv + round_up(rows * n_kv_heads * head_dim * 2, 256);
+  L.sink = L.seg + round_up(rows * 4, 256);
+  L.meta = L.sink + round_up(rows, 256);
+  L.plan = L.meta + round_up(size_t(batch) * 16, 256);
+  L.total = L.plan + round_up(prefill_plan_bytes(batch, L.Tk, 0), 256);
+  return L;
+}
+
+size_t nd_swa_sink_chunk_prefill_workspace_size(int batch, int chunk, int n_q_heads, int n_kv_heads,
+                                                int head_dim, int sink_cap, int ring_cap, int window) {
+  if (batch <= 0 || chunk <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || sink_cap < 0 ||
+      ring_cap <= 0 || window < 1)
+    return 0;
+  return chunk_layout(batch, chunk, n_kv_heads, head_dim, sink_cap, ring_cap, window).total;
+}
+
+int nd_swa_sink_chunk_prefill(const void *q, const void *k, const void *v, int chunk, const nd_kv_cache *cache,
+                              int n_q_heads, int window, void *out, float *lse, void *workspace,
+                              size_t workspace_bytes, nd_stream_t stream) {
+  int st = validate_cache(cache);
+  if (st != ND_OK) return st;
+  if (chunk < 0 || window < 1 || n_q_heads <= 0 || n_q_heads % cache->n_kv_heads || cache->ring_cap <= 0)
+    return ND_ERR_INVALID_ARG;
+  if (cache->head_dim != 64 && cache->head_dim != 128) return ND_ERR_UNSUPPORTED;
+  if (cache->batch == 0 || chunk == 0) return ND_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return ND_ERR_INVALID_ARG;
+  const int B = cache->batch, d = cache->head_dim;
+  const ChunkLayout L = chunk_layout(B, chunk, cache->n_kv_heads, d, cache->sink_cap, cache->ring_cap, window);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return ND_ERR_WORKSPACE;
+  if ((st = check_device(nullptr)) != ND_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int *err = device_error_word();
+  char *ws = static_cast<char *>(workspace);
+  int32_t *meta = reinterpret_cast<int32_t *>(ws + L.meta);
+  cudaError_t e = launch_chunk_gather(*cache, k, v, chunk, window, ws + L.kk, ws + L.vv,
+                                     reinterpret_cast<int32_t *>(ws + L.seg), reinterpret_cast<uint8_t *>(ws + L.sink),
+                                     meta, err, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  PrefillArgs a;
+  a.q = q;
+  a.k = ws + L.kk;
+  a.v = ws + L.vv;
+  a.dtype = ND_BF16;
+  a.batch = B;
+  a.T = L.Tk;
+  a.Hq = n_q_heads;
+  a.Hkv = cache->n_kv_heads;
+  a.d = d;
+  a.seg_ids = reinterpret_cast<const int32_t *>(ws + L.seg);
+  a.sink = reinterpret_cast<const uint8_t *>(ws + L.sink);
+  a.window = window;
+  a.pooled_k = a.pooled_v = nullptr;
+  a.block = 0;
+  a.out = out;
+  a.lse = lse;
+  a.q_off = cache->sink_cap + L.R;
+  e = launch_prefill_tc_prep(a, ws + L.plan, s);
+  if (e == cudaSuccess) e = launch_prefill_tc(a, ws + L.plan, err, s);
+  if (e == cudaSuccess) e = launch_chunk_append(*cache, k, v, chunk, meta, s);
+  return finish(e);
+}
+
 int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                   float rope_theta, nd_stream_t stream) {
   if (batch < 0 || T < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2) return ND_ERR_INVALID_ARG;

@@ -60,6 +60,16 @@ cudaError_t launch_compressed_append(const nd_kv_cache &c, float *k_sum, float *
                                      int window, const void *q, int Hq, const void *k_new, const void *v_new,
                                      void *q_rot, float theta, int *err, cudaStream_t stream);
 
+// Chunked prefill against the cache: ring rows of the gathered key layout,
+// the gather (cache -> bf16 keys / values, segment ids, sink flags, and a
+// metadata snapshot [B][4]) and the chunk's ring append from that snapshot;
+// dependent launches.
+int chunk_ring_rows(int ring_cap, int window);
+cudaError_t launch_chunk_gather(const nd_kv_cache &c, const void *k, const void *v, int Tc, int window, void *kk,
+                                void *vv, int32_t *seg, uint8_t *sink, int32_t *meta, int *err, cudaStream_t stream);
+cudaError_t launch_chunk_append(const nd_kv_cache &c, const void *k, const void *v, int Tc, const int32_t *meta,
+                                cudaStream_t stream);
+
 cudaError_t launch_rope(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                         float theta, cudaStream_t stream);
 
@@ -124,6 +134,9 @@ struct PrefillArgs {
   // bf16 path: (cos, sin) table float2 [T][d/2] of the rotation; q is then
   // rotated inside the attention kernel (k arrives rotated).  NULL: q as is.
   const void *rope_cs = nullptr;
+  // bf16 path: queries are key rows q_off .. T-1 (q, out and lse hold
+  // T - q_off rows); 0 for an ordinary prefill
+  int q_off = 0;
 };
 
 size_t prefill_plan_bytes(int batch, int T, int block);

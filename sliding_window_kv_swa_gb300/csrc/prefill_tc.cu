@@ -89,6 +89,9 @@ static_assert(sizeof(TileMeta) == 384, "16-byte chunks for cp.async");
 
 struct TcParams {
   int B, T, Hq, Hkv, G, W, block, nb, n_span, span, n_kt, plan_stride, pair_heads, n_pairs;
+  // queries are key rows q_off .. T-1 (Tq = T - q_off of them); q, out and lse
+  // hold only those rows
+  int q_off, Tq;
   const int32_t *seg;
   const uint8_t *sink;
   const int32_t *plan;
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(1024) tile_prep_kernel(TcParams p, TileMeta *m
   }
   __syncthreads();
   for (int sp = warp; sp < p.n_span; sp += nw) {
-    const int q0 = sp * p.span, q1 = min(p.T, q0 + p.span) - 1;
+    const int q0 = p.q_off + sp * p.span, q1 = min(p.T, q0 + p.span) - 1;
     int32_t *out = plan + (size_t(b) * p.n_span + sp) * p.plan_stride;
     int n = 0;
     if (p.block > 0) {
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.b = rest / p.n_span;
     it.head0 = p.pair_heads ? 2 * pr : pr;
     it.head1 = p.pair_heads ? it.head0 + 1 : it.head0;
-    it.row00 = p.pair_heads ? sp * BM : sp * 2 * BM;
+    it.row00 = p.q_off + (p.pair_heads ? sp * BM : sp * 2 * BM);
     it.row01 = p.pair_heads ? it.row00 : it.row00 + BM;
     it.hk = it.head0 / p.G;
     const int32_t *plan = p.plan + (size_t(it.b) * p.n_span + sp) * p.plan_stride;
@@ -619,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it >= 2 && !lwait(&q_empty[qb], ((it >> 1) - 1) & 1)) return false;
       expect_tx(&q_full[qb], 2 * L::kQ, leader);
       for (int x = 0; x < L::kBoxes; ++x) {
-        tma_load_4d(sQ(qb, 0) + x * BM * 128, &tm_q, 64 * x, I.head0, I.row00, I.b, &q_full[qb], leader);
-        tma_load_4d(sQ(qb, 1) + x * BM * 128, &tm_q, 64 * x, I.head1, I.row01, I.b, &q_full[qb], leader);
+        tma_load_4d(sQ(qb, 0) + x * BM * 128, &tm_q, 64 * x, I.head0, I.row00 - p.q_off, I.b, &q_full[qb], leader);
+        tma_load_4d(sQ(qb, 1) + x * BM * 128, &tm_q, 64 * x, I.head1, I.row01 - p.q_off, I.b, &q_full[qb], leader);
       }
       return true;
     };
@@ -876,7 +879,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ld_shared_v4(stage + rr * 64 + ((ch ^ ((rr >> 1) & 3)) << 4), a0, a1, a2, a3);
             const int qq = row0 + rr;
             if (qq < p.T)
-              st_global_v4(p.out + ((size_t(I.b) * p.T + qq) * p.Hq + head) * D + x + 8 * ch, a0, a1, a2, a3);
+              st_global_v4(p.out + ((size_t(I.b) * p.Tq + (qq - p.q_off)) * p.Hq + head) * D + x + 8 * ch, a0, a1,
+                           a2, a3);
           }
           __syncwarp();  // the staging block is free again
         }
@@ -1087,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_inv[rb][r] = l > 0.f ? 1.f / l : 0.f;
     mbar_arrive(&epi_full[rb]);
     if (q < p.T && p.lse && !fail)
-      p.lse[(size_t(b) * p.Hq + head) * p.T + q] =
+      p.lse[(size_t(b) * p.Hq + head) * p.Tq + (q - p.q_off)] =
           l > 0.f ? (m_used * c + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     gt += n;
     }
@@ -1143,16 +1147,16 @@ struct PlanDims {
 // span = rows one CTA covers: 128 (two heads of a GQA pair) or 256 (two
 // consecutive row blocks of one head).  The workspace is sized for the larger
 // of the two so the query does not depend on the head layout.
-PlanDims plan_dims(int B, int T, int block, int span) {
+PlanDims plan_dims(int B, int T, int block, int span, int Tq) {
   PlanDims d;
   d.span = span;
-  d.n_span = (T + span - 1) / span;
+  d.n_span = (Tq + span - 1) / span;
   d.n_kt = (T + BN - 1) / BN;
   const int nb = block > 0 ? T / block : 0;
   d.n_pt = (nb + BN - 1) / BN;
   d.stride = 1 + d.n_kt + d.n_pt;
   d.sum_bytes = (size_t(B) * d.n_kt * sizeof(TileMeta) + 255) / 256 * 256;
-  d.plan_bytes = size_t(B) * ((T + BM - 1) / BM) * d.stride * sizeof(int32_t);
+  d.plan_bytes = size_t(B) * ((Tq + BM - 1) / BM) * d.stride * sizeof(int32_t);
   return d;
 }
 
@@ -1167,12 +1171,14 @@ TcSetup tc_setup(const PrefillArgs &a, void *ws, int *err) {
   TcSetup S;
   const int G = a.Hq / a.Hkv;
   const bool pair_heads = G % 2 == 0;
-  S.pd = plan_dims(a.batch, a.T, a.block, pair_heads ? BM : 2 * BM);
+  S.pd = plan_dims(a.batch, a.T, a.block, pair_heads ? BM : 2 * BM, a.T - a.q_off);
   S.meta = static_cast<TileMeta *>(ws);
   S.plan = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + S.pd.sum_bytes);
   TcParams &p = S.p;
   p.B = a.batch;
   p.T = a.T;
+  p.q_off = a.q_off;
+  p.Tq = a.T - a.q_off;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.G = G;
@@ -1201,7 +1207,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
   const TcSetup S = tc_setup(a, ws, err);
   const TcParams &p = S.p;
   CUtensorMap tq, tk, tv, tpk, tpv;
-  if (!make_map(&tq, a.q, a.batch, a.T, a.Hq, D, BM) || !make_map(&tk, a.k, a.batch, a.T, a.Hkv, D, BN) ||
+  if (!make_map(&tq, a.q, a.batch, a.T - a.q_off, a.Hq, D, BM) || !make_map(&tk, a.k, a.batch, a.T, a.Hkv, D, BN) ||
       !make_map(&tv, a.v, a.batch, a.T, a.Hkv, D, BN))
     return cudaErrorInvalidValue;
   if (a.block > 0 && p.nb > 0) {
@@ -1228,7 +1234,7 @@ cudaError_t launch_tc(const PrefillArgs &a, void *ws, int *err, cudaStream_t str
 }  // namespace
 
 size_t prefill_plan_bytes(int batch, int T, int block) {
-  PlanDims pd = plan_dims(batch, T, block, BM);  // the 128-row span has the most plan rows
+  PlanDims pd = plan_dims(batch, T, block, BM, T);  // the 128-row span has the most plan rows
   return pd.sum_bytes + pd.plan_bytes;
 }
 

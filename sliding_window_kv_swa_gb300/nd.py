@@ -85,6 +85,8 @@ def _lib():
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
             "nd_swa_sink_prefill_tiles": (I, [P, I, I, I, I, I, F, I, P]),
+            "nd_swa_sink_chunk_prefill_workspace_size": (S, [I, I, I, I, I, I, I, I]),
+            "nd_swa_sink_chunk_prefill": (I, [P, P, P, I, P, I, I, P, P, P, S, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
             "nd_kv_compress_pool": (I, [P, P, I, I, I, I, I, F, P, P, P]),
             "nd_kv_budget_window": (I, [P, P, P]),
@@ -110,6 +112,7 @@ EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_e
             "nd_compressed_decode_step_workspace_size", "nd_compressed_decode_step",
             "nd_swa_sink_prefill_workspace_size",
             "nd_swa_sink_prefill", "nd_swa_sink_prefill_tiles",
+            "nd_swa_sink_chunk_prefill_workspace_size", "nd_swa_sink_chunk_prefill",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
 
 
@@ -436,6 +439,31 @@ def nd_swa_sink_prefill_tiles(workspace: torch.Tensor, batch: int, T: int, n_q_h
     _check("nd_swa_sink_prefill_tiles", _lib().nd_swa_sink_prefill_tiles(
         _ptr(workspace), batch, T, n_q_heads, n_kv_heads, head_dim, float(rope_theta), int(block), ctypes.byref(n)))
     return n.value
+
+
+def nd_swa_sink_chunk_prefill_workspace_size(batch: int, chunk: int, n_q_heads: int, n_kv_heads: int,
+                                             head_dim: int, sink_cap: int, ring_cap: int, window: int) -> int:
+    return int(_lib().nd_swa_sink_chunk_prefill_workspace_size(batch, chunk, n_q_heads, n_kv_heads, head_dim,
+                                                               sink_cap, ring_cap, window))
+
+
+def nd_swa_sink_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cache: KVCache, window: int,
+                              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Prefill a chunk (q [B, Tc, Hq, d], k / v [B, Tc, Hkv, d], bf16, rotated)
+    against the cache, then ring-append the chunk to it; returns out."""
+    B, Tc, Hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = nd_swa_sink_chunk_prefill_workspace_size(B, Tc, Hq, cache.n_kv_heads, d, cache.sink_cap,
+                                                          cache.ring_cap, window)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    s = cache.struct()
+    _check("nd_swa_sink_chunk_prefill", _lib().nd_swa_sink_chunk_prefill(
+        _ptr(q), _ptr(k), _ptr(v), Tc, ctypes.byref(s), Hq, int(window), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return out
 
 
 def nd_rope_apply(x: torch.Tensor, y: Optional[torch.Tensor] = None, rope_theta: float = 10000.0,

@@ -112,6 +112,20 @@ def test_host_validation_before_any_device_work():
     assert fill(ctypes.byref(cache), P(16), P(16), -1, 8, None, None, P(16), None, None) == 1
     wide = nd.nd._Cache(1, 1, 512, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
     assert fill(ctypes.byref(wide), P(16), P(16), 1, 8, None, None, P(16), None, None) == 2
+    # chunked prefill: window >= 1, a ring, GQA ratio, head_dim 64/128, workspace
+    chunk = lib.nd_swa_sink_chunk_prefill
+    chunk.restype = ctypes.c_int
+    Z = ctypes.c_size_t
+    call = lambda c, hq, win, ws, n: chunk(P(16), P(16), P(16), 8, ctypes.byref(c), hq, win, P(16), None, ws, Z(n),
+                                           None)
+    assert call(cache, 4, 0, P(16), 1 << 20) == 1
+    assert call(no_ring, 4, 8, P(16), 1 << 20) == 1
+    c3 = nd.nd._Cache(1, 3, 64, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert call(c3, 4, 8, P(16), 1 << 20) == 1
+    c96 = nd.nd._Cache(1, 1, 96, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert call(c96, 4, 8, P(16), 1 << 20) == 2
+    assert call(cache, 4, 8, None, 1 << 20) == 4
+    assert call(cache, 4, 8, P(16), 16) == 4
 
 
 def test_workspace_sizes():
@@ -124,6 +138,10 @@ def test_workspace_sizes():
     # (64+2) floats per partial
     assert nd.nd_swa_sink_decode_workspace_size(8, 8, 2, 64, 320) == 0
     assert nd.nd_swa_sink_decode_workspace_size(8, 8, 2, 64, 1088) == 8 * 8 * 4 * 66 * 4
+    # chunked prefill: gathered bf16 keys and values of sinks + window-1 ring
+    # rows + the chunk, per sequence
+    n = nd.nd_swa_sink_chunk_prefill_workspace_size(2, 100, 8, 2, 64, 16, 32, 8)
+    assert n >= 2 * 2 * (16 + 7 + 100) * 2 * 64 * 2
     # prefill with rotation keeps rotated copies of q and k
     n = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, 1, 512, 4, 1, 64, 10000.0, 0)
     assert n >= 512 * 4 * 64 * 4 + 512 * 1 * 64 * 4
@@ -186,6 +204,7 @@ def test_empty_problems_return_ok_without_a_device():
         "nd_kv_append_quant": (e, None, None, 0, None),
         "nd_kv_quant_rows": (None, ctypes.c_int64(0), 64, None, None, None),
         "nd_kv_cache_from_prefill": (e, None, None, 1, 16, None, None, None, None, None),
+        "nd_swa_sink_chunk_prefill": (None, None, None, 16, e, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode": (None, e, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step": (None, e, None, None, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step_host": (None, e, None, None, 4, 8, None, None, None, Z(0), None),
