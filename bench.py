@@ -477,6 +477,79 @@ def bench_packed_prefill(torch, nd, steps, warmup, pk, dist=None, batch=8, cpu_b
                 launches=4 * steps)
 
 
+def bench_chunk(torch, nd, steps, warmup, pk, dist=None, B=8, Tc=4096, Hq=32, Hkv=8, d=128, S=1024, W=256,
+                cpu_budget=None):
+    """Chunked prefill of Tc new tokens per sequence against the large-batch
+    cache layout (full sinks and ring, random int8 contents), then the
+    chunk's append.  The cache advances with every call; its ring stays
+    full, so every call does the same work."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234 + 9)
+    ns = S + W
+    codes = lambda: torch.randint(-127, 128, (B, Hkv, ns, d), generator=g, device="cuda").to(torch.int8)
+    scales = lambda: torch.rand((B, Hkv, ns, d // 32), generator=g, device="cuda") * (1.1 / 127) + 2.2 / 127
+    cache = nd.KVCache(codes(), codes(), scales(), scales(), torch.full((B,), S, dtype=torch.int32, device="cuda"),
+                       torch.randint(0, W, (B,), generator=g, device="cuda").to(torch.int32),
+                       torch.full((B,), W, dtype=torch.int32, device="cuda"),
+                       torch.full((B,), S + W, dtype=torch.int32, device="cuda"), S, W)
+    q = torch.randn((B, Tc, Hq, d), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((B, Tc, Hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((B, Tc, Hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    ws = torch.empty(nd.nd_swa_sink_chunk_prefill_workspace_size(B, Tc, Hq, Hkv, d, S, W, W), dtype=torch.uint8,
+                     device="cuda")
+
+    def step(i):
+        nd.nd_swa_sink_chunk_prefill(q, k, v, cache, W, out=out, workspace=ws)
+
+    ms = time_graph(torch, step, steps, warmup, dist)
+    t = ms / steps
+    tiles = nd.nd_swa_sink_chunk_prefill_tiles(ws, B, Tc, Hq, Hkv, d, S, W, W)
+    # every chunk row sees the S sinks and W window keys (cache ring + chunk)
+    pairs = B * Tc * (S + W)
+    flops = 4.0 * d * pairs * Hq
+    tile_flops = 4.0 * 128 * 64 * d * tiles
+    orow = None
+    if int(os.environ.get("RANK", "0")) == 0 and cpu_budget is not None:
+        try:
+            orow = oracle_chunk_sample(Hq, Hkv, d, S, W, Tc, cpu_budget)
+        except Exception as ex:  # the product path never depends on it
+            orow = {"tok_s": None, "sample": f"unavailable: {ex}"}
+    return dict(config=f"chunked prefill B{B} x {Tc} new tokens, Hq{Hq} Hkv{Hkv} d{d}, against {S} sinks + {W} ring "
+                       f"(int8 g32), W{W}; gather + plan + attention + append", oracle=orow,
+                ms_per_step=t, tok_s=B * Tc / (t * 1e-3), visible_pairs=pairs, tiles=tiles,
+                tile_overhead=tile_flops / flops,
+                algorithmic=roofline("tensor", flops, t, pk["bf16"], "TFLOP/s", "whole call (visible pairs)",
+                                     pk["src"]),
+                roofline=roofline("tensor", tile_flops, t, pk["bf16"], "TFLOP/s",
+                                  "whole call (tiles the attention kernel's plan performed)", pk["src"]),
+                launches=4 * steps)
+
+
+def oracle_chunk_sample(Hq, Hkv, d, S, W, Tc, budget_s, rows=256):
+    """Times the oracle's chunked prefill on one sequence with the first
+    `rows` tokens of a chunk, scaled to tok/s."""
+    import oracle
+    from workloads import philox, random_codes
+    rng = philox(1234 + 9)
+    kc, ks, vc, vs = random_codes(rng, 1, Hkv, S + W, d)
+    ref = oracle.Cache(1, Hkv, d, S, W)
+    ref.k_codes[...], ref.k_scale[...], ref.v_codes[...], ref.v_scale[...] = kc, ks, vc, vs
+    ref.sink_len[:], ref.ring_len[:], ref.seq_len[:] = S, W, S + W
+    q = rng.standard_normal((1, rows, Hq, d))
+    k = rng.standard_normal((1, rows, Hkv, d))
+    v = rng.standard_normal((1, rows, Hkv, d))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.chunk_prefill(q, k, v, ref, W)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return dict(tok_s=rows * n / el, cores=oracle.num_threads(), kind="oracle",
+                sample=f"{n} run(s) of a {rows}-token chunk of one sequence in {el:.1f} s (fp64 oracle)")
+
+
 def bench_compressed(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None, block=4):
     from workloads import compressed
     w = compressed()
@@ -748,7 +821,7 @@ def oracle_decode_sample(B, Hq, Hkv, d, S, W, seed, budget_s, of_batch=None):
 HEAD = dict(B=512, Hq=32, Hkv=8, d=128, S=1024, W=256)
 ORACLE_SAMPLE = 32   # sequences of the headline workload the oracle decodes per step
 ALL_ROWS = ("step_b64", "sweep", "wsweep", "packed", "compressed", "compressed_b8", "tiny", "pool", "append",
-            "fill", "cdecode")
+            "fill", "cdecode", "chunk")
 
 
 def main():
@@ -763,13 +836,20 @@ def main():
                     help="batch sizes of the decode sweep besides the headline's 512")
     ap.add_argument("--packed-batch", type=int, default=8,
                     help="sequences in the packed-prefill row (8 = the measured configuration; smaller for profiling)")
+    ap.add_argument("--head-batch", type=int, default=HEAD["B"],
+                    help="sequences of the headline decode step (512 = the measured configuration; smaller for "
+                         "profiling)")
+    ap.add_argument("--cdecode-batch", type=int, default=128,
+                    help="sequences of the compressed-decode row (128 = the measured configuration)")
+    ap.add_argument("--chunk-batch", type=int, default=8,
+                    help="sequences of the chunked-prefill row (8 = the measured configuration)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    h = HEAD
+    h = dict(HEAD, B=args.head_batch)
     workload = (f"decode step B{h['B']} Hq{h['Hq']} Hkv{h['Hkv']} d{h['d']}, {h['S']} sink slots + {h['W']}-slot ring "
                 f"(full, random offset), int8 g32 K/V, quantise-and-append of one bf16 token per sequence")
 
@@ -816,7 +896,7 @@ def main():
 
     with ClockSampler(dev_index) as clk:
         head = bench_decode(torch, nd, h["B"], h["Hq"], h["Hkv"], h["d"], h["S"], h["W"], steps, warmup,
-                            seed=rank_seed(1234 + 4, rank), pk=pk, dist=dist, traffic_key="decode@decode_b512")
+                            seed=rank_seed(1234 + 4, rank), pk=pk, dist=dist, traffic_key=f"decode@decode_b{h['B']}")
     clocks = clk.summary()
     e2e = e2e_decode(torch, nd, head.pop("_state"), h["B"], h["Hq"], h["Hkv"], h["d"], h["S"], h["W"],
                      min(steps, 50), warmup)
@@ -870,8 +950,13 @@ def main():
     if "fill" in want:
         rows["cache_handoff"] = bench_fill(torch, nd, row_steps, warmup, pk, dist)
         torch.cuda.empty_cache()
+    if "chunk" in want:
+        rows["chunk_prefill"] = bench_chunk(torch, nd, row_steps, warmup, pk, dist, B=args.chunk_batch,
+                                            cpu_budget=budget)
+        torch.cuda.empty_cache()
     if "cdecode" in want:
-        rows["compressed_decode"] = bench_compressed_decode(torch, nd, max(20, steps // 4), warmup, pk, dist)
+        rows["compressed_decode"] = bench_compressed_decode(torch, nd, max(20, steps // 4), warmup, pk, dist,
+                                                            B=args.cdecode_batch)
         torch.cuda.empty_cache()
 
     value = job_throughput(head["bytes_per_step"], steps, world, head["ms_per_step"] * steps)

@@ -81,6 +81,19 @@ ND_API int nd_last_cuda_error(void);
  */
 ND_API int nd_device_errors(int *flags_out, int clear);
 
+/*
+ * Failure-path hook for tests: the bf16 prefill's attention kernel waits
+ * for each row block's last P*V before its epilogue reads the output; that
+ * wait guards no copy in flight.  With polls > 0 the epilogue instead polls,
+ * `polls` times without blocking, a barrier that nothing arrives on, so the
+ * wait runs out on every CTA and raises device flag 1: the kernel then stops
+ * issuing work, lets what is in flight land, frees its tensor memory and
+ * exits, and the call's output is undefined.  0 restores the ordinary
+ * bounded wait.  Applies to the current device from the next launch on;
+ * blocks until earlier work on the legacy default stream is done.
+ */
+ND_API int nd_set_prefill_epilogue_wait_limit(unsigned polls);
+
 /* ------------------------------------------------------------------------ */
 /* Bounded KV cache                                                          */
 /* ------------------------------------------------------------------------ */
@@ -448,6 +461,13 @@ ND_API int nd_swa_sink_chunk_prefill(const void *q, const void *k, const void *v
                                      const nd_kv_cache *cache, int n_q_heads, int window,
                                      void *out, float *lse, void *workspace,
                                      size_t workspace_bytes, nd_stream_t stream);
+/* The tile products nd_swa_sink_chunk_prefill's attention kernel performed
+ * in its last call on `workspace` (as nd_swa_sink_prefill_tiles; the
+ * arguments are those of the call and of its cache). */
+ND_API int nd_swa_sink_chunk_prefill_tiles(const void *workspace, int batch, int chunk,
+                                           int n_q_heads, int n_kv_heads, int head_dim,
+                                           int sink_cap, int ring_cap, int window,
+                                           long long *tiles_out);
 
 /*
  * Work the bf16 prefill's attention kernel performed: after an

@@ -172,7 +172,8 @@ __device__ __forceinline__ float ldsf(uint32_t a) {
 // grids of at most four CTAs per SM, where the bytes each CTA keeps in flight
 // matter more than how many CTAs an SM holds.
 template <int D, int NW, int ST>
-__global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : (NW == 4 ? 5 : 1))
+    decode_kernel(const DecodeParams p) {
   constexpr int kStages = ST;
   constexpr int NG = D / 32;  // scale groups per row
   using S = Stage<D>;
@@ -497,10 +498,10 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : 1) dec
   }
   cp_async_wait<0>();
 
-  // At d = 64 (one CTA per SM) the next kernel's CTAs may be scheduled from
-  // here on; at d = 128 two or three CTAs share an SM and early-placed CTAs of the
-  // next step crowd unevenly, so there the trigger stays implicit (exit).
-  if (D == 64) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // With one CTA per SM (d = 64, 20 warps) the next kernel's CTAs may be
+  // scheduled from here on; where several CTAs share an SM, early-placed CTAs
+  // of the next step crowd unevenly, so there the trigger stays implicit (exit).
+  if (D == 64 && NW == 20) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- merge: quad-sum l, then the warps through shared memory (the stage
   //      buffers are free once every warp is past its loop)
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -595,8 +596,11 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 
 // Warps per CTA: 20 at head_dim 64 (one CTA per SM covers a whole short
 // sequence in one or two steps per warp), 4 at head_dim 128 (two or three CTAs
-// per SM, by ring depth).
+// per SM, by ring depth).  Grids of many (sequence, KV head) pairs at head_dim
+// 64 take a 4-warp build at five CTAs per SM instead (kManyPairs64): each
+// warp then walks more steps and a CTA's merge spans 4 warps, not 20.
 constexpr int warps_for(int D) { return D == 64 ? 20 : 4; }
+constexpr long kManyPairs64 = 4L * kTargetCtas;
 
 template <int D, int NW, int ST>
 size_t decode_smem_bytes() {
@@ -605,9 +609,8 @@ size_t decode_smem_bytes() {
   return stages > merge ? stages : merge;
 }
 
-template <int D, int ST>
+template <int D, int ST, int NW = warps_for(D)>
 cudaError_t launch_d(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
-  constexpr int NW = warps_for(D);
   const size_t smem = decode_smem_bytes<D, NW, ST>();
   auto kern = decode_kernel<D, NW, ST>;
   // the shared-memory opt-in once per device (a per-launch call is host
@@ -714,7 +717,10 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
     const long ctas = long(grid.x) * grid.y * grid.z;
     return ctas <= 4L * kTargetCtas ? launch_d<128, 5>(p, grid, stream) : launch_d<128, 4>(p, grid, stream);
   }
-  if (c.head_dim == 64) return launch_d<64, 4>(p, grid, stream);
+  if (c.head_dim == 64) {
+    const long ctas = long(grid.x) * grid.y * grid.z;
+    return ctas >= kManyPairs64 ? launch_d<64, 4, 4>(p, grid, stream) : launch_d<64, 4>(p, grid, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

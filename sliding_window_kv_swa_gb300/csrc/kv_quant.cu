@@ -235,37 +235,60 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
   }
   if (tid == 0) s_first_r = 0x7fffffff;
   if (tid < kFillTokens) s_src[tid] = -1;
-  // this thread's positions [t0, t1) of the batch row
-  const int per = (p.T + kFillThreads - 1) / kFillThreads;
-  const int t0 = min(p.T, tid * per), t1 = min(p.T, t0 + per);
+  __syncthreads();
+  // The batch row is walked in passes of 4 * kFillThreads positions: thread
+  // tid takes positions base + 4 tid .. + 3 (four independent loads in
+  // flight), ranks come from a block-wide prefix of the per-thread counts.
+  constexpr int kPer = 4, kPass = kPer * kFillThreads;
   const int32_t *sg = p.seg_ids ? p.seg_ids + size_t(b) * p.T : nullptr;
   const uint8_t *sk = p.sink ? p.sink + size_t(b) * p.T : nullptr;
-  int n_seg = 0, n_snk = 0, first_r = -1;
-  for (int t = t0; t < t1; ++t) {
-    if (sg && sg[t] != seg) continue;
-    const bool is_sink = sk && sk[t];
-    if (!is_sink && first_r < 0) first_r = n_seg;
-    n_seg += 1;
-    n_snk += is_sink;
-  }
-  // block-wide exclusive prefix of (n_seg, n_snk)
-  int a = n_seg, s = n_snk;
+  auto load_flags = [&](int base, bool *in, bool *snk) {
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int ya = __shfl_up_sync(0xffffffffu, a, off), ys = __shfl_up_sync(0xffffffffu, s, off);
-    if (lane >= off) a += ya, s += ys;
-  }
-  if (lane == 31) s_wsum[warp][0] = a, s_wsum[warp][1] = s;
-  __syncthreads();
-  int ex_seg = a - n_seg, ex_snk = s - n_snk, tot_seg = 0, tot_snk = 0;
+    for (int j = 0; j < kPer; ++j) {
+      const int t = base + kPer * tid + j;
+      in[j] = t < p.T && (!sg || sg[t] == seg);
+      snk[j] = in[j] && sk && sk[t];
+    }
+  };
+  // block-wide exclusive prefix of (a, s) over threads; totals in ta, ts
+  auto block_scan = [&](int a, int s, int &ea, int &es, int &ta, int &ts) {
+    int ia = a, is = s;
 #pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    if (w < warp) ex_seg += s_wsum[w][0], ex_snk += s_wsum[w][1];
-    tot_seg += s_wsum[w][0], tot_snk += s_wsum[w][1];
+    for (int off = 1; off < 32; off <<= 1) {
+      const int ya = __shfl_up_sync(0xffffffffu, ia, off), ys = __shfl_up_sync(0xffffffffu, is, off);
+      if (lane >= off) ia += ya, is += ys;
+    }
+    if (lane == 31) s_wsum[warp][0] = ia, s_wsum[warp][1] = is;
+    __syncthreads();
+    ea = ia - a, es = is - s, ta = 0, ts = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      if (w < warp) ea += s_wsum[w][0], es += s_wsum[w][1];
+      ta += s_wsum[w][0], ts += s_wsum[w][1];
+    }
+    __syncthreads();  // s_wsum is reused by the next call
+  };
+  // totals, and the rank of the first ring (non-sink) token: the segment's
+  // tokens before it, all sinks (no ring token: every token of the segment)
+  int tot_seg = 0, tot_snk = 0;
+  for (int base = 0; base < p.T; base += kPass) {
+    bool in[kPer], snk[kPer];
+    load_flags(base, in, snk);
+    int a = 0, s = 0, first_local = -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (in[j] && !snk[j] && first_local < 0) first_local = a;
+      a += in[j];
+      s += snk[j];
+    }
+    int ea, es, ta, ts;
+    block_scan(a, s, ea, es, ta, ts);
+    if (first_local >= 0) atomicMin(&s_first_r, tot_seg + ea + first_local);
+    tot_seg += ta;
+    tot_snk += ts;
   }
-  if (first_r >= 0) atomicMin(&s_first_r, ex_seg + first_r);
   __syncthreads();
-  const int f = s_first_r == 0x7fffffff ? tot_seg : s_first_r;  // rank of the first ring token
+  const int f = s_first_r == 0x7fffffff ? tot_seg : s_first_r;
   const int n_sink = min(f, c.sink_cap);                         // accepted sink tokens
   const int n_ring = tot_seg - tot_snk;                          // ring tokens
   const int kept_ring = min(n_ring, c.ring_cap);
@@ -279,29 +302,42 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
   }
   const int n_kept = n_sink + kept_ring;
   if (c0 >= n_kept) return;
-  // second walk: place the kept tokens that fall into this CTA's chunk
+  // second walk: each token's rank and ring index; place the kept tokens
+  // that fall into this CTA's chunk
   {
-    int rank = ex_seg, rsnk = ex_snk;
-    for (int t = t0; t < t1; ++t) {
-      if (sg && sg[t] != seg) continue;
-      const bool is_sink = sk && sk[t];
-      int kept = -1, slot = 0;
-      if (rank < n_sink) {
-        kept = rank;
-        slot = rank;
-      } else if (!is_sink) {
-        const int i = rank - rsnk;  // ring index of this token
-        if (i >= i0) {
-          kept = n_sink + i - i0;
-          slot = c.sink_cap + i % c.ring_cap;
+    int carry_seg = 0, carry_snk = 0;
+    for (int base = 0; base < p.T; base += kPass) {
+      bool in[kPer], snk[kPer];
+      load_flags(base, in, snk);
+      int a = 0, s = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) a += in[j], s += snk[j];
+      int ea, es, ta, ts;
+      block_scan(a, s, ea, es, ta, ts);
+      int rank = carry_seg + ea, rsnk = carry_snk + es;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        if (!in[j]) continue;
+        int kept = -1, slot = 0;
+        if (rank < n_sink) {
+          kept = rank;
+          slot = rank;
+        } else if (!snk[j]) {
+          const int i = rank - rsnk;  // ring index of this token
+          if (i >= i0) {
+            kept = n_sink + i - i0;
+            slot = c.sink_cap + i % c.ring_cap;
+          }
         }
+        if (kept >= c0 && kept < c0 + kFillTokens) {
+          s_src[kept - c0] = base + kPer * tid + j;
+          s_slot[kept - c0] = slot;
+        }
+        rank += 1;
+        rsnk += snk[j];
       }
-      if (kept >= c0 && kept < c0 + kFillTokens) {
-        s_src[kept - c0] = t;
-        s_slot[kept - c0] = slot;
-      }
-      rank += 1;
-      rsnk += is_sink;
+      carry_seg += ta;
+      carry_snk += ts;
     }
   }
   __syncthreads();

@@ -640,6 +640,38 @@ int nd_swa_sink_chunk_prefill(const void *q, const void *k, const void *v, int c
   return finish(e);
 }
 
+int nd_swa_sink_chunk_prefill_tiles(const void *workspace, int batch, int chunk, int n_q_heads, int n_kv_heads,
+                                    int head_dim, int sink_cap, int ring_cap, int window, long long *tiles_out) {
+  if (!tiles_out || batch < 0 || chunk < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || sink_cap < 0 ||
+      ring_cap <= 0 || window < 1 || n_q_heads % n_kv_heads || (head_dim != 64 && head_dim != 128))
+    return ND_ERR_INVALID_ARG;
+  *tiles_out = 0;
+  if (size_t(batch) * chunk == 0) return ND_OK;
+  if (!workspace || !aligned16(workspace)) return ND_ERR_WORKSPACE;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  const ChunkLayout L = chunk_layout(batch, chunk, n_kv_heads, head_dim, sink_cap, ring_cap, window);
+  PrefillArgs a = {};
+  a.dtype = ND_BF16;
+  a.batch = batch;
+  a.T = L.Tk;
+  a.Hq = n_q_heads;
+  a.Hkv = n_kv_heads;
+  a.d = head_dim;
+  a.q_off = sink_cap + L.R;
+  long long n = 0;
+  cudaError_t e = prefill_tile_count(a, static_cast<const char *>(workspace) + L.plan, &n);
+  if (e != cudaSuccess) return fail_cuda(e);
+  *tiles_out = n;
+  return ND_OK;
+}
+
+int nd_set_prefill_epilogue_wait_limit(unsigned polls) {
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  return finish(set_epilogue_wait_limit(polls));
+}
+
 int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                   float rope_theta, nd_stream_t stream) {
   if (batch < 0 || T < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2) return ND_ERR_INVALID_ARG;

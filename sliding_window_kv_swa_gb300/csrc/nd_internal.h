@@ -146,6 +146,9 @@ cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 // launch: it waits for the kernel before it, which may be the rotation pass).
 cudaError_t launch_prefill_tc_prep(const PrefillArgs &a, void *plan_ws, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream);
+// Poll limit of the tensor-core prefill epilogue's wait for a block's last
+// PV on the current device (0 = the default bound); synchronous.
+cudaError_t set_epilogue_wait_limit(unsigned polls);
 // Products of a 128-row block with a 64-key tile that the attention kernel
 // performs for the plan in plan_ws (synchronous read of the plan's counts).
 cudaError_t prefill_tile_count(const PrefillArgs &a, const void *plan_ws, long long *tiles);

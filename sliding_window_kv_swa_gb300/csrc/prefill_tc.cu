@@ -397,6 +397,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *e
   return __all_sync(0xffffffffu, ok);
 }
 
+// Failure-path test mode (nd.h: nd_set_prefill_epilogue_wait_limit): with
+// a limit set, the epilogue's wait for a block's last PV -- a wait that
+// guards no copy in flight -- is replaced by `limit` non-blocking polls of a
+// barrier nothing arrives on, so it runs out on every CTA and the kernel
+// takes its abort path.  0 (the default): the ordinary bounded wait.
+__device__ unsigned g_epi_wait_limit = 0;
+
+__device__ __forceinline__ bool warp_wait_never(uint64_t *never, int *err, volatile int *abort_flag,
+                                                uint32_t limit) {
+  bool ok = false;
+  for (uint32_t i = 0; i < limit && !ok; ++i) ok = mbar_test_wait(never, 0);
+  if (!ok && !*abort_flag) {
+    raise_device_error(err, ND_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // The same for the loader's waits at d = 64: try_wait with a suspend-time
 // hint, so the waiting loader sleeps instead of re-polling and leaves issue
 // slots to the softmax warps on its SM sub-partition (measured: 2% off the
@@ -506,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(128) uint8_t s_stage[4][32 * 64];  // epilogue staging, one block per warp
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ __align__(8) uint64_t s_never;  // failure-path test mode only: nothing arrives on it
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int *abort_flag = &s_abort;
@@ -574,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&epi_empty[r], BM);  // the epilogue threads have taken it
     }
     s_abort = 0;
+    mbar_init(&s_never, 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma0) {
@@ -770,6 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qd = warp & 3;
     const int r = qd * 32 + lane;
     const uint32_t lane_base = uint32_t(qd * 32) << 16;
+    const uint32_t o_test_limit = g_epi_wait_limit;
     const uint32_t stage = smem_u32(&s_stage[qd][0]);
     bool ok = true;
     int gt = 0;
@@ -842,7 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n > 0) {
           // PV(gl) landing implies every earlier MMA of the block has
           const int gl = gt + n - 1;
-          ok = warp_wait(&pv_done[rb][gl % NS], (gl / NS) & 1, p.err, abort_flag);
+          ok = o_test_limit ? warp_wait_never(&s_never, p.err, abort_flag, o_test_limit)
+                            : warp_wait(&pv_done[rb][gl % NS], (gl / NS) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
         }
@@ -1269,6 +1291,10 @@ cudaError_t prefill_tile_count(const PrefillArgs &a, const void *plan_ws, long l
   for (size_t i = 0; i < rows; ++i) total += n[i];
   *tiles = total * (S.p.pair_heads ? a.Hq : 2LL * a.Hq);
   return cudaSuccess;
+}
+
+cudaError_t set_epilogue_wait_limit(unsigned polls) {
+  return cudaMemcpyToSymbol(g_epi_wait_limit, &polls, sizeof(polls));
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *plan_ws, int *err, cudaStream_t stream) {

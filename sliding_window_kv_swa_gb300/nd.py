@@ -70,6 +70,7 @@ def _lib():
             "nd_status_string": (ctypes.c_char_p, [I]),
             "nd_last_cuda_error": (I, []),
             "nd_device_errors": (I, [P, I]),
+            "nd_set_prefill_epilogue_wait_limit": (I, [ctypes.c_uint]),
             "nd_kv_append_quant": (I, [P, P, P, I, P]),
             "nd_kv_quant_rows": (I, [P, L, I, P, P, P]),
             "nd_kv_cache_from_prefill": (I, [P, P, P, I, I, P, P, P, P, P]),
@@ -87,6 +88,7 @@ def _lib():
             "nd_swa_sink_prefill_tiles": (I, [P, I, I, I, I, I, F, I, P]),
             "nd_swa_sink_chunk_prefill_workspace_size": (S, [I, I, I, I, I, I, I, I]),
             "nd_swa_sink_chunk_prefill": (I, [P, P, P, I, P, I, I, P, P, P, S, P]),
+            "nd_swa_sink_chunk_prefill_tiles": (I, [P, I, I, I, I, I, I, I, I, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
             "nd_kv_compress_pool": (I, [P, P, I, I, I, I, I, F, P, P, P]),
             "nd_kv_budget_window": (I, [P, P, P]),
@@ -105,6 +107,7 @@ def library_path() -> str:
 
 
 EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_errors",
+            "nd_set_prefill_epilogue_wait_limit",
             "nd_kv_append_quant", "nd_kv_quant_rows", "nd_kv_cache_from_prefill", "nd_swa_sink_decode_workspace_size",
             "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_decode_step",
             "nd_swa_sink_decode_step_host_workspace_size", "nd_swa_sink_decode_step_host",
@@ -113,6 +116,7 @@ EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_e
             "nd_swa_sink_prefill_workspace_size",
             "nd_swa_sink_prefill", "nd_swa_sink_prefill_tiles",
             "nd_swa_sink_chunk_prefill_workspace_size", "nd_swa_sink_chunk_prefill",
+            "nd_swa_sink_chunk_prefill_tiles",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
 
 
@@ -231,6 +235,11 @@ def nd_device_errors(clear: bool = True) -> int:
     flags = ctypes.c_int(0)
     _check("nd_device_errors", _lib().nd_device_errors(ctypes.byref(flags), 1 if clear else 0))
     return flags.value
+
+
+def nd_set_prefill_epilogue_wait_limit(polls: int) -> None:
+    """Test hook: poll limit of the bf16 prefill's epilogue wait (0 = default)."""
+    _check("nd_set_prefill_epilogue_wait_limit", _lib().nd_set_prefill_epilogue_wait_limit(int(polls)))
 
 
 def nd_kv_append_quant(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -464,6 +473,15 @@ def nd_swa_sink_chunk_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         _ptr(q), _ptr(k), _ptr(v), Tc, ctypes.byref(s), Hq, int(window), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return out
+
+
+def nd_swa_sink_chunk_prefill_tiles(workspace: torch.Tensor, batch: int, chunk: int, n_q_heads: int,
+                                    n_kv_heads: int, head_dim: int, sink_cap: int, ring_cap: int,
+                                    window: int) -> int:
+    n = ctypes.c_longlong(0)
+    _check("nd_swa_sink_chunk_prefill_tiles", _lib().nd_swa_sink_chunk_prefill_tiles(
+        _ptr(workspace), batch, chunk, n_q_heads, n_kv_heads, head_dim, sink_cap, ring_cap, window, ctypes.byref(n)))
+    return n.value
 
 
 def nd_rope_apply(x: torch.Tensor, y: Optional[torch.Tensor] = None, rope_theta: float = 10000.0,
