@@ -563,12 +563,12 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None, b
     nbytes = nd.nd_swa_sink_prefill_workspace_size(nd.ND_BF16, B, T, H, H, d, w["rope_theta"], block)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
 
-    def step(i):
-        nd.nd_kv_compress_pool(k, v, block, w["rope_theta"], pooled_k=pkk, pooled_v=pvv)
-        nd.nd_swa_sink_prefill(q, k, v, None, None, w["window"], rope_theta=w["rope_theta"], pooled_k=pkk,
-                               pooled_v=pvv, block=block, out=out, workspace=ws)
+    def step(i):   # one call: pooling fused with K's rotation, then the attention
+        nd.nd_swa_sink_prefill(q, k, v, None, None, w["window"], rope_theta=w["rope_theta"], block=block, out=out,
+                               workspace=ws)
 
     ms = time_graph(torch, step, steps, warmup, dist)
+    nd.nd_kv_compress_pool(k, v, block, w["rope_theta"], pooled_k=pkk, pooled_v=pvv)
     qr, kr = torch.empty_like(q), torch.empty_like(k)
     nd.nd_rope_apply(q, qr, w["rope_theta"])
     nd.nd_rope_apply(k, kr, w["rope_theta"])
@@ -591,7 +591,8 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None, b
             oracle_row = oracle_prefill_sample("compressed", w, 2, 2, cpu_budget)
         except Exception as ex:  # the product path never depends on it
             oracle_row = {"tok_s": None, "sample": f"unavailable: {ex}"}
-    return dict(config=f"compressed prefill B{B} T{T} H{H} d{d} W256 b{block} RoPE (pooling + rotation + attention)",
+    return dict(config=f"compressed prefill B{B} T{T} H{H} d{d} W256 b{block} RoPE, one call (pooling fused with "
+                       f"K's rotation, then attention)",
                 oracle=oracle_row, ms_per_step=t, tok_s=B * T / (t * 1e-3), step_tflops=flops / (t * 1e-3) / 1e12,
                 visible_pairs=pairs, attn_ms=ta,
                 attn_algorithmic=roofline("tensor", flops, ta, pk["bf16"], "TFLOP/s",
@@ -600,7 +601,7 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None, b
                 roofline=roofline("tensor", tile_flops, ta, pk["bf16"], "TFLOP/s",
                                   "prefill_tc_kernel (tiles its plan performed)", pk["src"],
                                   load_traffic(f"prefill_tc@compressed_b{block}")),
-                launches=5 * steps)
+                launches=4 * steps)
 
 
 def bench_tiny_fp32(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None):
@@ -689,6 +690,40 @@ def bench_pool(torch, nd, steps, warmup, pk, dist=None, block=4, cpu_budget=None
                                   load_traffic(f"pool@compressed_b{block}")))
 
 
+def bench_pool_rope(torch, nd, steps, warmup, pk, dist=None, block=4):
+    """The compressed prefill's fused pass over K and V alone
+    (nd_kv_compress_pool_rope: angle table, then K rotated at every position
+    and the pooled blocks), rotating replicas of the inputs."""
+    from workloads import compressed
+    w = compressed()
+    B, T, H, d = w["k"].shape
+    nb = T // block
+    per = 2 * B * T * H * d * 2 + B * T * H * d * 2 + 2 * B * nb * H * d * 2
+    replicas = max(1, math.ceil(4 * L2_BYTES / per))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    reps = []
+    for _ in range(replicas):
+        k = torch.randn((B, T, H, d), generator=g, device="cuda").to(torch.bfloat16)
+        v = torch.randn((B, T, H, d), generator=g, device="cuda").to(torch.bfloat16)
+        reps.append((k, v, torch.empty_like(k), torch.empty((B, nb, H, d), dtype=torch.bfloat16, device="cuda"),
+                     torch.empty((B, nb, H, d), dtype=torch.bfloat16, device="cuda")))
+    ws = torch.empty(nd.nd_kv_compress_pool_rope_workspace_size(T, d, w["rope_theta"]), dtype=torch.uint8,
+                     device="cuda")
+
+    def step(i):
+        k, v, kr, pkk, pvv = reps[i % replicas]
+        nd.nd_kv_compress_pool_rope(k, v, block, w["rope_theta"], k_rot=kr, pooled_k=pkk, pooled_v=pvv, workspace=ws)
+
+    ms = time_graph(torch, step, steps, warmup, dist)
+    t = ms / steps
+    return dict(config=f"pooling fused with K's rotation, B{B} T{T} H{H} d{d} b{block}: read K and V once, write "
+                       f"rotated K and the pooled blocks (+ the 0.5 MB angle table)",
+                ms_per_step=t, bytes_per_launch=per, replicas=replicas,
+                roofline=roofline("hbm", per, t, pk["hbm"], "GB/s", "rope_table_kernel + pool_rope_kernel", pk["src"],
+                                  load_traffic(f"pool_rope@compressed_b{block}")))
+
+
 def bench_append(torch, nd, steps, warmup, pk, dist=None, B=512, Hkv=8, d=128, S=1024, W=256):
     """Standalone quantise-and-append of one token per sequence into the
     large-batch cache (new tokens rotate through buffers larger than L2)."""
@@ -748,17 +783,19 @@ def bench_fill(torch, nd, steps, warmup, pk, dist=None, S=512, W=256):
     kvs = [(k0, v0)] + [(k0.roll(r, 1).contiguous(), v0.roll(r, 1).contiguous()) for r in range(1, replicas)]
     caches = [nd.KVCache.empty(n, Hkv, d, S, W) for _ in range(replicas)]
     seg_d, sink_d = torch.from_numpy(seg).cuda(), torch.from_numpy(sink).cuda()
+    ws = torch.empty(nd.nd_kv_cache_from_prefill_workspace_size(n, S, W), dtype=torch.uint8, device="cuda")
 
     def step(i):
         k, v = kvs[i % replicas]
-        nd.nd_kv_cache_from_prefill(caches[i % replicas], k, v, src_row, seg_d, sink_d, src_seg)
+        nd.nd_kv_cache_from_prefill(caches[i % replicas], k, v, src_row, seg_d, sink_d, src_seg, workspace=ws)
 
     ms = time_graph(torch, step, steps, warmup, dist)
     t = ms / steps
     return dict(config=f"prefill->cache handoff of the packed workload (B{B} T{T} Hkv{Hkv} d{d}, {n} segments) "
                        f"into {S} sink + {W} ring slots per segment", ms_per_launch=t, kept_tokens=kept,
                 bytes_per_launch=per, replicas=replicas,
-                roofline=roofline("hbm", per, t, pk["hbm"], "GB/s", "kv_fill_kernel", pk["src"]))
+                roofline=roofline("hbm", per, t, pk["hbm"], "GB/s", "kv_fill_plan_kernel + kv_fill_kernel",
+                                  pk["src"]))
 
 
 # ----------------------------------------------------------------------------
@@ -820,8 +857,8 @@ def oracle_decode_sample(B, Hq, Hkv, d, S, W, seed, budget_s, of_batch=None):
 
 HEAD = dict(B=512, Hq=32, Hkv=8, d=128, S=1024, W=256)
 ORACLE_SAMPLE = 32   # sequences of the headline workload the oracle decodes per step
-ALL_ROWS = ("step_b64", "sweep", "wsweep", "packed", "compressed", "compressed_b8", "tiny", "pool", "append",
-            "fill", "cdecode", "chunk")
+ALL_ROWS = ("step_b64", "sweep", "wsweep", "packed", "compressed", "compressed_b8", "tiny", "pool", "pool_rope",
+            "append", "fill", "cdecode", "chunk")
 
 
 def main():
@@ -943,6 +980,9 @@ def main():
                                                     cpu_budget=None if budget is None else 1.0)
     if "pool" in want:
         rows["pool"] = bench_pool(torch, nd, row_steps, warmup, pk, dist, cpu_budget=None if budget is None else 1.0)
+        torch.cuda.empty_cache()
+    if "pool_rope" in want:
+        rows["pool_rope"] = bench_pool_rope(torch, nd, row_steps, warmup, pk, dist)
         torch.cuda.empty_cache()
     if "append" in want:
         rows["append"] = bench_append(torch, nd, max(20, steps // 4), warmup, pk, dist)

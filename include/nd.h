@@ -186,12 +186,17 @@ ND_API int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim,
  *            when seg_ids is.  src_row[e] < 0 leaves cache row e untouched;
  *            src_row[e] >= batch or src_seg[e] <= 0 (padding) sets device
  *            error flag 2 and leaves it untouched.
- * Requires ring_cap > 0; head_dim 32, 64, 128 or 256.
+ * Requires ring_cap > 0; head_dim 32, 64, 128 or 256.  The kept tokens'
+ * plan lives in `workspace` (device, 16-byte aligned) of
+ * nd_kv_cache_from_prefill_workspace_size(cache->batch, sink_cap, ring_cap)
+ * bytes, else ND_ERR_WORKSPACE.
  */
+ND_API size_t nd_kv_cache_from_prefill_workspace_size(int cache_batch, int sink_cap, int ring_cap);
 ND_API int nd_kv_cache_from_prefill(const nd_kv_cache *cache, const void *k, const void *v,
                                     int batch, int T, const int32_t *seg_ids,
                                     const uint8_t *sink, const int32_t *src_row,
-                                    const int32_t *src_seg, nd_stream_t stream);
+                                    const int32_t *src_seg, void *workspace,
+                                    size_t workspace_bytes, nd_stream_t stream);
 
 /*
  * One decode step ([N1] "256-token 滑动窗口：源码走读"): each sequence's query
@@ -416,6 +421,9 @@ ND_API int nd_compressed_decode_step(const void *q, const nd_compressed_cache *c
  * one softmax over the columns [pooled blocks j visible iff
  * (j+1)*block <= t - window + 1, exact keys k <= t with t - k < window].  The
  * compressed variant requires seg_ids == NULL, sink == NULL and window >= 1.
+ * pooled_k and pooled_v may both be NULL: the call then pools K and V itself
+ * (exactly as nd_kv_compress_pool, into its workspace) in one pass over K
+ * and V that also rotates K (nd_kv_compress_pool_rope).
  *
  * dtype ND_F32 runs on CUDA cores in fp32; ND_BF16 runs on the tensor cores
  * (bf16 operands, fp32 accumulation).  head_dim 64 or 128.
@@ -504,6 +512,23 @@ ND_API int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads,
 ND_API int nd_kv_compress_pool(const void *k, const void *v, int batch, int T,
                         int n_heads, int head_dim, int block, float rope_theta,
                         void *pooled_k, void *pooled_v, nd_stream_t stream);
+
+/*
+ * Block pooling and K's rotation in one pass over K and V, as the compressed
+ * prefill needs them ([C3] "Pool before rotating, not after"): writes
+ *   k_rot               bf16 [batch][T][n_heads][head_dim]: k rotated at its
+ *                       position (exactly as nd_rope_apply); not written and
+ *                       may be NULL when rope_theta == 0
+ *   pooled_k, pooled_v  exactly as nd_kv_compress_pool
+ * The (cos, sin) table of positions 0..T-1 is built in `workspace` (device,
+ * 16-byte aligned) of nd_kv_compress_pool_rope_workspace_size() bytes (0
+ * when rope_theta == 0).  head_dim a multiple of 16, at most 256.
+ */
+ND_API size_t nd_kv_compress_pool_rope_workspace_size(int T, int head_dim, float rope_theta);
+ND_API int nd_kv_compress_pool_rope(const void *k, const void *v, int batch, int T, int n_heads,
+                                    int head_dim, int block, float rope_theta, void *k_rot,
+                                    void *pooled_k, void *pooled_v, void *workspace,
+                                    size_t workspace_bytes, nd_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* KV budget window (host only)                                              */

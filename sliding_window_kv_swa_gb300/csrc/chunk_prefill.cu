@@ -38,11 +38,10 @@ struct GatherParams {
   int *err;
 };
 
-// grid (row blocks of 8 key rows, B); a warp per (key row, head) writes D
-// bf16 values: lane l handles channels [l*D/32, +D/32).
+// grid (row blocks of 8 key rows, B); each warp writes 256/D (key row, head,
+// K or V) rows per step, a lane 8 channels of one row.
 template <int D>
 __global__ void __launch_bounds__(256) chunk_gather_kernel(const GatherParams p) {
-  constexpr int CPL = D / 32;
   const nd_kv_cache &c = p.c;
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = c.sink_cap, Tk = S + p.R + p.Tc, Hkv = c.n_kv_heads, nslot = c.sink_cap + c.ring_cap;
@@ -73,40 +72,72 @@ __global__ void __launch_bounds__(256) chunk_gather_kernel(const GatherParams p)
     p.seg[size_t(b) * Tk + i] = sg;
     p.sink[size_t(b) * Tk + i] = uint8_t(sk);
   }
-  for (int item = warp; item < 8 * Hkv * 2; item += 8) {
-    const int i = row0 + item / (2 * Hkv), h = (item >> 1) % Hkv;
-    const bool is_v = item & 1;
-    if (i >= Tk) continue;
-    uint16_t *dst = (is_v ? p.vv : p.kk) + ((size_t(b) * Tk + i) * Hkv + h) * D + lane * CPL;
-    int slot = -1;
-    if (i < S) {
-      if (sane && i < sl) slot = i;
-    } else if (i < S + p.R) {
-      const int r = S + p.R - i;
-      if (sane && r <= rl) slot = S + (rs + rl - r) % c.ring_cap;
-    } else {
-      const uint16_t *src = (is_v ? p.v : p.k) + ((size_t(b) * p.Tc + (i - S - p.R)) * Hkv + h) * D + lane * CPL;
-      if constexpr (CPL == 4) *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(src);
-      else *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
-      continue;
-    }
-    float x[CPL];
-    if (slot >= 0) {
-      const size_t row = (size_t(b) * Hkv + h) * nslot + slot;
-      const int8_t *codes = (is_v ? c.v_codes : c.k_codes) + row * D + lane * CPL;
-      const float scale = (is_v ? c.v_scale : c.k_scale)[row * (D / 32) + lane * CPL / 32];
+  // rows of this block: (key row i, head h, K or V); a lane moves 8
+  // channels (16 bytes of bf16), RPI rows per warp-iteration, kU
+  // iterations' loads in flight before any is converted
+  constexpr int RPI = 256 / D, kU = 4, kLanesPerRow = D / 8;
+  const int sub = lane / kLanesPerRow, ch = (lane % kLanesPerRow) * 8;
+  const int n_rows = 8 * Hkv * 2;
+  for (int r0 = warp * RPI * kU; r0 < n_rows; r0 += 8 * RPI * kU) {
+    int kind[kU];  // 0: zeros, 1: cached codes, 2: chunk copy, -1: past the end
+    uint2 cw[kU];
+    float sc[kU];
+    uint4 cv[kU];
+    size_t dst[kU];
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) x[e] = float(codes[e]) * scale;
-    } else {
-#pragma unroll
-      for (int e = 0; e < CPL; ++e) x[e] = 0.f;
+    for (int u = 0; u < kU; ++u) {
+      const int r = r0 + u * RPI + sub;
+      const int i = row0 + r / (2 * Hkv), h = (r >> 1) % Hkv;
+      const bool is_v = r & 1;
+      kind[u] = -1;
+      if (r >= n_rows || i >= Tk) continue;
+      dst[u] = ((size_t(b) * Tk + i) * Hkv + h) * D + ch;
+      int slot = -1;
+      if (i < S) {
+        if (sane && i < sl) slot = i;
+      } else if (i < S + p.R) {
+        const int rr = S + p.R - i;
+        if (sane && rr <= rl) slot = S + (rs + rl - rr) % c.ring_cap;
+      } else {
+        kind[u] = 2;
+        cv[u] = *reinterpret_cast<const uint4 *>((is_v ? p.v : p.k) +
+                                                 ((size_t(b) * p.Tc + (i - S - p.R)) * Hkv + h) * D + ch);
+        continue;
+      }
+      kind[u] = slot >= 0 ? 1 : 0;
+      if (slot >= 0) {
+        const size_t row = (size_t(b) * Hkv + h) * nslot + slot;
+        cw[u] = *reinterpret_cast<const uint2 *>((is_v ? c.v_codes : c.k_codes) + row * D + ch);
+        sc[u] = (is_v ? c.v_scale : c.k_scale)[row * (D / 32) + ch / 32];
+      }
     }
-    if constexpr (CPL == 4)
-      *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-    else
-      *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(x[0], x[1]);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int r = r0 + u * RPI + sub;
+      if (kind[u] < 0) continue;
+      uint16_t *out = ((r & 1) ? p.vv : p.kk) + dst[u];
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (kind[u] == 2) {
+        o = cv[u];
+      } else if (kind[u] == 1) {
+        const uint32_t w2[2] = {cw[u].x, cw[u].y};
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t wd = w2[q / 2];
+          const int sh = (q & 1) * 16;
+          const float lo = float(int8_t((wd >> sh) & 0xffu)) * sc[u];
+          const float hi = float(int8_t((wd >> (sh + 8)) & 0xffu)) * sc[u];
+          pk[q] = pack_bf16x2(lo, hi);
+        }
+        o = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      *reinterpret_cast<uint4 *>(out) = o;
+    }
   }
 }
+
+constexpr int kAppendTokens = 2;  // chunk tokens per append CTA
 
 struct AppendParams {
   nd_kv_cache c;
@@ -115,7 +146,7 @@ struct AppendParams {
   const int32_t *meta;    // the snapshot taken before the chunk
 };
 
-// grid (chunks of 8 tokens of the newest min(Tc, ring_cap), B): a warp per
+// grid (pairs of tokens of the newest min(Tc, ring_cap), B): a warp per
 // (token, head, K or V) quantises one row into its ring slot; block 0 of a
 // sequence then advances its metadata (from the snapshot, so no block reads
 // metadata another one has written).
@@ -129,8 +160,8 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const AppendParams p)
   const int rs = p.meta[4 * b + 1], rl = p.meta[4 * b + 2], sq = p.meta[4 * b + 3];
   if (sq < 0) return;
   const int first = p.Tc > cap ? p.Tc - cap : 0;  // older chunk tokens are overwritten within the chunk
-  const int t0 = first + blockIdx.x * 8;
-  for (int item = warp; item < 8 * Hkv * 2; item += 8) {
+  const int t0 = first + blockIdx.x * kAppendTokens;
+  for (int item = warp; item < kAppendTokens * Hkv * 2; item += blockDim.x >> 5) {
     const int t = t0 + item / (2 * Hkv), h = (item >> 1) % Hkv;
     const bool is_v = item & 1;
     if (t >= p.Tc) continue;
@@ -197,7 +228,7 @@ cudaError_t launch_chunk_append(const nd_kv_cache &c, const void *k, const void 
   p.Tc = Tc;
   p.meta = meta;
   const int n = Tc < c.ring_cap ? Tc : c.ring_cap;
-  const dim3 grid((n + 7) / 8, c.batch);
+  const dim3 grid((n + kAppendTokens - 1) / kAppendTokens, c.batch);
   if (c.head_dim == 64) return launch_pdl(chunk_append_kernel<64>, grid, dim3(256), 0, stream, p);
   if (c.head_dim == 128) return launch_pdl(chunk_append_kernel<128>, grid, dim3(256), 0, stream, p);
   return cudaErrorInvalidValue;

@@ -101,10 +101,11 @@ __device__ __forceinline__ void quant_row_regs(uint2 w, int lane, int *code, flo
 #pragma unroll
   for (int off = kLanesPerGroup / 2; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   scale = __fdiv_rn(amax, 127.0f);
+  const float inv = __frcp_rn(scale);
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     float r = 0.f;
-    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    if (amax != 0.f) r = fminf(fmaxf(codec_rint(x[i], scale, inv), -127.f), 127.f);
     code[i] = int(r);
   }
 }

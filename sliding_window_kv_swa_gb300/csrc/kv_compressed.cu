@@ -50,7 +50,7 @@ struct CompressedParams {
 
 // One CTA per sequence; warp items: (KV head, K or V) rows, then q heads.
 template <int D>
-__global__ void __launch_bounds__(256) compressed_append_kernel(const CompressedParams p) {
+__global__ void __launch_bounds__(512) compressed_append_kernel(const CompressedParams p) {
   constexpr int CPL = D / 32;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -59,6 +59,9 @@ __global__ void __launch_bounds__(256) compressed_append_kernel(const Compressed
   //         3 new ring_start, 4 new ring_len, 5 new sink_len, 6 block
   //         flags (bit 0: first token of its block, bit 1: closes it)
   __shared__ int s_meta[8];
+  // (cos, sin) at the token's position and at its block's midpoint, built
+  // once per CTA (the double-precision reduction is off every row's chain)
+  __shared__ float2 s_cs[2][D / 2];
   pdl_wait();
   if (threadIdx.x == 0) {
     const int sl = c.sink_len[b], rs = c.ring_start[b], rl = c.ring_len[b], pos = c.seq_len[b];
@@ -102,19 +105,23 @@ __global__ void __launch_bounds__(256) compressed_append_kernel(const Compressed
   const int pos = s_meta[0], exact = s_meta[1], pooled = s_meta[2], mode = s_meta[6];
   if (exact < 0) return;
   const bool pinned = pos < p.n_pinned;
+  const int mid = pinned ? 0 : p.n_pinned + ((pos - p.n_pinned) / p.block) * p.block + p.block / 2;
+  for (int i = threadIdx.x; i < D; i += blockDim.x)
+    s_cs[i / (D / 2)][i % (D / 2)] = rot_cs(double(i < D / 2 ? pos : mid), p.fr.f[i % (D / 2)]);
+  __syncthreads();
   const int Hkv = c.n_kv_heads, nslot = c.sink_cap + c.ring_cap;
   // this lane's channel pairs: lanes 0-15 hold x_i, lanes 16-31 the partner
   // x_{i + D/2} of the same pairs (lane ^ 16)
   const int c0 = lane * CPL;
   const int i0 = c0 % (D / 2);
   const bool hi = lane >= 16;
-  auto rotate = [&](float *x, double at) {
+  auto rotate = [&](float *x, int which) {  // which: 0 at the position, 1 at the block midpoint
     float partner[CPL];
 #pragma unroll
     for (int e = 0; e < CPL; ++e) partner[e] = __shfl_xor_sync(0xffffffffu, x[e], 16);
 #pragma unroll
     for (int e = 0; e < CPL; ++e) {
-      const float2 cs = rot_cs(at, p.fr.f[i0 + e]);
+      const float2 cs = s_cs[which][i0 + e];
       float ya, yb;
       if (hi) {
         rope_pair(partner[e], x[e], cs.x, cs.y, ya, yb);
@@ -151,7 +158,7 @@ __global__ void __launch_bounds__(256) compressed_append_kernel(const Compressed
       const size_t off = (size_t(b) * p.Hq + h) * D;
       float x[CPL];
       load(p.q + off, x);
-      rotate(x, double(pos));
+      rotate(x, 0);
       if constexpr (CPL == 4)
         reinterpret_cast<uint2 *>(p.q_rot + off)[lane] = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
       else
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(256) compressed_append_kernel(const Compressed
     for (int e = 0; e < CPL; ++e) raw[e] = x[e];
     // the exact key (rotated at pos, rounded to bf16) or value
     if (!is_v) {
-      rotate(x, double(pos));
+      rotate(x, 0);
 #pragma unroll
       for (int e = 0; e < CPL; ++e) x[e] = round_bf16(x[e]);
     }
@@ -188,10 +195,7 @@ __global__ void __launch_bounds__(256) compressed_append_kernel(const Compressed
     const float fb = float(p.block);
 #pragma unroll
     for (int e = 0; e < CPL; ++e) acc[e] = __fdiv_rn(acc[e], fb);
-    if (!is_v) {
-      const int j = (pos - p.n_pinned) / p.block;
-      rotate(acc, double(p.n_pinned + j * p.block + p.block / 2));
-    }
+    if (!is_v) rotate(acc, 1);
 #pragma unroll
     for (int e = 0; e < CPL; ++e) acc[e] = round_bf16(acc[e]);
     if (pooled >= 0)
@@ -230,7 +234,7 @@ cudaError_t launch_compressed_append(const nd_kv_cache &c, float *k_sum, float *
   p.fr = make_freqs(c.head_dim, theta);
   if (theta == 0.f)  // no rotation: every angle 0 (cos 1, sin 0: rope_pair is exact)
     for (int i = 0; i < kMaxHalf; ++i) p.fr.f[i] = 0.0;
-  const dim3 grid(c.batch), blk(256);
+  const dim3 grid(c.batch), blk(512);
   if (c.head_dim == 64) return launch_pdl(compressed_append_kernel<64>, grid, blk, 0, stream, p);
   if (c.head_dim == 128) return launch_pdl(compressed_append_kernel<128>, grid, blk, 0, stream, p);
   return cudaErrorInvalidValue;

@@ -91,12 +91,12 @@ __device__ __forceinline__ void quant_row(const uint16_t *src, int8_t *codes, fl
 #pragma unroll
   for (int off = kLanesPerGroup / 2; off >= 1; off >>= 1)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float scale = __fdiv_rn(amax, 127.0f);
+  const float scale = __fdiv_rn(amax, 127.0f), inv = __frcp_rn(scale);
   int c[CPL];
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     float r = 0.f;
-    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    if (amax != 0.f) r = fminf(fmaxf(codec_rint(x[i], scale, inv), -127.f), 127.f);
     c[i] = int(r);
   }
   RowIO<CPL>::store(codes, lane, c);
@@ -183,11 +183,12 @@ __device__ __forceinline__ uint2 quant8(const uint4 w, float &scale) {
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   scale = __fdiv_rn(amax, 127.0f);
+  const float inv = __frcp_rn(scale);
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     float r = 0.f;
-    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    if (amax != 0.f) r = fminf(fmaxf(codec_rint(x[i], scale, inv), -127.f), 127.f);
     const uint32_t cb = uint32_t(int(r)) & 0xffu;
     if (i < 4) lo |= cb << (8 * i);
     else hi |= cb << (8 * (i - 4));
@@ -195,8 +196,9 @@ __device__ __forceinline__ uint2 quant8(const uint4 w, float &scale) {
   return make_uint2(lo, hi);
 }
 
-constexpr int kFillTokens = 16;   // kept tokens per CTA
+constexpr int kFillTokens = 16;     // kept tokens per quantising CTA
 constexpr int kFillThreads = 256;
+constexpr int kPlanThreads = 1024;  // one planning CTA per cache row
 
 struct FillParams {
   nd_kv_cache c;
@@ -205,41 +207,38 @@ struct FillParams {
   const int32_t *seg_ids;  // may be NULL
   const uint8_t *sink;     // may be NULL
   const int32_t *src_row, *src_seg;
+  int32_t *plan;  // per cache row: [0] kept tokens (-1: row untouched), then (position, slot) pairs
+  int plan_stride;
   int *err;
 };
 
-// Cache row e = blockIdx.y takes the tokens of segment src_seg[e] of batch row
-// src_row[e], in position order, under the append rule: while the ring is
-// empty a sink token goes to the next sink slot (rejected once the sink
+// Plan of cache row e (one CTA): the tokens of segment src_seg[e] of batch
+// row src_row[e], in position order, under the append rule -- while the ring
+// is empty a sink token goes to the next sink slot (rejected once the sink
 // region is full); every other token goes to the ring, and once the ring has
-// a token, sink tokens are rejected.  Every CTA ranks the segment's tokens
-// (two block-wide prefix counts over the batch row) and then quantises the
-// kept tokens [16*blockIdx.x, +16) into their slots; CTA 0 of the row writes
-// the metadata.
-template <int D>
-__global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams p) {
-  constexpr int NW = kFillThreads / 32;
+// a token, sink tokens are rejected.  Two walks over the batch row, four
+// positions per thread per pass: totals and the first ring token's rank,
+// then every token's rank; the kept tokens' (position, slot) pairs go to the
+// plan, the row's metadata to the cache.
+__global__ void __launch_bounds__(kPlanThreads) kv_fill_plan_kernel(const FillParams p) {
+  constexpr int NW = kPlanThreads / 32, kPer = 4, kPass = kPer * kPlanThreads;
   __shared__ int s_wsum[NW][2];
   __shared__ int s_first_r;
-  __shared__ int s_src[kFillTokens], s_slot[kFillTokens];
   const nd_kv_cache &c = p.c;
-  const int e = blockIdx.y, c0 = blockIdx.x * kFillTokens;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int e = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int32_t *plan = p.plan + size_t(e) * p.plan_stride;
   pdl_wait();
   const int b = p.src_row[e];
   const int seg = p.seg_ids ? p.src_seg[e] : 1;
-  if (b < 0) return;  // row left untouched
-  if (b >= p.batch || seg <= 0) {
-    if (blockIdx.x == 0 && tid == 0) raise_device_error(p.err, ND_DEVERR_METADATA);
+  if (b < 0 || b >= p.batch || seg <= 0) {  // row left untouched
+    if (tid == 0) {
+      plan[0] = -1;
+      if (b >= 0) raise_device_error(p.err, ND_DEVERR_METADATA);
+    }
     return;
   }
   if (tid == 0) s_first_r = 0x7fffffff;
-  if (tid < kFillTokens) s_src[tid] = -1;
   __syncthreads();
-  // The batch row is walked in passes of 4 * kFillThreads positions: thread
-  // tid takes positions base + 4 tid .. + 3 (four independent loads in
-  // flight), ranks come from a block-wide prefix of the per-thread counts.
-  constexpr int kPer = 4, kPass = kPer * kFillThreads;
   const int32_t *sg = p.seg_ids ? p.seg_ids + size_t(b) * p.T : nullptr;
   const uint8_t *sk = p.sink ? p.sink + size_t(b) * p.T : nullptr;
   auto load_flags = [&](int base, bool *in, bool *snk) {
@@ -261,15 +260,13 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
     if (lane == 31) s_wsum[warp][0] = ia, s_wsum[warp][1] = is;
     __syncthreads();
     ea = ia - a, es = is - s, ta = 0, ts = 0;
-#pragma unroll
+#pragma unroll 8
     for (int w = 0; w < NW; ++w) {
       if (w < warp) ea += s_wsum[w][0], es += s_wsum[w][1];
       ta += s_wsum[w][0], ts += s_wsum[w][1];
     }
     __syncthreads();  // s_wsum is reused by the next call
   };
-  // totals, and the rank of the first ring (non-sink) token: the segment's
-  // tokens before it, all sinks (no ring token: every token of the segment)
   int tot_seg = 0, tot_snk = 0;
   for (int base = 0; base < p.T; base += kPass) {
     bool in[kPer], snk[kPer];
@@ -288,75 +285,96 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
     tot_snk += ts;
   }
   __syncthreads();
+  // the rank of the first ring token = the segment's tokens before it (all
+  // sinks); no ring token: every token of the segment
   const int f = s_first_r == 0x7fffffff ? tot_seg : s_first_r;
-  const int n_sink = min(f, c.sink_cap);                         // accepted sink tokens
-  const int n_ring = tot_seg - tot_snk;                          // ring tokens
+  const int n_sink = min(f, c.sink_cap);  // accepted sink tokens
+  const int n_ring = tot_seg - tot_snk;   // ring tokens
   const int kept_ring = min(n_ring, c.ring_cap);
-  const int i0 = n_ring - kept_ring;                             // oldest ring token kept
-  if (blockIdx.x == 0 && tid == 0) {
+  const int i0 = n_ring - kept_ring;      // oldest ring token kept
+  if (tid == 0) {
     c.sink_len[e] = n_sink;
     c.ring_len[e] = kept_ring;
     c.ring_start[e] = n_ring > c.ring_cap ? n_ring % c.ring_cap : 0;
     c.seq_len[e] = n_sink + n_ring;
+    plan[0] = n_sink + kept_ring;
     if (tot_snk > n_sink) raise_device_error(p.err, ND_DEVERR_METADATA);  // rejected sink tokens
   }
-  const int n_kept = n_sink + kept_ring;
-  if (c0 >= n_kept) return;
-  // second walk: each token's rank and ring index; place the kept tokens
-  // that fall into this CTA's chunk
-  {
-    int carry_seg = 0, carry_snk = 0;
-    for (int base = 0; base < p.T; base += kPass) {
-      bool in[kPer], snk[kPer];
-      load_flags(base, in, snk);
-      int a = 0, s = 0;
+  int carry_seg = 0, carry_snk = 0;
+  for (int base = 0; base < p.T; base += kPass) {
+    bool in[kPer], snk[kPer];
+    load_flags(base, in, snk);
+    int a = 0, s = 0;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) a += in[j], s += snk[j];
-      int ea, es, ta, ts;
-      block_scan(a, s, ea, es, ta, ts);
-      int rank = carry_seg + ea, rsnk = carry_snk + es;
+    for (int j = 0; j < kPer; ++j) a += in[j], s += snk[j];
+    int ea, es, ta, ts;
+    block_scan(a, s, ea, es, ta, ts);
+    int rank = carry_seg + ea, rsnk = carry_snk + es;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        if (!in[j]) continue;
-        int kept = -1, slot = 0;
-        if (rank < n_sink) {
-          kept = rank;
-          slot = rank;
-        } else if (!snk[j]) {
-          const int i = rank - rsnk;  // ring index of this token
-          if (i >= i0) {
-            kept = n_sink + i - i0;
-            slot = c.sink_cap + i % c.ring_cap;
-          }
+    for (int j = 0; j < kPer; ++j) {
+      if (!in[j]) continue;
+      int kept = -1, slot = 0;
+      if (rank < n_sink) {
+        kept = rank;
+        slot = rank;
+      } else if (!snk[j]) {
+        const int i = rank - rsnk;  // ring index of this token
+        if (i >= i0) {
+          kept = n_sink + i - i0;
+          slot = c.sink_cap + i % c.ring_cap;
         }
-        if (kept >= c0 && kept < c0 + kFillTokens) {
-          s_src[kept - c0] = base + kPer * tid + j;
-          s_slot[kept - c0] = slot;
-        }
-        rank += 1;
-        rsnk += snk[j];
       }
-      carry_seg += ta;
-      carry_snk += ts;
+      if (kept >= 0) {
+        plan[1 + 2 * kept] = base + kPer * tid + j;
+        plan[2 + 2 * kept] = slot;
+      }
+      rank += 1;
+      rsnk += snk[j];
     }
+    carry_seg += ta;
+    carry_snk += ts;
+  }
+}
+
+// Quantise kept tokens [16*blockIdx.x, +16) of cache row blockIdx.y from its
+// plan: rows (token, head, K or V), RPI = 256/D rows per warp-iteration, four
+// iterations' loads in flight.
+template <int D>
+__global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams p) {
+  constexpr int NW = kFillThreads / 32;
+  const nd_kv_cache &c = p.c;
+  const int e = blockIdx.y, c0 = blockIdx.x * kFillTokens;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  __shared__ int s_pos[kFillTokens], s_slot[kFillTokens];
+  const int32_t *plan = p.plan + size_t(e) * p.plan_stride;
+  const int n_kept = plan[0];
+  if (c0 >= n_kept) return;  // also the untouched rows (-1)
+  const int b = p.src_row[e];
+  // this CTA's (position, slot) pairs, so no row's load waits on the plan
+  if (threadIdx.x < kFillTokens && c0 + int(threadIdx.x) < n_kept) {
+    s_pos[threadIdx.x] = plan[1 + 2 * (c0 + threadIdx.x)];
+    s_slot[threadIdx.x] = plan[2 + 2 * (c0 + threadIdx.x)];
   }
   __syncthreads();
-  // rows of this chunk: (token j, head h, K or V); RPI rows per warp-iteration
   constexpr int RPI = 256 / D, kUnroll = 4;
   const int n_tok = min(kFillTokens, n_kept - c0), Hkv = c.n_kv_heads;
   const int n_rows = n_tok * Hkv * 2, nslot = c.sink_cap + c.ring_cap;
   const int sub = lane / (D / 8);
   for (int r0 = warp * RPI * kUnroll; r0 < n_rows; r0 += NW * RPI * kUnroll) {
     uint4 w[kUnroll];
-    int rows[kUnroll];
+    int rows[kUnroll], slots[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int r = r0 + u * RPI + sub;
       rows[u] = r;
       w[u] = make_uint4(0, 0, 0, 0);
+      slots[u] = 0;
       if (r < n_rows) {
         const int j = r / (2 * Hkv), h = (r >> 1) % Hkv;
-        const uint16_t *src = ((r & 1) ? p.v : p.k) + ((size_t(b) * p.T + s_src[j]) * Hkv + h) * D;
+        const int t = s_pos[j];
+        slots[u] = s_slot[j];
+        const uint16_t *src = ((r & 1) ? p.v : p.k) + ((size_t(b) * p.T + t) * Hkv + h) * D;
         w[u] = *reinterpret_cast<const uint4 *>(src + (lane % (D / 8)) * 8);
       }
     }
@@ -367,9 +385,9 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
       const uint2 q8 = quant8(w[u], scale);
       const int r = rows[u];
       if (r < n_rows) {
-        const int j = r / (2 * Hkv), h = (r >> 1) % Hkv, ch = (lane % (D / 8)) * 8;
+        const int h = (r >> 1) % Hkv, ch = (lane % (D / 8)) * 8;
         const bool is_v = r & 1;
-        const size_t row = (size_t(e) * Hkv + h) * nslot + s_slot[j];
+        const size_t row = (size_t(e) * Hkv + h) * nslot + slots[u];
         *reinterpret_cast<uint2 *>((is_v ? c.v_codes : c.k_codes) + row * D + ch) = q8;
         if ((lane & 3) == 0) (is_v ? c.v_scale : c.k_scale)[row * (D / 32) + ch / 32] = scale;
       }
@@ -379,9 +397,13 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
 
 }  // namespace
 
+size_t kv_fill_plan_ints(int sink_cap, int ring_cap) {
+  return (size_t(1) + 2 * size_t(sink_cap + ring_cap) + 3) / 4 * 4;  // 16-byte rows
+}
+
 cudaError_t launch_kv_fill(const nd_kv_cache &c, const void *k, const void *v, int batch, int T,
                            const int32_t *seg_ids, const uint8_t *sink, const int32_t *src_row,
-                           const int32_t *src_seg, int *err, cudaStream_t stream) {
+                           const int32_t *src_seg, int32_t *plan, int *err, cudaStream_t stream) {
   FillParams p;
   p.c = c;
   p.k = static_cast<const uint16_t *>(k);
@@ -392,7 +414,11 @@ cudaError_t launch_kv_fill(const nd_kv_cache &c, const void *k, const void *v, i
   p.sink = sink;
   p.src_row = src_row;
   p.src_seg = src_seg;
+  p.plan = plan;
+  p.plan_stride = int(kv_fill_plan_ints(c.sink_cap, c.ring_cap));
   p.err = err;
+  cudaError_t e = launch_pdl(kv_fill_plan_kernel, dim3(c.batch), dim3(kPlanThreads), 0, stream, p);
+  if (e != cudaSuccess) return e;
   const int slots = c.sink_cap + c.ring_cap;
   const dim3 grid((slots + kFillTokens - 1) / kFillTokens, c.batch);
   switch (c.head_dim) {

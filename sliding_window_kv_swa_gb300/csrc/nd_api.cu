@@ -173,9 +173,15 @@ int nd_kv_quant_rows(const void *x, int64_t n_rows, int head_dim, int8_t *codes,
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t nd_kv_cache_from_prefill_workspace_size(int cache_batch, int sink_cap, int ring_cap) {
+  if (cache_batch <= 0 || sink_cap < 0 || ring_cap <= 0) return 0;
+  return round_up(size_t(cache_batch) * kv_fill_plan_ints(sink_cap, ring_cap) * sizeof(int32_t), 256);
+}
+
 int nd_kv_cache_from_prefill(const nd_kv_cache *cache, const void *k, const void *v, int batch, int T,
                              const int32_t *seg_ids, const uint8_t *sink, const int32_t *src_row,
-                             const int32_t *src_seg, nd_stream_t stream) {
+                             const int32_t *src_seg, void *workspace, size_t workspace_bytes,
+                             nd_stream_t stream) {
   int st = validate_cache(cache);
   if (st != ND_OK) return st;
   if (batch < 0 || T < 0) return ND_ERR_INVALID_ARG;
@@ -185,8 +191,11 @@ int nd_kv_cache_from_prefill(const nd_kv_cache *cache, const void *k, const void
   if (cache->batch == 0) return ND_OK;
   if (!src_row || (seg_ids && !src_seg)) return ND_ERR_INVALID_ARG;
   if (size_t(batch) * T > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return ND_ERR_INVALID_ARG;
+  const size_t need = nd_kv_cache_from_prefill_workspace_size(cache->batch, cache->sink_cap, cache->ring_cap);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ND_ERR_WORKSPACE;
   if ((st = check_device(nullptr)) != ND_OK) return st;
-  return finish(launch_kv_fill(*cache, k, v, batch, T, seg_ids, sink, src_row, src_seg, device_error_word(),
+  return finish(launch_kv_fill(*cache, k, v, batch, T, seg_ids, sink, src_row, src_seg,
+                               static_cast<int32_t *>(workspace), device_error_word(),
                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -450,12 +459,20 @@ static size_t prefill_rotation_bytes(nd_dtype dtype, int batch, int T, int n_q_h
   return bytes;
 }
 
+// Pooled K and V the compressed bf16 prefill builds itself (block > 0,
+// pooled_k = pooled_v = NULL), after the plan.
+static size_t prefill_pooled_bytes(int batch, int T, int n_kv_heads, int head_dim, int block) {
+  return block > 0 ? 2 * round_up(size_t(batch) * (T / block) * n_kv_heads * head_dim * 2, 256) : 0;
+}
+
 size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int n_q_heads,
                                           int n_kv_heads, int head_dim, float rope_theta,
                                           int block) {
   if (batch <= 0 || T <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return 0;
   size_t bytes = prefill_rotation_bytes(dtype, batch, T, n_q_heads, n_kv_heads, head_dim, rope_theta);
-  if (dtype == ND_BF16) bytes += round_up(prefill_plan_bytes(batch, T, block), 256);
+  if (dtype == ND_BF16)
+    bytes += round_up(prefill_plan_bytes(batch, T, block), 256) +
+             prefill_pooled_bytes(batch, T, n_kv_heads, head_dim, block);
   return bytes;
 }
 
@@ -499,10 +516,11 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
   if (size_t(batch) * T == 0) return ND_OK;
   if (!q || !k || !v || !out) return ND_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ND_ERR_INVALID_ARG;
+  const bool pool_inside = block > 0 && !pooled_k && !pooled_v;
   if (block > 0) {
     if (dtype != ND_BF16) return ND_ERR_UNSUPPORTED;
     if (seg_ids || sink || window < 1) return ND_ERR_INVALID_ARG;
-    if (!pooled_k || !pooled_v || !aligned16(pooled_k) || !aligned16(pooled_v))
+    if (!pool_inside && (!pooled_k || !pooled_v || !aligned16(pooled_k) || !aligned16(pooled_v)))
       return ND_ERR_INVALID_ARG;
   }
   const size_t need = nd_swa_sink_prefill_workspace_size(dtype, batch, T, n_q_heads, n_kv_heads,
@@ -547,10 +565,25 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
     ws += round_up(rope_table_bytes(T, head_dim), 256);
   }
   // bf16: the tile records and plan go first (an ordinary launch), the
-  // rotation table beside them, then K's rotation and the attention kernel,
-  // each a dependent launch that waits for the kernel before it
+  // rotation table beside them, then K's rotation (fused with the pooling
+  // when the call pools) and the attention kernel, each a dependent launch
+  // that waits for the kernel before it
   cudaError_t e = cudaSuccess;
   if (!f32) e = launch_prefill_tc_prep(a, ws, s);
+  if (e == cudaSuccess && pool_inside) {
+    char *pooled = ws + round_up(prefill_plan_bytes(batch, T, block), 256);
+    const size_t pb = prefill_pooled_bytes(batch, T, n_kv_heads, head_dim, block) / 2;
+    a.pooled_k = pooled;
+    a.pooled_v = pooled + pb;
+    e = launch_pool_rope(k, v, kr, pooled, pooled + pb, batch, T, n_kv_heads, head_dim, block, rope_theta, table,
+                         /*chained=*/true, s);
+    if (table) {
+      a.k = kr;
+      a.rope_cs = table;
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    return finish(launch_prefill_tc(a, ws, device_error_word(), s));
+  }
   if (e == cudaSuccess && table) {
     e = launch_rope_qk(f32 ? q : nullptr, qr, f32 ? n_q_heads : 0, k, kr, n_kv_heads, batch, T, head_dim,
                        rope_theta, f32, table, /*chained=*/!f32, s);
@@ -696,6 +729,31 @@ int nd_kv_compress_pool(const void *k, const void *v, int batch, int T, int n_he
   if (st != ND_OK) return st;
   return finish(launch_compress_pool(k, v, batch, T, n_heads, head_dim, block, rope_theta, pooled_k,
                                      pooled_v, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t nd_kv_compress_pool_rope_workspace_size(int T, int head_dim, float rope_theta) {
+  if (T <= 0 || head_dim <= 0 || rope_theta == 0.f) return 0;
+  return round_up(rope_table_bytes(T, head_dim), 256);
+}
+
+int nd_kv_compress_pool_rope(const void *k, const void *v, int batch, int T, int n_heads, int head_dim, int block,
+                             float rope_theta, void *k_rot, void *pooled_k, void *pooled_v, void *workspace,
+                             size_t workspace_bytes, nd_stream_t stream) {
+  if (batch < 0 || T < 0 || n_heads <= 0 || block <= 0) return ND_ERR_INVALID_ARG;
+  if (head_dim <= 0 || head_dim % 16 || head_dim > 256)
+    return head_dim > 0 && head_dim % 2 == 0 ? ND_ERR_UNSUPPORTED : ND_ERR_INVALID_ARG;
+  if (size_t(batch) * T == 0) return ND_OK;
+  const bool blocks = T / block > 0;  // pooled outputs are written only when there is a whole block
+  if (!k || !v || (blocks && (!pooled_k || !pooled_v)) || (rope_theta != 0.f && !k_rot)) return ND_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || (blocks && (!aligned16(pooled_k) || !aligned16(pooled_v))) ||
+      (k_rot && !aligned16(k_rot)))
+    return ND_ERR_INVALID_ARG;
+  const size_t need = nd_kv_compress_pool_rope_workspace_size(T, head_dim, rope_theta);
+  if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return ND_ERR_WORKSPACE;
+  int st = check_device(nullptr);
+  if (st != ND_OK) return st;
+  return finish(launch_pool_rope(k, v, k_rot, pooled_k, pooled_v, batch, T, n_heads, head_dim, block, rope_theta,
+                                 workspace, /*chained=*/false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int nd_kv_budget_window(const nd_model_cfg *cfg, int *budget_out, int *effective_out) {

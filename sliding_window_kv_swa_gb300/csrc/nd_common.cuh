@@ -122,6 +122,20 @@ __device__ __forceinline__ float2 rot_cs(double pos, double freq) {
   return make_float2(c, s);
 }
 
+// rint(x / scale) with the IEEE fp32 divide, bit for bit, without paying
+// for the divide on almost every element: p = x * fl(1/scale) differs from
+// the rounded quotient fl(x/scale) by at most |x/scale| * 1.5 * 2^-23
+// <= 2.3e-5 (|x/scale| <= 127.5 for codec inputs), so rint(p) equals
+// rint(fl(x/scale)) unless p lies within that distance of a half-integer;
+// within 1e-4 of one (or for scales so small that 1/scale could overflow) the
+// quotient is taken with the IEEE divide.  inv = __frcp_rn(scale).
+__device__ __forceinline__ float codec_rint(float x, float scale, float inv) {
+  const float p = x * inv;
+  const float f = p - floorf(p);
+  if (fabsf(f - 0.5f) > 1e-4f && scale >= 1e-30f) return rintf(p);
+  return rintf(__fdiv_rn(x, scale));
+}
+
 // The cache codec on one row of 32*CPL channels held by a full warp (lane l
 // has channels [l*CPL, l*CPL + CPL)): per 32-channel group amax = max |x|
 // (a shuffle over the group's 32/CPL lanes), scale = amax / 127 and
@@ -136,11 +150,11 @@ __device__ __forceinline__ float quant_lanes(const float *x, int *code) {
 #pragma unroll
   for (int off = kLanesPerGroup / 2; off >= 1; off >>= 1)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float scale = __fdiv_rn(amax, 127.0f);
+  const float scale = __fdiv_rn(amax, 127.0f), inv = __frcp_rn(scale);
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     float r = 0.f;
-    if (amax != 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f);
+    if (amax != 0.f) r = fminf(fmaxf(codec_rint(x[i], scale, inv), -127.f), 127.f);
     code[i] = int(r);
   }
   return scale;

@@ -26,10 +26,14 @@ int validate_decode(const void *q, const nd_kv_cache *cache, int n_q_heads, int 
 cudaError_t launch_kv_append_quant(const nd_kv_cache &c, const void *k_new, const void *v_new,
                                    int to_sink, int *err, cudaStream_t stream);
 
-// Prefill -> cache handoff (nd_kv_cache_from_prefill); a dependent launch.
+// Prefill -> cache handoff (nd_kv_cache_from_prefill): a planning kernel
+// (one CTA per cache row) writes each row's kept tokens to `plan`
+// (kv_fill_plan_ints ints per row), then a quantising kernel; dependent
+// launches.
+size_t kv_fill_plan_ints(int sink_cap, int ring_cap);
 cudaError_t launch_kv_fill(const nd_kv_cache &c, const void *k, const void *v, int batch, int T,
                            const int32_t *seg_ids, const uint8_t *sink, const int32_t *src_row,
-                           const int32_t *src_seg, int *err, cudaStream_t stream);
+                           const int32_t *src_seg, int32_t *plan, int *err, cudaStream_t stream);
 
 cudaError_t launch_kv_quant_rows(const void *x, int64_t n_rows, int head_dim, int8_t *codes,
                                  float *scales, cudaStream_t stream);
@@ -115,6 +119,14 @@ size_t rope_table_bytes(int T, int head_dim);
 cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, void *k_out, int Hkv,
                            int batch, int T, int head_dim, float theta, bool f32, void *table,
                            bool chained, cudaStream_t stream);
+
+// The compressed prefill's fused pass: the angle table (theta != 0) into
+// `table`, then one read of K and V writing K rotated at every position
+// (k_rot; nothing when theta == 0) and the pooled blocks (pooled K rotated
+// at the midpoint).  chained as in launch_rope_qk.
+cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk, void *pv, int batch, int T,
+                             int n_heads, int head_dim, int block, float theta, void *table, bool chained,
+                             cudaStream_t stream);
 
 cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T, int n_heads,
                                  int head_dim, int block, float theta, void *pk, void *pv,

@@ -8,11 +8,13 @@
 // visible iff (j+1)*block <= q - window + 1, then the causal sliding window.
 //
 // This is the path for fp32 inputs (parity at 1e-4 rules out reduced-precision
-// tensor-core inputs).  One CTA takes 64 query rows of one (sequence, query
-// head); two threads share a row and split the head dimension.  Key tiles of
-// 64 are staged in shared memory; a tile is skipped when no row of the CTA can
-// see any of its keys (causal bound, window bound without sinks, or disjoint
-// segment-id ranges).  Online softmax in the log2 domain.
+// tensor-core inputs).  One CTA takes 16 query rows of one (sequence, query
+// head); eight threads share a row and split the head dimension (short
+// dot-product chains, two partial sums each, and four times the CTAs of a
+// two-threads-per-row layout for the small problems this path serves).  Key
+// tiles of 64 are staged in shared memory; a tile is skipped when no row of
+// the CTA can see any of its keys (causal bound, window bound without sinks,
+// or disjoint segment-id ranges).  Online softmax in the log2 domain.
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -22,7 +24,8 @@ namespace nd {
 
 namespace {
 
-constexpr int kRows = 64, kKeys = 64, kThreads = 128;
+constexpr int kTpr = 8;  // threads per query row
+constexpr int kRows = 16, kKeys = 64, kThreads = kRows * kTpr;
 
 template <typename E>
 __device__ __forceinline__ float ld_elem(const E *p, size_t i);
@@ -43,7 +46,7 @@ __device__ __forceinline__ void st_elem<uint16_t>(uint16_t *p, size_t i, float x
 
 template <typename E, int D>
 __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArgs a) {
-  constexpr int H2 = D / 2;
+  constexpr int H2 = D / kTpr;  // channels per thread
   extern __shared__ float smem[];
   float *sk = smem;                 // [kKeys][D]
   float *sv = sk + kKeys * D;       // [kKeys][D]
@@ -53,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
 
   const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
   const int T = a.T, G = a.Hq / a.Hkv, hk = hq / G;
-  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int r = threadIdx.x / kTpr, part = threadIdx.x % kTpr;  // part: this thread's channel slice
   const int q0 = qt * kRows;
   const int q = q0 + r;
   const bool row_ok = q < T;
@@ -69,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
     s_qseg_hi = INT_MIN;
   }
   __syncthreads();
-  if (half == 0 && row_ok && my_seg > 0) {
+  if (part == 0 && row_ok && my_seg > 0) {
     atomicMin(&s_qseg_lo, my_seg);
     atomicMax(&s_qseg_hi, my_seg);
   }
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
   float qr[H2], o[H2];
 #pragma unroll
   for (int c = 0; c < H2; ++c) {
-    qr[c] = row_ok ? ld_elem(Q, ((size_t(b) * T + q) * a.Hq + hq) * D + half * H2 + c) * qscale : 0.f;
+    qr[c] = row_ok ? ld_elem(Q, ((size_t(b) * T + q) * a.Hq + hq) * D + part * H2 + c) * qscale : 0.f;
     o[c] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -122,47 +125,94 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
           continue;
         }
       }
-      // ---- stage K and V tile (fp32)
-      for (int idx = threadIdx.x; idx < kKeys * D; idx += kThreads) {
-        const int kk = idx / D, c = idx % D;
-        const int k = k0 + kk;
-        float kv = 0.f, vv = 0.f;
-        if (k < TK) {
-          const size_t off = ((size_t(b) * TK + k) * a.Hkv + hk) * D + c;
-          kv = ld_elem(KK, off);
-          vv = ld_elem(VV, off);
+      // ---- stage K and V tile (fp32): 16-byte loads, a thread's loads all
+      //      issued before its shared-memory stores
+      if constexpr (sizeof(E) == 4) {
+        constexpr int kVec = kKeys * D / 4, kPer = kVec / kThreads;
+        float4 kx[kPer], vx[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int idx = threadIdx.x + u * kThreads;
+          const int kk = idx / (D / 4), c4 = idx % (D / 4);
+          const int k = k0 + kk;
+          kx[u] = vx[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (k < TK) {
+            const size_t off = ((size_t(b) * TK + k) * a.Hkv + hk) * D + 4 * c4;
+            kx[u] = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(KK) + off);
+            vx[u] = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(VV) + off);
+          }
         }
-        sk[idx] = kv;
-        sv[idx] = vv;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int idx = threadIdx.x + u * kThreads;
+          reinterpret_cast<float4 *>(sk)[idx] = kx[u];
+          reinterpret_cast<float4 *>(sv)[idx] = vx[u];
+        }
+      } else {
+        for (int idx = threadIdx.x; idx < kKeys * D; idx += kThreads) {
+          const int kk = idx / D, c = idx % D;
+          const int k = k0 + kk;
+          float kv = 0.f, vv = 0.f;
+          if (k < TK) {
+            const size_t off = ((size_t(b) * TK + k) * a.Hkv + hk) * D + c;
+            kv = ld_elem(KK, off);
+            vv = ld_elem(VV, off);
+          }
+          sk[idx] = kv;
+          sv[idx] = vv;
+        }
       }
       __syncthreads();
-      for (int kk = 0; kk < kKeys; ++kk) {
-        const int k = k0 + kk;
-        bool vis;
-        if (src) {
-          vis = row_ok && k < n_cols && (k + 1) * a.block <= q - W + 1;
-        } else {
-          vis = row_ok && k <= q && my_seg > 0 && s_seg[kk] == my_seg &&
-                (W == 0 || q - k < W || s_sink[kk]);
-        }
-        const float *kr = sk + kk * D + half * H2;
-        float s = 0.f;
+      // four keys per step: four independent dot products, then one max,
+      // one rescale and four exponentials (the online softmax's serial
+      // chain is a quarter as long)
+      constexpr int kStepKeys = 4;
+      for (int kk0 = 0; kk0 < kKeys; kk0 += kStepKeys) {
+        float sv4[kStepKeys];
+        bool vis4[kStepKeys];
 #pragma unroll
-        for (int c = 0; c < H2; ++c) s = fmaf(qr[c], kr[c], s);
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        if (!vis) continue;
-        if (s > m) {
-          const float f = ex2(m - s);
+        for (int u = 0; u < kStepKeys; ++u) {
+          const int kk = kk0 + u, k = k0 + kk;
+          if (src) {
+            vis4[u] = row_ok && k < n_cols && (k + 1) * a.block <= q - W + 1;
+          } else {
+            vis4[u] = row_ok && k <= q && my_seg > 0 && s_seg[kk] == my_seg &&
+                      (W == 0 || q - k < W || s_sink[kk]);
+          }
+          const float *kr = sk + kk * D + part * H2;
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int c = 0; c < H2; c += 2) {
+            s0 = fmaf(qr[c], kr[c], s0);
+            s1 = fmaf(qr[c + 1], kr[c + 1], s1);
+          }
+          sv4[u] = s0 + s1;
+        }
+#pragma unroll
+        for (int off = 1; off < kTpr; off <<= 1)
+#pragma unroll
+          for (int u = 0; u < kStepKeys; ++u) sv4[u] += __shfl_xor_sync(0xffffffffu, sv4[u], off);
+        float mx = m;
+#pragma unroll
+        for (int u = 0; u < kStepKeys; ++u)
+          if (vis4[u]) mx = fmaxf(mx, sv4[u]);
+        if (mx == -INFINITY) continue;  // nothing visible yet
+        if (mx > m) {
+          const float f = ex2(m - mx);  // m = -inf: f = 0
           l *= f;
 #pragma unroll
           for (int c = 0; c < H2; ++c) o[c] *= f;
-          m = s;
+          m = mx;
         }
-        const float pr = ex2(s - m);
-        l += pr;
-        const float *vr = sv + kk * D + half * H2;
 #pragma unroll
-        for (int c = 0; c < H2; ++c) o[c] = fmaf(pr, vr[c], o[c]);
+        for (int u = 0; u < kStepKeys; ++u) {
+          if (!vis4[u]) continue;
+          const float pr = ex2(sv4[u] - m);
+          l += pr;
+          const float *vr = sv + (kk0 + u) * D + part * H2;
+#pragma unroll
+          for (int c = 0; c < H2; ++c) o[c] = fmaf(pr, vr[c], o[c]);
+        }
       }
       __syncthreads();
     }
@@ -176,8 +226,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int c = 0; c < H2; ++c)
-      st_elem(O, ((size_t(b) * T + q) * a.Hq + hq) * D + half * H2 + c, o[c] * inv);
-    if (a.lse && half == 0)
+      st_elem(O, ((size_t(b) * T + q) * a.Hq + hq) * D + part * H2 + c, o[c] * inv);
+    if (a.lse && part == 0)
       a.lse[(size_t(b) * a.Hq + hq) * T + q] =
           l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   }

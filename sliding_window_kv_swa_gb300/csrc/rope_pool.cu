@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const 
   const int b = blockIdx.x / n_grp, j0 = (blockIdx.x % n_grp) * kPoolJ;
   const int nj = min(kPoolJ, nblk - j0);
   const int half = D / 2, groups = half / 8;
+  const int per_kv = nj * H * groups;
   if (apply_rope)
     for (int idx = threadIdx.x; idx < nj * half; idx += blockDim.x) {
       const int jj = idx / half, i = idx % half;
@@ -210,7 +211,6 @@ __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const 
     }
   __syncthreads();
   const float fblock = float(block);
-  const int per_kv = nj * H * groups;
   for (int idx = threadIdx.x; idx < 2 * per_kv; idx += blockDim.x) {
     const bool is_v = idx >= per_kv;
     const int w = is_v ? idx - per_kv : idx;
@@ -254,7 +254,141 @@ __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const 
   }
 }
 
+// The compressed prefill's pass over K and V, fused: K and V are read once;
+// K is written rotated at every position (k_rot, from the angle table as
+// rope_vec_kernel does) and the pooled blocks are written as pool_vec_kernel
+// writes them (the same sums, mean and midpoint rotation, angles from the
+// same table rows).  A CTA takes kPoolJ pooled blocks of one sequence (one
+// thread per (block, head, 8 channel pairs) of K or of V); one more CTA per
+// sequence rotates the positions past the last whole block.  cs == NULL: no
+// rotation (pooling only, k_rot untouched).
+// (The output pointers never alias the inputs: __restrict__ lets every row's
+// loads go out before the first rotated row is stored.)
+constexpr int kPoolRows = 4;  // rows of a block loaded before any is used
+__global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restrict__ k,
+                                                        const uint16_t *__restrict__ v,
+                                                        uint16_t *__restrict__ k_rot, uint16_t *__restrict__ pk,
+                                                        uint16_t *__restrict__ pv, int T, int H, int D, int block,
+                                                        const float2 *__restrict__ cs) {
+  pdl_wait();  // the angle table (or what the previous kernel wrote) is in
+  const int nblk = T / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ, tail = T - nblk * block;
+  const int per_seq = n_grp + (tail > 0 ? 1 : 0);
+  const int b = blockIdx.x / per_seq, grp = blockIdx.x % per_seq;
+  const int half = D / 2, groups = half / 8;
+  const size_t rstride = size_t(H) * D;
+  auto rotate8 = [&](int t, int i0, const float *a, const float *bb, float *ya, float *yb) {
+    const float4 *t4 = reinterpret_cast<const float4 *>(cs + size_t(t) * half + i0);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const float4 w = t4[q4];
+      rope_pair(a[2 * q4], bb[2 * q4], w.x, w.y, ya[2 * q4], yb[2 * q4]);
+      rope_pair(a[2 * q4 + 1], bb[2 * q4 + 1], w.z, w.w, ya[2 * q4 + 1], yb[2 * q4 + 1]);
+    }
+  };
+  if (grp == n_grp) {  // positions past the last whole block: K's rotation only
+    if (!cs) return;
+    for (int idx = threadIdx.x; idx < tail * H * groups; idx += blockDim.x) {
+      const int g = idx % groups, rest = idx / groups;
+      const int h = rest % H, t = nblk * block + rest / H, i0 = g * 8;
+      const size_t row = (size_t(b) * T + t) * rstride + size_t(h) * D;
+      float xa[8], xb[8], ya[8], yb[8];
+      ld8(k + row + i0, xa);
+      ld8(k + row + i0 + half, xb);
+      rotate8(t, i0, xa, xb, ya, yb);
+      st8(k_rot + row + i0, ya);
+      st8(k_rot + row + i0 + half, yb);
+    }
+    return;
+  }
+  const int j0 = grp * kPoolJ, nj = min(kPoolJ, nblk - j0);
+  const float fblock = float(block);
+  const int per_kv = nj * H * groups;
+  for (int idx = threadIdx.x; idx < 2 * per_kv; idx += blockDim.x) {
+    const bool is_v = idx >= per_kv;
+    const int w = is_v ? idx - per_kv : idx;
+    const int g = w % groups, rest = w / groups;
+    const int h = rest % H, j = j0 + rest / H;
+    const int i0 = g * 8;
+    const uint16_t *x = is_v ? v : k;
+    float sa[8], sb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sa[e] = sb[e] = 0.f;
+    const size_t row0 = (size_t(b) * T + size_t(j) * block) * rstride + size_t(h) * D;
+    for (int r0 = 0; r0 < block; r0 += kPoolRows) {
+      uint4 ra[kPoolRows], rb[kPoolRows];
+#pragma unroll
+      for (int r = 0; r < kPoolRows; ++r)
+        if (r0 + r < block) {
+          const size_t row = row0 + size_t(r0 + r) * rstride;
+          ra[r] = *reinterpret_cast<const uint4 *>(x + row + i0);
+          rb[r] = *reinterpret_cast<const uint4 *>(x + row + i0 + half);
+        }
+#pragma unroll
+      for (int r = 0; r < kPoolRows; ++r) {
+        if (r0 + r >= block) break;
+        float xa[8], xb[8];
+        const uint32_t ua[4] = {ra[r].x, ra[r].y, ra[r].z, ra[r].w}, ub[4] = {rb[r].x, rb[r].y, rb[r].z, rb[r].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xa[2 * e] = bf16_lo(ua[e]), xa[2 * e + 1] = bf16_hi(ua[e]);
+          xb[2 * e] = bf16_lo(ub[e]), xb[2 * e + 1] = bf16_hi(ub[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sa[e] += xa[e];
+          sb[e] += xb[e];
+        }
+        if (cs && !is_v) {
+          const size_t row = row0 + size_t(r0 + r) * rstride;
+          float ya[8], yb[8];
+          rotate8(j * block + r0 + r, i0, xa, xb, ya, yb);
+          st8(k_rot + row + i0, ya);
+          st8(k_rot + row + i0 + half, yb);
+        }
+      }
+    }
+    float ya[8], yb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sa[e] /= fblock;
+      sb[e] /= fblock;
+      ya[e] = sa[e];
+      yb[e] = sb[e];
+    }
+    if (cs && !is_v) rotate8(min(j * block + block / 2, T - 1), i0, sa, sb, ya, yb);
+    uint16_t *y = is_v ? pv : pk;
+    const size_t orow = ((size_t(b) * nblk + j) * H + h) * D;
+    st8(y + orow + i0, ya);
+    st8(y + orow + i0 + half, yb);
+  }
+}
+
 }  // namespace
+
+// The angle table (when theta != 0), then the fused pass; the table kernel
+// is chained as in launch_rope_qk.  head_dim a multiple of 16, 16-byte
+// aligned tensors.
+cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk, void *pv, int batch, int T,
+                             int n_heads, int head_dim, int block, float theta, void *table, bool chained,
+                             cudaStream_t stream) {
+  if (size_t(batch) * T == 0) return cudaSuccess;
+  float2 *cs = nullptr;
+  if (theta != 0.f) {
+    Freqs fr = make_freqs(head_dim, theta);
+    cs = static_cast<float2 *>(table);
+    const int half = head_dim / 2;
+    cudaError_t e = launch_pdl(rope_table_kernel, dim3((T * half + 255) / 256), dim3(256), 0, stream, cs, T,
+                               half, fr, chained ? 0 : 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int nblk = T / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
+  const int per_seq = n_grp + (T - nblk * block > 0 ? 1 : 0);
+  if (per_seq == 0) return cudaSuccess;
+  return launch_pdl(pool_rope_kernel, dim3(unsigned(size_t(batch) * per_seq)), dim3(256), 0, stream,
+                    static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), static_cast<uint16_t *>(k_rot),
+                    static_cast<uint16_t *>(pk), static_cast<uint16_t *>(pv), T, n_heads, head_dim, block,
+                    static_cast<const float2 *>(cs));
+}
 
 Freqs make_freqs(int D, float theta) {
   Freqs fr;

@@ -73,7 +73,8 @@ def _lib():
             "nd_set_prefill_epilogue_wait_limit": (I, [ctypes.c_uint]),
             "nd_kv_append_quant": (I, [P, P, P, I, P]),
             "nd_kv_quant_rows": (I, [P, L, I, P, P, P]),
-            "nd_kv_cache_from_prefill": (I, [P, P, P, I, I, P, P, P, P, P]),
+            "nd_kv_cache_from_prefill_workspace_size": (S, [I, I, I]),
+            "nd_kv_cache_from_prefill": (I, [P, P, P, I, I, P, P, P, P, P, S, P]),
             "nd_swa_sink_decode_workspace_size": (S, [I, I, I, I, I]),
             "nd_swa_sink_decode": (I, [P, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_decode_noalloc": (I, [P, P, I, I, P, P, P]),
@@ -91,6 +92,8 @@ def _lib():
             "nd_swa_sink_chunk_prefill_tiles": (I, [P, I, I, I, I, I, I, I, I, P]),
             "nd_rope_apply": (I, [P, P, I, I, I, I, F, P]),
             "nd_kv_compress_pool": (I, [P, P, I, I, I, I, I, F, P, P, P]),
+            "nd_kv_compress_pool_rope_workspace_size": (S, [I, I, F]),
+            "nd_kv_compress_pool_rope": (I, [P, P, I, I, I, I, I, F, P, P, P, P, S, P]),
             "nd_kv_budget_window": (I, [P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -108,7 +111,7 @@ def library_path() -> str:
 
 EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_errors",
             "nd_set_prefill_epilogue_wait_limit",
-            "nd_kv_append_quant", "nd_kv_quant_rows", "nd_kv_cache_from_prefill", "nd_swa_sink_decode_workspace_size",
+            "nd_kv_append_quant", "nd_kv_quant_rows", "nd_kv_cache_from_prefill_workspace_size", "nd_kv_cache_from_prefill", "nd_swa_sink_decode_workspace_size",
             "nd_swa_sink_decode", "nd_swa_sink_decode_noalloc", "nd_swa_sink_decode_step",
             "nd_swa_sink_decode_step_host_workspace_size", "nd_swa_sink_decode_step_host",
             "nd_swa_sink_decode_step_host_packed",
@@ -117,7 +120,8 @@ EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_e
             "nd_swa_sink_prefill", "nd_swa_sink_prefill_tiles",
             "nd_swa_sink_chunk_prefill_workspace_size", "nd_swa_sink_chunk_prefill",
             "nd_swa_sink_chunk_prefill_tiles",
-            "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_budget_window")
+            "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_compress_pool_rope_workspace_size",
+            "nd_kv_compress_pool_rope", "nd_kv_budget_window")
 
 
 def _check(fn: str, status: int):
@@ -256,17 +260,25 @@ def nd_kv_quant_rows(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
                                                        _stream(stream)))
 
 
+def nd_kv_cache_from_prefill_workspace_size(cache_batch: int, sink_cap: int, ring_cap: int) -> int:
+    return int(_lib().nd_kv_cache_from_prefill_workspace_size(cache_batch, sink_cap, ring_cap))
+
+
 def nd_kv_cache_from_prefill(cache: KVCache, k: torch.Tensor, v: torch.Tensor, src_row: torch.Tensor,
                              seg_ids: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
-                             src_seg: Optional[torch.Tensor] = None, stream=None) -> None:
+                             src_seg: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                             stream=None) -> None:
     """Fill cache row e from segment src_seg[e] of batch row src_row[e] of a
     prefill's k / v (bf16 [B, T, Hkv, d]) as appending its tokens in order
     would; src_row / src_seg int32 [cache.batch] on the device."""
     B, T = k.shape[:2]
+    if workspace is None:
+        nbytes = nd_kv_cache_from_prefill_workspace_size(cache.batch, cache.sink_cap, cache.ring_cap)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=cache.k_codes.device)
     s = cache.struct()
     _check("nd_kv_cache_from_prefill", _lib().nd_kv_cache_from_prefill(
         ctypes.byref(s), _ptr(k), _ptr(v), B, T, _ptr(seg_ids), _ptr(sink), _ptr(src_row), _ptr(src_seg),
-        _stream(stream)))
+        _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def nd_swa_sink_decode_workspace_size(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
@@ -507,6 +519,33 @@ def nd_kv_compress_pool(k: torch.Tensor, v: torch.Tensor, block: int, rope_theta
         _ptr(k), _ptr(v), B, T, H, d, int(block), float(rope_theta), _ptr(pooled_k), _ptr(pooled_v),
         _stream(stream)))
     return pooled_k, pooled_v
+
+
+def nd_kv_compress_pool_rope_workspace_size(T: int, head_dim: int, rope_theta: float) -> int:
+    return int(_lib().nd_kv_compress_pool_rope_workspace_size(T, head_dim, float(rope_theta)))
+
+
+def nd_kv_compress_pool_rope(k: torch.Tensor, v: torch.Tensor, block: int, rope_theta: float = 0.0,
+                             k_rot: Optional[torch.Tensor] = None, pooled_k: Optional[torch.Tensor] = None,
+                             pooled_v: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                             stream=None):
+    """One pass over K and V: K rotated at every position (k_rot) and the
+    pooled blocks (as nd_kv_compress_pool).  Returns (k_rot, pooled_k, pooled_v)."""
+    B, T, H, d = k.shape
+    nb = T // block
+    if k_rot is None and rope_theta:
+        k_rot = torch.empty_like(k)
+    if pooled_k is None:
+        pooled_k = torch.empty((B, nb, H, d), dtype=k.dtype, device=k.device)
+    if pooled_v is None:
+        pooled_v = torch.empty((B, nb, H, d), dtype=v.dtype, device=v.device)
+    if workspace is None:
+        workspace = torch.empty(max(nd_kv_compress_pool_rope_workspace_size(T, d, rope_theta), 16),
+                                dtype=torch.uint8, device=k.device)
+    _check("nd_kv_compress_pool_rope", _lib().nd_kv_compress_pool_rope(
+        _ptr(k), _ptr(v), B, T, H, d, int(block), float(rope_theta), _ptr(k_rot), _ptr(pooled_k), _ptr(pooled_v),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return k_rot, pooled_k, pooled_v
 
 
 def nd_kv_budget_window(d_model: int, attn_dim: int, num_heads: int, num_kv_heads: int, num_layers: int,

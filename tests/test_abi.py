@@ -105,13 +105,19 @@ def test_host_validation_before_any_device_work():
     fill = lib.nd_kv_cache_from_prefill
     fill.restype = ctypes.c_int
     no_ring = nd.nd._Cache(1, 1, 64, 4, 0, 16, 16, 16, 16, 16, 16, 16, 16)
-    assert fill(ctypes.byref(no_ring), P(16), P(16), 1, 8, None, None, P(16), None, None) == 1
-    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, None, None, None) == 1
-    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, P(16), None, P(16), None, None) == 1
-    assert fill(ctypes.byref(cache), P(18), P(16), 1, 8, None, None, P(16), None, None) == 1
-    assert fill(ctypes.byref(cache), P(16), P(16), -1, 8, None, None, P(16), None, None) == 1
+    W16, Z = P(16), ctypes.c_size_t
+    assert fill(ctypes.byref(no_ring), P(16), P(16), 1, 8, None, None, P(16), None, W16, Z(1 << 20), None) == 1
+    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, None, None, W16, Z(1 << 20), None) == 1
+    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, P(16), None, P(16), None, W16, Z(1 << 20), None) == 1
+    assert fill(ctypes.byref(cache), P(18), P(16), 1, 8, None, None, P(16), None, W16, Z(1 << 20), None) == 1
+    assert fill(ctypes.byref(cache), P(16), P(16), -1, 8, None, None, P(16), None, W16, Z(1 << 20), None) == 1
     wide = nd.nd._Cache(1, 1, 512, 4, 8, 16, 16, 16, 16, 16, 16, 16, 16)
-    assert fill(ctypes.byref(wide), P(16), P(16), 1, 8, None, None, P(16), None, None) == 2
+    assert fill(ctypes.byref(wide), P(16), P(16), 1, 8, None, None, P(16), None, W16, Z(1 << 20), None) == 2
+    # the kept tokens' plan: one (position, slot) pair per slot and a count, per row
+    need = nd.nd_kv_cache_from_prefill_workspace_size(1, 4, 8)
+    assert need >= (1 + 2 * 12) * 4
+    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, P(16), None, None, Z(need), None) == 4
+    assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, P(16), None, W16, Z(need - 16), None) == 4
     # chunked prefill: window >= 1, a ring, GQA ratio, head_dim 64/128, workspace
     chunk = lib.nd_swa_sink_chunk_prefill
     chunk.restype = ctypes.c_int
@@ -203,7 +209,7 @@ def test_empty_problems_return_ok_without_a_device():
     calls = {
         "nd_kv_append_quant": (e, None, None, 0, None),
         "nd_kv_quant_rows": (None, ctypes.c_int64(0), 64, None, None, None),
-        "nd_kv_cache_from_prefill": (e, None, None, 1, 16, None, None, None, None, None),
+        "nd_kv_cache_from_prefill": (e, None, None, 1, 16, None, None, None, None, None, Z(0), None),
         "nd_swa_sink_chunk_prefill": (None, None, None, 16, e, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode": (None, e, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step": (None, e, None, None, 4, 8, None, None, None, Z(0), None),

@@ -43,6 +43,38 @@ def test_quant_rows_bit_exact(d):
     np.testing.assert_array_equal(host(scales).view(np.uint32), ws.view(np.uint32))
 
 
+def test_quant_rows_quotients_at_and_beside_half_integers():
+    """Groups whose quotients x / scale sit exactly on half-integers (ties to
+    even) and one or two bf16 steps either side of them, at several scales:
+    the kernels' rounding near these boundaries must give the oracle's codes
+    (fp32 IEEE divide, rint) bit for bit."""
+    rows = []
+    for k in (-20, -3, 0, 5, 17):
+        sc = 2.0 ** k
+        for n in range(-127, 127, 3):
+            base = (n + 0.5) * sc
+            vals = [base]
+            b = to_bf16_bits(np.array([base], np.float32)).astype(np.int32)[0]
+            for dlt in (-2, -1, 1, 2):
+                vals.append(float(bf16_bits_to_f32(np.array([b + dlt], np.uint16))[0]))
+            row = np.zeros(32, np.float32)
+            row[0] = 127.0 * sc              # amax: scale = 2^k exactly
+            row[1:1 + len(vals)] = vals
+            row[6:] = np.linspace(-126.0, 126.0, 26, dtype=np.float32) * sc
+            rows.append(row)
+    while len(rows) % 4:
+        rows.append(rows[0])
+    x = np.stack(rows).reshape(-1, 128)
+    bits = to_bf16_bits(x)
+    n = x.shape[0]
+    codes = torch.empty((n, 128), dtype=torch.int8, device="cuda")
+    scales = torch.empty((n, 4), dtype=torch.float32, device="cuda")
+    nd().nd_kv_quant_rows(dev_bf16(bits), codes, scales)
+    wc, ws = oracle.quant_g32(bf16_bits_to_f32(bits))
+    np.testing.assert_array_equal(host(codes), wc)
+    np.testing.assert_array_equal(host(scales).view(np.uint32), ws.view(np.uint32))
+
+
 def test_quant_rows_golden_ties():
     from test_oracle_attention import read_codec_fixture
     groups = read_codec_fixture()

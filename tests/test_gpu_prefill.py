@@ -376,3 +376,51 @@ def test_prefill_tile_count_reported_by_the_kernel_plan(Hq, Hkv, d):
         assert visible * Hq <= got <= causal * Hq, (visible * Hq, got, causal * Hq)
         if snk is None:
             assert got == causal * Hq
+
+
+@pytest.mark.parametrize("block,T,d,theta", [(4, 4096, 64, 10000.0), (3, 301, 64, 10000.0), (8, 1000, 128, 500000.0),
+                                             (1, 77, 64, 10000.0), (4, 258, 128, 0.0), (16, 10, 64, 10000.0)])
+def test_pool_rope_pass_matches_the_separate_passes(block, T, d, theta):
+    """nd_kv_compress_pool_rope (one read of K and V) gives bit for bit the
+    rotated keys of nd_rope_apply and the pooled blocks of nd_kv_compress_pool
+    (positions past the last whole block are rotated too)."""
+    rng = philox(1950 + block + T + d)
+    B, H = 2, 3
+    kb, _ = normal_bf16(rng, (B, T, H, d))
+    vb, _ = normal_bf16(rng, (B, T, H, d))
+    lib = nd()
+    k_d, v_d = dev_bf16(kb), dev_bf16(vb)
+    k_rot, pk, pv = lib.nd_kv_compress_pool_rope(k_d, v_d, block, theta)
+    rk, rv = lib.nd_kv_compress_pool(k_d, v_d, block, theta)
+    torch.cuda.synchronize()
+    assert torch.equal(pk.view(torch.int16), rk.view(torch.int16))
+    assert torch.equal(pv.view(torch.int16), rv.view(torch.int16))
+    if theta:
+        assert torch.equal(k_rot.view(torch.int16), lib.nd_rope_apply(k_d, rope_theta=theta).view(torch.int16))
+
+
+@pytest.mark.parametrize("T,W,block,d,H", [(4096, 256, 4, 64, 16), (700, 40, 8, 128, 4), (301, 17, 3, 64, 2),
+                                           (129, 1, 2, 128, 3)])
+def test_compressed_prefill_pooling_inside_the_call(T, W, block, d, H):
+    """With pooled_k = pooled_v = NULL the compressed prefill pools K and V
+    itself in the same pass that rotates K: the output carries the same bits
+    as pooling with nd_kv_compress_pool first (and matches the oracle)."""
+    rng = philox(1960 + T + d)
+    B = 2 if T < 4096 else 1
+    qb, q = normal_bf16(rng, (B, T, H, d))
+    kb, k = normal_bf16(rng, (B, T, H, d))
+    vb, v = normal_bf16(rng, (B, T, H, d))
+    lib = nd()
+    q_d, k_d, v_d = dev_bf16(qb), dev_bf16(kb), dev_bf16(vb)
+    pk, pv = lib.nd_kv_compress_pool(k_d, v_d, block, 10000.0)
+    lse_a = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    lse_b = torch.empty_like(lse_a)
+    a = lib.nd_swa_sink_prefill(q_d, k_d, v_d, None, None, W, rope_theta=10000.0, pooled_k=pk, pooled_v=pv,
+                                block=block, lse=lse_a)
+    b = lib.nd_swa_sink_prefill(q_d, k_d, v_d, None, None, W, rope_theta=10000.0, block=block, lse=lse_b)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(lse_a, lse_b)
+    if T < 4096:
+        want, _ = oracle.compressed_prefill(q, k, v, W, block, 10000.0)
+        assert_close_bf16(host(b), want, "pooling inside the call")
