@@ -604,6 +604,49 @@ def bench_compressed(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None, b
                 launches=4 * steps)
 
 
+def visible_pairs_pinned(T, W, b, P):
+    """Visible (query, column) pairs of one (sequence, head) of the pinned
+    compressed prefill: pinned keys, exact window keys past the pins, and
+    the visible pooled blocks of the positions after the pins."""
+    t = np.arange(T)
+    pinned = np.minimum(t + 1, P)
+    lo = np.maximum(t - W + 1, P)
+    exact = np.clip(t - lo + 1, 0, None)
+    pooled = np.clip((t - W + 1 - P) // b, 0, (T - P) // b)
+    return int((pinned + exact + pooled).sum())
+
+
+def bench_compressed_pinned(torch, nd, steps, warmup, pk, dist=None, block=4, n_pinned=512):
+    """The compressed prefill with a pinned prefix (the first n_pinned
+    positions exact and visible at any distance, blocks pooled after them):
+    one nd_compressed_prefill call (fused pooling + rotation, attention)."""
+    from workloads import compressed
+    w = compressed()
+    B, T, H, d = w["q"].shape
+    q, k, v = dev_bf16(torch, w["q_bits"]), dev_bf16(torch, w["k_bits"]), dev_bf16(torch, w["v_bits"])
+    out = torch.empty_like(q)
+    ws = torch.empty(nd.nd_compressed_prefill_workspace_size(B, T, H, H, d, w["rope_theta"], block), dtype=torch.uint8,
+                     device="cuda")
+
+    def step(i):
+        nd.nd_compressed_prefill(q, k, v, w["window"], block, n_pinned=n_pinned, rope_theta=w["rope_theta"], out=out,
+                                 workspace=ws)
+
+    ms = time_graph(torch, step, steps, warmup, dist)
+    t = ms / steps
+    tiles = nd.nd_swa_sink_prefill_tiles(ws, B, T, H, H, d, w["rope_theta"], block)
+    pairs = visible_pairs_pinned(T, w["window"], block, n_pinned) * B * H
+    flops = 4.0 * d * pairs
+    tile_flops = 4.0 * 128 * 64 * d * tiles
+    return dict(config=f"compressed prefill with a {n_pinned}-token pinned prefix, B{B} T{T} H{H} d{d} W256 b{block} "
+                       f"RoPE, one call", ms_per_step=t, tok_s=B * T / (t * 1e-3), visible_pairs=pairs, tiles=tiles,
+                tile_overhead=tile_flops / flops,
+                algorithmic=roofline("tensor", flops, t, pk["bf16"], "TFLOP/s", "whole call (visible pairs)", pk["src"]),
+                roofline=roofline("tensor", tile_flops, t, pk["bf16"], "TFLOP/s",
+                                  "whole call (tiles the attention kernel's plan performed)", pk["src"]),
+                launches=4 * steps)
+
+
 def bench_tiny_fp32(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None):
     """fp32 tiny prefill (B1 T512 Hq4 Hkv1 d64, W256; literal segments and the
     single-segment variant) on CUDA cores: FLOP/s against the fp32 FFMA peak."""
@@ -857,8 +900,8 @@ def oracle_decode_sample(B, Hq, Hkv, d, S, W, seed, budget_s, of_batch=None):
 
 HEAD = dict(B=512, Hq=32, Hkv=8, d=128, S=1024, W=256)
 ORACLE_SAMPLE = 32   # sequences of the headline workload the oracle decodes per step
-ALL_ROWS = ("step_b64", "sweep", "wsweep", "packed", "compressed", "compressed_b8", "tiny", "pool", "pool_rope",
-            "append", "fill", "cdecode", "chunk")
+ALL_ROWS = ("step_b64", "sweep", "wsweep", "packed", "compressed", "compressed_b8", "compressed_pinned", "tiny",
+            "pool", "pool_rope", "append", "fill", "cdecode", "chunk")
 
 
 def main():
@@ -975,6 +1018,9 @@ def main():
         rows["compressed_prefill_b8"] = bench_compressed(torch, nd, row_steps, warmup, pk, dist, cpu_budget=budget,
                                                          block=8)
         torch.cuda.empty_cache()
+    if "compressed_pinned" in want:
+        rows["compressed_prefill_pinned"] = bench_compressed_pinned(torch, nd, row_steps, warmup, pk, dist)
+        torch.cuda.empty_cache()
     if "tiny" in want:
         rows["tiny_prefill_fp32"] = bench_tiny_fp32(torch, nd, row_steps, warmup, pk, dist,
                                                     cpu_budget=None if budget is None else 1.0)
@@ -1017,7 +1063,7 @@ def main():
     }
     if rank == 0:
         try:
-            cb = oracle_decode_sample(ORACLE_SAMPLE, h["Hq"], h["Hkv"], h["d"], h["S"], h["W"], 1234 + 4,
+            cb = oracle_decode_sample(min(ORACLE_SAMPLE, h["B"]), h["Hq"], h["Hkv"], h["d"], h["S"], h["W"], 1234 + 4,
                                       args.cpu_budget, of_batch=h["B"])
             cb.pop("seconds", None)
             line["cpu_baseline"] = cb

@@ -441,6 +441,31 @@ ND_API int nd_swa_sink_prefill(const void *q, const void *k, const void *v,
                         size_t workspace_bytes, nd_stream_t stream);
 
 /*
+ * Compressed-attention prefill with a pinned prefix (the compressed
+ * attention of [C3] "Two kinds of columns" with the sink prefix of [N2]
+ * "KV Sinks for Tools"; the library's reading, the same as
+ * nd_compressed_decode_step's): keys 0 .. n_pinned-1 are exact keys visible
+ * to every later query; the pooled blocks tile the positions after them
+ * (block j = positions n_pinned + j*block .. + block-1, its key the mean of
+ * the unrotated keys rotated at n_pinned + j*block + block/2) and are visible
+ * to query t iff (j+1)*block <= t - window + 1 - n_pinned; the other keys are
+ * exact within the window (t - k < window, k <= t).  n_pinned = 0 is
+ * nd_swa_sink_prefill's compressed variant with pooled_k = pooled_v = NULL.
+ * The call pools K and V itself (fused with K's rotation, into the
+ * workspace).  q, k, v, out, lse as nd_swa_sink_prefill (bf16, before
+ * rotation; rope_theta 0 = none); window >= 1, block >= 1,
+ * 0 <= n_pinned <= T; head_dim 64 or 128.
+ */
+ND_API size_t nd_compressed_prefill_workspace_size(int batch, int T, int n_q_heads,
+                                                   int n_kv_heads, int head_dim,
+                                                   float rope_theta, int block);
+ND_API int nd_compressed_prefill(const void *q, const void *k, const void *v, int batch, int T,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int window,
+                                 int block, int n_pinned, float rope_theta, void *out,
+                                 float *lse, void *workspace, size_t workspace_bytes,
+                                 nd_stream_t stream);
+
+/*
  * Chunked prefill against the bounded cache: a chunk of `chunk` new tokens
  * per sequence, at positions p0 .. p0+chunk-1 where p0 = seq_len, attends
  * under the decode mask of [N1] "256-token 滑动窗口：源码走读" (causal, and a

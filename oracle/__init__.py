@@ -189,6 +189,38 @@ def compressed_prefill(q, k, v, window: int, block: int, rope_theta: float = 0.0
     return attention(qr, kk, vv, mask, rows)
 
 
+def compressed_prefill_pinned(q, k, v, window: int, block: int, n_pinned: int,
+                              rope_theta: float = 0.0, rows=None):
+    """Compressed attention with a pinned prefix ("Compressed attention and
+    the copy probe" with the sink prefix of "KV Sinks for Tools"; the reading
+    used by the compressed decode): keys 0..n_pinned-1 are exact keys visible
+    at any distance; pooled block j covers positions n_pinned + j*block ..
+    + block-1 (mean before rotation, rotated at n_pinned + j*block +
+    block//2) and is visible to query t iff (j+1)*block <= t - window + 1 -
+    n_pinned; other keys k are visible iff k <= t and t - k < window.  One
+    softmax over [pooled blocks, exact keys].  Returns (out, lse) as
+    :func:`attention`."""
+    q = _c(q, np.float64)
+    k = _c(k, np.float64)
+    v = _c(v, np.float64)
+    B, T, Hq, d = q.shape
+    pos = np.arange(T)
+    qr = rope(q, pos, rope_theta) if rope_theta else q
+    kr = rope(k, pos, rope_theta) if rope_theta else k
+    nb = (T - n_pinned) // block
+    pk = pool_blocks(k[:, n_pinned:n_pinned + nb * block], block) if nb else np.zeros((B, 0) + k.shape[2:])
+    pv = pool_blocks(v[:, n_pinned:n_pinned + nb * block], block) if nb else np.zeros((B, 0) + v.shape[2:])
+    if nb and rope_theta:
+        pk = rope(pk, n_pinned + np.arange(nb) * block + block // 2, rope_theta)
+    t = pos[:, None]
+    j = np.arange(nb)[None, :]
+    pooled_vis = (j + 1) * block <= t - window + 1 - n_pinned
+    kk = pos[None, :]
+    exact_vis = (kk <= t) & ((t - kk < window) | (kk < n_pinned))
+    mask = np.concatenate([pooled_vis, exact_vis], axis=1)
+    return attention(qr, np.concatenate([pk, kr], axis=1), np.concatenate([pv, v], axis=1), mask, rows)
+
+
 # --------------------------------------------------------------------------
 # int8 group-32 codec and the bounded cache
 # --------------------------------------------------------------------------

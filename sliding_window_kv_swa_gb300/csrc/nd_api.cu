@@ -502,11 +502,11 @@ int nd_swa_sink_prefill_tiles(const void *workspace, int batch, int T, int n_q_h
   return ND_OK;
 }
 
-int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dtype, int batch,
-                        int T, int n_q_heads, int n_kv_heads, int head_dim,
-                        const int32_t *seg_ids, const uint8_t *sink, int window, float rope_theta,
-                        const void *pooled_k, const void *pooled_v, int block, void *out,
-                        float *lse, void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+static int prefill_impl(const void *q, const void *k, const void *v, nd_dtype dtype, int batch, int T,
+                        int n_q_heads, int n_kv_heads, int head_dim, const int32_t *seg_ids,
+                        const uint8_t *sink, int window, float rope_theta, const void *pooled_k,
+                        const void *pooled_v, int block, int n_pinned, void *out, float *lse,
+                        void *workspace, size_t workspace_bytes, nd_stream_t stream) {
   if (dtype != ND_F32 && dtype != ND_BF16) return ND_ERR_INVALID_ARG;
   if (batch < 0 || T < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || window < 0 || block < 0)
     return ND_ERR_INVALID_ARG;
@@ -549,6 +549,7 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
   a.block = block;
   a.out = out;
   a.lse = lse;
+  a.n_pinned = n_pinned;
 
   char *ws = static_cast<char *>(workspace);
   const size_t esz = dtype == ND_F32 ? 4 : 2;
@@ -575,8 +576,8 @@ int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dt
     const size_t pb = prefill_pooled_bytes(batch, T, n_kv_heads, head_dim, block) / 2;
     a.pooled_k = pooled;
     a.pooled_v = pooled + pb;
-    e = launch_pool_rope(k, v, kr, pooled, pooled + pb, batch, T, n_kv_heads, head_dim, block, rope_theta, table,
-                         /*chained=*/true, s);
+    e = launch_pool_rope(k, v, kr, pooled, pooled + pb, batch, T, n_kv_heads, head_dim, block, a.n_pinned,
+                         rope_theta, table, /*chained=*/true, s);
     if (table) {
       a.k = kr;
       a.rope_cs = table;
@@ -705,6 +706,29 @@ int nd_set_prefill_epilogue_wait_limit(unsigned polls) {
   return finish(set_epilogue_wait_limit(polls));
 }
 
+int nd_swa_sink_prefill(const void *q, const void *k, const void *v, nd_dtype dtype, int batch,
+                        int T, int n_q_heads, int n_kv_heads, int head_dim,
+                        const int32_t *seg_ids, const uint8_t *sink, int window, float rope_theta,
+                        const void *pooled_k, const void *pooled_v, int block, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+  return prefill_impl(q, k, v, dtype, batch, T, n_q_heads, n_kv_heads, head_dim, seg_ids, sink, window, rope_theta,
+                      pooled_k, pooled_v, block, 0, out, lse, workspace, workspace_bytes, stream);
+}
+
+size_t nd_compressed_prefill_workspace_size(int batch, int T, int n_q_heads, int n_kv_heads, int head_dim,
+                                            float rope_theta, int block) {
+  if (block <= 0) return 0;
+  return nd_swa_sink_prefill_workspace_size(ND_BF16, batch, T, n_q_heads, n_kv_heads, head_dim, rope_theta, block);
+}
+
+int nd_compressed_prefill(const void *q, const void *k, const void *v, int batch, int T, int n_q_heads,
+                          int n_kv_heads, int head_dim, int window, int block, int n_pinned, float rope_theta,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes, nd_stream_t stream) {
+  if (block < 1 || window < 1 || n_pinned < 0 || (T >= 0 && n_pinned > T)) return ND_ERR_INVALID_ARG;
+  return prefill_impl(q, k, v, ND_BF16, batch, T, n_q_heads, n_kv_heads, head_dim, nullptr, nullptr, window,
+                      rope_theta, nullptr, nullptr, block, n_pinned, out, lse, workspace, workspace_bytes, stream);
+}
+
 int nd_rope_apply(const void *x, void *y, int batch, int T, int n_heads, int head_dim,
                   float rope_theta, nd_stream_t stream) {
   if (batch < 0 || T < 0 || n_heads <= 0 || head_dim <= 0 || head_dim % 2) return ND_ERR_INVALID_ARG;
@@ -752,8 +776,8 @@ int nd_kv_compress_pool_rope(const void *k, const void *v, int batch, int T, int
   if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return ND_ERR_WORKSPACE;
   int st = check_device(nullptr);
   if (st != ND_OK) return st;
-  return finish(launch_pool_rope(k, v, k_rot, pooled_k, pooled_v, batch, T, n_heads, head_dim, block, rope_theta,
-                                 workspace, /*chained=*/false, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launch_pool_rope(k, v, k_rot, pooled_k, pooled_v, batch, T, n_heads, head_dim, block, 0,
+                                 rope_theta, workspace, /*chained=*/false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int nd_kv_budget_window(const nd_model_cfg *cfg, int *budget_out, int *effective_out) {

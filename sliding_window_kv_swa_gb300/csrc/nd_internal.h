@@ -122,10 +122,11 @@ cudaError_t launch_rope_qk(const void *q, void *q_out, int Hq, const void *k, vo
 
 // The compressed prefill's fused pass: the angle table (theta != 0) into
 // `table`, then one read of K and V writing K rotated at every position
-// (k_rot; nothing when theta == 0) and the pooled blocks (pooled K rotated
-// at the midpoint).  chained as in launch_rope_qk.
+// (k_rot; nothing when theta == 0) and the pooled blocks of positions pos0..
+// ((T - pos0) / block of them, pooled K rotated at the midpoint).  chained as
+// in launch_rope_qk.
 cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk, void *pv, int batch, int T,
-                             int n_heads, int head_dim, int block, float theta, void *table, bool chained,
+                             int n_heads, int head_dim, int block, int pos0, float theta, void *table, bool chained,
                              cudaStream_t stream);
 
 cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T, int n_heads,
@@ -149,6 +150,9 @@ struct PrefillArgs {
   // bf16 path: queries are key rows q_off .. T-1 (q, out and lse hold
   // T - q_off rows); 0 for an ordinary prefill
   int q_off = 0;
+  // compressed variant: keys 0 .. n_pinned-1 pinned, pooled blocks tile the
+  // positions after them ((T - n_pinned) / block of them)
+  int n_pinned = 0;
 };
 
 size_t prefill_plan_bytes(int batch, int T, int block);

@@ -92,6 +92,9 @@ struct TcParams {
   // queries are key rows q_off .. T-1 (Tq = T - q_off of them); q, out and lse
   // hold only those rows
   int q_off, Tq;
+  // compressed variant: keys 0 .. n_pinned-1 are pinned (visible at any
+  // distance) and the pooled blocks tile the positions after them
+  int n_pinned;
   const int32_t *seg;
   const uint8_t *sink;
   const int32_t *plan;
@@ -196,7 +199,8 @@ __global__ void __launch_bounds__(1024) tile_prep_kernel(TcParams p, TileMeta *m
     int32_t *out = plan + (size_t(b) * p.n_span + sp) * p.plan_stride;
     int n = 0;
     if (p.block > 0) {
-      const int lim = q1 - p.W + 1;  // pooled column j visible iff (j+1)*block <= q - W + 1
+      // pooled column j visible iff (j+1)*block <= q - W + 1 - n_pinned
+      const int lim = q1 - p.W + 1 - p.n_pinned;
       const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
       n = (ncol + BN - 1) / BN;
       for (int j = lane; j < n; j += 32) out[1 + j] = (1 << 20) | j;
@@ -221,7 +225,8 @@ __global__ void __launch_bounds__(1024) tile_prep_kernel(TcParams p, TileMeta *m
         bool keep = false;
         if (j <= jmax) {
           const bool in_window = p.W == 0 || (j + 1) * BN - 1 >= q0 - p.W + 1;
-          keep = t_lo[j] <= t_hi[j] && t_lo[j] <= qhi && t_hi[j] >= qlo && (in_window || t_any[j]);
+          const bool pinned = j * BN < p.n_pinned;  // holds a pinned key (compressed variant)
+          keep = t_lo[j] <= t_hi[j] && t_lo[j] <= qhi && t_hi[j] >= qlo && (in_window || t_any[j] || pinned);
         }
         const unsigned m = __ballot_sync(0xffffffffu, keep);
         if (keep) out[1 + n + __popc(m & ((1u << lane) - 1u))] = j;
@@ -971,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       unsigned long long vis;
       if (pooled) {
-        const int lim = q - p.W + 1;
+        const int lim = q - p.W + 1 - p.n_pinned;
         const int ncol = lim >= p.block ? min(lim / p.block, p.nb) : 0;
         vis = myseg > 0 ? prefix(ncol - 1 - k0) : 0ull;
       } else {
@@ -979,8 +984,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned long long window = lo <= 0 ? all1 : (lo > 63 ? 0ull : (all1 << lo));
         const unsigned long long causal = prefix(q - k0);
         if (kPooled) {
-          // no segment ids or sinks in the compressed variant
-          vis = myseg > 0 ? (causal & window) : 0ull;
+          // no segment ids in the compressed variant; keys below n_pinned
+          // are pinned (visible at any distance)
+          vis = myseg > 0 ? (causal & (window | prefix(p.n_pinned - 1 - k0))) : 0ull;
         } else {
           const TileMeta *f = meta_at(sm);
           const unsigned long long cw = causal & (window | f->sink_bits);
@@ -1206,7 +1212,8 @@ TcSetup tc_setup(const PrefillArgs &a, void *ws, int *err) {
   p.G = G;
   p.W = a.window;
   p.block = a.block;
-  p.nb = a.block > 0 ? a.T / a.block : 0;
+  p.n_pinned = a.block > 0 ? a.n_pinned : 0;
+  p.nb = a.block > 0 ? (a.T - p.n_pinned) / a.block : 0;
   p.n_span = S.pd.n_span;
   p.span = S.pd.span;
   p.n_kt = S.pd.n_kt;

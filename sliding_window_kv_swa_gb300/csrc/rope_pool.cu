@@ -269,10 +269,13 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
                                                         const uint16_t *__restrict__ v,
                                                         uint16_t *__restrict__ k_rot, uint16_t *__restrict__ pk,
                                                         uint16_t *__restrict__ pv, int T, int H, int D, int block,
-                                                        const float2 *__restrict__ cs) {
+                                                        int pos0, const float2 *__restrict__ cs) {
   pdl_wait();  // the angle table (or what the previous kernel wrote) is in
-  const int nblk = T / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ, tail = T - nblk * block;
-  const int per_seq = n_grp + (tail > 0 ? 1 : 0);
+  // blocks tile positions pos0 .. pos0 + nblk*block - 1; the positions
+  // before pos0 and past the last whole block are rotated by one more CTA
+  const int nblk = (T - pos0) / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
+  const int tail = T - pos0 - nblk * block, n_rest = pos0 + tail;
+  const int per_seq = n_grp + (n_rest > 0 ? 1 : 0);
   const int b = blockIdx.x / per_seq, grp = blockIdx.x % per_seq;
   const int half = D / 2, groups = half / 8;
   const size_t rstride = size_t(H) * D;
@@ -285,11 +288,12 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
       rope_pair(a[2 * q4 + 1], bb[2 * q4 + 1], w.z, w.w, ya[2 * q4 + 1], yb[2 * q4 + 1]);
     }
   };
-  if (grp == n_grp) {  // positions past the last whole block: K's rotation only
+  if (grp == n_grp) {  // positions outside the blocks: K's rotation only
     if (!cs) return;
-    for (int idx = threadIdx.x; idx < tail * H * groups; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < n_rest * H * groups; idx += blockDim.x) {
       const int g = idx % groups, rest = idx / groups;
-      const int h = rest % H, t = nblk * block + rest / H, i0 = g * 8;
+      const int h = rest % H, u = rest / H, i0 = g * 8;
+      const int t = u < pos0 ? u : pos0 + nblk * block + (u - pos0);
       const size_t row = (size_t(b) * T + t) * rstride + size_t(h) * D;
       float xa[8], xb[8], ya[8], yb[8];
       ld8(k + row + i0, xa);
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
     float sa[8], sb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) sa[e] = sb[e] = 0.f;
-    const size_t row0 = (size_t(b) * T + size_t(j) * block) * rstride + size_t(h) * D;
+    const size_t row0 = (size_t(b) * T + pos0 + size_t(j) * block) * rstride + size_t(h) * D;
     for (int r0 = 0; r0 < block; r0 += kPoolRows) {
       uint4 ra[kPoolRows], rb[kPoolRows];
 #pragma unroll
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
         if (cs && !is_v) {
           const size_t row = row0 + size_t(r0 + r) * rstride;
           float ya[8], yb[8];
-          rotate8(j * block + r0 + r, i0, xa, xb, ya, yb);
+          rotate8(pos0 + j * block + r0 + r, i0, xa, xb, ya, yb);
           st8(k_rot + row + i0, ya);
           st8(k_rot + row + i0 + half, yb);
         }
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
       ya[e] = sa[e];
       yb[e] = sb[e];
     }
-    if (cs && !is_v) rotate8(min(j * block + block / 2, T - 1), i0, sa, sb, ya, yb);
+    if (cs && !is_v) rotate8(min(pos0 + j * block + block / 2, T - 1), i0, sa, sb, ya, yb);
     uint16_t *y = is_v ? pv : pk;
     const size_t orow = ((size_t(b) * nblk + j) * H + h) * D;
     st8(y + orow + i0, ya);
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
 // is chained as in launch_rope_qk.  head_dim a multiple of 16, 16-byte
 // aligned tensors.
 cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk, void *pv, int batch, int T,
-                             int n_heads, int head_dim, int block, float theta, void *table, bool chained,
+                             int n_heads, int head_dim, int block, int pos0, float theta, void *table, bool chained,
                              cudaStream_t stream) {
   if (size_t(batch) * T == 0) return cudaSuccess;
   float2 *cs = nullptr;
@@ -381,12 +385,12 @@ cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk
                                half, fr, chained ? 0 : 1);
     if (e != cudaSuccess) return e;
   }
-  const int nblk = T / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
+  const int nblk = (T - pos0) / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
   const int per_seq = n_grp + (T - nblk * block > 0 ? 1 : 0);
   if (per_seq == 0) return cudaSuccess;
   return launch_pdl(pool_rope_kernel, dim3(unsigned(size_t(batch) * per_seq)), dim3(256), 0, stream,
                     static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), static_cast<uint16_t *>(k_rot),
-                    static_cast<uint16_t *>(pk), static_cast<uint16_t *>(pv), T, n_heads, head_dim, block,
+                    static_cast<uint16_t *>(pk), static_cast<uint16_t *>(pv), T, n_heads, head_dim, block, pos0,
                     static_cast<const float2 *>(cs));
 }
 

@@ -87,6 +87,8 @@ def _lib():
             "nd_swa_sink_prefill_workspace_size": (S, [I, I, I, I, I, I, F, I]),
             "nd_swa_sink_prefill": (I, [P, P, P, I, I, I, I, I, I, P, P, I, F, P, P, I, P, P, P, S, P]),
             "nd_swa_sink_prefill_tiles": (I, [P, I, I, I, I, I, F, I, P]),
+            "nd_compressed_prefill_workspace_size": (S, [I, I, I, I, I, F, I]),
+            "nd_compressed_prefill": (I, [P, P, P, I, I, I, I, I, I, I, I, F, P, P, P, S, P]),
             "nd_swa_sink_chunk_prefill_workspace_size": (S, [I, I, I, I, I, I, I, I]),
             "nd_swa_sink_chunk_prefill": (I, [P, P, P, I, P, I, I, P, P, P, S, P]),
             "nd_swa_sink_chunk_prefill_tiles": (I, [P, I, I, I, I, I, I, I, I, P]),
@@ -118,6 +120,7 @@ EXPORTED = ("nd_version", "nd_status_string", "nd_last_cuda_error", "nd_device_e
             "nd_compressed_decode_step_workspace_size", "nd_compressed_decode_step",
             "nd_swa_sink_prefill_workspace_size",
             "nd_swa_sink_prefill", "nd_swa_sink_prefill_tiles",
+            "nd_compressed_prefill_workspace_size", "nd_compressed_prefill",
             "nd_swa_sink_chunk_prefill_workspace_size", "nd_swa_sink_chunk_prefill",
             "nd_swa_sink_chunk_prefill_tiles",
             "nd_rope_apply", "nd_kv_compress_pool", "nd_kv_compress_pool_rope_workspace_size",
@@ -460,6 +463,31 @@ def nd_swa_sink_prefill_tiles(workspace: torch.Tensor, batch: int, T: int, n_q_h
     _check("nd_swa_sink_prefill_tiles", _lib().nd_swa_sink_prefill_tiles(
         _ptr(workspace), batch, T, n_q_heads, n_kv_heads, head_dim, float(rope_theta), int(block), ctypes.byref(n)))
     return n.value
+
+
+def nd_compressed_prefill_workspace_size(batch: int, T: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                                         rope_theta: float, block: int) -> int:
+    return int(_lib().nd_compressed_prefill_workspace_size(batch, T, n_q_heads, n_kv_heads, head_dim,
+                                                           float(rope_theta), int(block)))
+
+
+def nd_compressed_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int, block: int,
+                          n_pinned: int = 0, rope_theta: float = 0.0, out: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """Compressed attention with a pinned prefix of n_pinned exact keys (bf16
+    q [B, T, Hq, d], k / v [B, T, Hkv, d] before rotation); returns out."""
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = nd_compressed_prefill_workspace_size(B, T, Hq, Hkv, d, rope_theta, block)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    _check("nd_compressed_prefill", _lib().nd_compressed_prefill(
+        _ptr(q), _ptr(k), _ptr(v), B, T, Hq, Hkv, d, int(window), int(block), int(n_pinned), float(rope_theta),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
 
 
 def nd_swa_sink_chunk_prefill_workspace_size(batch: int, chunk: int, n_q_heads: int, n_kv_heads: int,

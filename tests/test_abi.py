@@ -118,6 +118,15 @@ def test_host_validation_before_any_device_work():
     assert need >= (1 + 2 * 12) * 4
     assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, P(16), None, None, Z(need), None) == 4
     assert fill(ctypes.byref(cache), P(16), P(16), 1, 8, None, None, P(16), None, W16, Z(need - 16), None) == 4
+    # pinned compressed prefill: block >= 1, window >= 1, 0 <= n_pinned <= T
+    cp = lib.nd_compressed_prefill
+    cp.restype = ctypes.c_int
+    cargs = lambda win, blk, pin: (P(16), P(16), P(16), 1, 8, 4, 4, 64, win, blk, pin, ctypes.c_float(1e4), P(16),
+                                   None, P(16), ctypes.c_size_t(1 << 20), None)
+    assert cp(*cargs(8, 0, 0)) == 1
+    assert cp(*cargs(0, 4, 0)) == 1
+    assert cp(*cargs(8, 4, 9)) == 1
+    assert cp(*cargs(8, 4, -1)) == 1
     # chunked prefill: window >= 1, a ring, GQA ratio, head_dim 64/128, workspace
     chunk = lib.nd_swa_sink_chunk_prefill
     chunk.restype = ctypes.c_int
@@ -211,6 +220,8 @@ def test_empty_problems_return_ok_without_a_device():
         "nd_kv_quant_rows": (None, ctypes.c_int64(0), 64, None, None, None),
         "nd_kv_cache_from_prefill": (e, None, None, 1, 16, None, None, None, None, None, Z(0), None),
         "nd_swa_sink_chunk_prefill": (None, None, None, 16, e, 4, 8, None, None, None, Z(0), None),
+        "nd_compressed_prefill": (None, None, None, 0, 16, 4, 4, 64, 8, 4, 2, F(10000.0), None, None, None, Z(0),
+                                  None),
         "nd_swa_sink_decode": (None, e, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step": (None, e, None, None, 4, 8, None, None, None, Z(0), None),
         "nd_swa_sink_decode_step_host": (None, e, None, None, 4, 8, None, None, None, Z(0), None),

@@ -54,3 +54,17 @@ def test_rows_cover_every_measured_configuration():
                                    "append", "fill", "cdecode", "wsweep"}
     r = bench.roofline("hbm", 6e9, 1.0, 6000.0, "GB/s", "k", "measured")
     assert abs(r["achieved"] - 6000.0) < 1e-9 and abs(r["frac"] - 1.0) < 1e-12
+
+
+def test_visible_pairs_pinned_matches_the_oracle_mask():
+    """The pinned compressed row's visible pairs equal the oracle's: with
+    q = 0 every visible column scores 0, so each row's lse is the log of its
+    visible column count."""
+    import oracle
+    rng = philox(78)
+    for T, W, b, P in ((64, 8, 4, 5), (100, 17, 3, 0), (53, 6, 2, 53), (300, 40, 8, 100)):
+        q = np.zeros((1, T, 1, 32))
+        k, v = (rng.standard_normal((1, T, 1, 32)) for _ in range(2))
+        _, lse = oracle.compressed_prefill_pinned(q, k, v, W, b, P, 0.0)
+        n = int(np.rint(np.exp(lse)).sum())
+        assert bench.visible_pairs_pinned(T, W, b, P) == n

@@ -424,3 +424,30 @@ def test_compressed_prefill_pooling_inside_the_call(T, W, block, d, H):
     if T < 4096:
         want, _ = oracle.compressed_prefill(q, k, v, W, block, 10000.0)
         assert_close_bf16(host(b), want, "pooling inside the call")
+
+
+@pytest.mark.parametrize("T,W,block,P,d,H", [(300, 16, 4, 5, 64, 4), (513, 40, 8, 64, 128, 2), (129, 1, 2, 0, 64, 3),
+                                             (700, 64, 4, 100, 64, 4), (200, 30, 3, 200, 128, 2),
+                                             (4096, 256, 4, 512, 64, 16)])
+def test_compressed_prefill_with_pinned_prefix(T, W, block, P, d, H):
+    """nd_compressed_prefill: the first P keys pinned (visible at any
+    distance), pooled blocks over the positions after them, the exact window;
+    every row (the 4096-token case: every row of the one sequence) against
+    the oracle; without pins, the same bits as the compressed
+    nd_swa_sink_prefill."""
+    rng = philox(1990 + T + P + d)
+    B = 2 if T < 4096 else 1
+    qb, q = normal_bf16(rng, (B, T, H, d))
+    kb, k = normal_bf16(rng, (B, T, H, d))
+    vb, v = normal_bf16(rng, (B, T, H, d))
+    lib = nd()
+    q_d, k_d, v_d = dev_bf16(qb), dev_bf16(kb), dev_bf16(vb)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    out = lib.nd_compressed_prefill(q_d, k_d, v_d, W, block, n_pinned=P, rope_theta=10000.0, lse=lse)
+    want, wlse = oracle.compressed_prefill_pinned(q, k, v, W, block, P, 10000.0)
+    assert_close_bf16(host(out), want, f"pinned {P}")
+    np.testing.assert_allclose(host(lse).transpose(0, 2, 1), wlse, atol=2e-2, rtol=0)
+    if P == 0:
+        ref = lib.nd_swa_sink_prefill(q_d, k_d, v_d, None, None, W, rope_theta=10000.0, block=block)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

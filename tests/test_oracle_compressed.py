@@ -286,3 +286,48 @@ def test_pinned_tokens_are_seen_at_any_distance():
     a, _, _ = oracle.compressed_decode(q[:, W + 1], k, v, W + 1, W, b, 1e4)
     c_, _, _ = oracle.compressed_decode(q[:, W + 1], k, v2, W + 1, W, b, 1e4)
     np.testing.assert_array_equal(a, c_)
+
+
+# ---------------------------------------------------------------- pinned prefix + compressed prefill
+
+@pytest.mark.parametrize("theta", [0.0, 10000.0])
+def test_pinned_compressed_prefill_without_pins_is_the_compressed_prefill(theta):
+    rng = philox(90)
+    B, T, H, d, W, b = 2, 53, 2, 16, 7, 4
+    q, k, v = (rng.standard_normal((B, T, H, d)) for _ in range(3))
+    got, gl = oracle.compressed_prefill_pinned(q, k, v, W, b, 0, theta)
+    want, wl = oracle.compressed_prefill(q, k, v, W, b, theta)
+    np.testing.assert_allclose(got, want, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(gl, wl, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("P", [1, 6, 40])
+def test_pinned_compressed_prefill_block_one_is_causal_attention(P):
+    """Block 1: pinned keys, single-token blocks at their own positions and the
+    window cover every causal key once -- plain causal attention (SDPA)."""
+    rng = philox(91 + P)
+    B, T, H, d, W = 1, 40, 2, 16, 5
+    q, k, v = (rng.standard_normal((B, T, H, d)) for _ in range(3))
+    got, _ = oracle.compressed_prefill_pinned(q, k, v, W, 1, P, 10000.0)
+    pos = np.arange(T)
+    qr, kr = oracle.rope(q, pos, 1e4), oracle.rope(k, pos, 1e4)
+    tq, tk, tv = (torch.from_numpy(a).permute(0, 2, 1, 3) for a in (qr, kr, v))
+    want = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True).permute(0, 2, 1, 3).numpy()
+    np.testing.assert_allclose(got, want, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("P", [0, 5])
+def test_pinned_compressed_prefill_rows_match_the_compressed_decode(P):
+    """Every row of the prefill equals the compressed decode at that position
+    (the same reading of pinned + pooled + window) within the int8 storage
+    error of the decode's cache."""
+    rng = philox(95 + P)
+    B, T, H, d, W, b = 2, 46, 2, 64, 6, 4
+    q, k, v = (rng.standard_normal((B, T, H, d)) for _ in range(3))
+    pre, _ = oracle.compressed_prefill_pinned(q, k, v, W, b, P, 1e4)
+    errs = []
+    for t in range(T):
+        out, _, _ = oracle.compressed_decode(q[:, t], k, v, t, W, b, 1e4, n_pinned=P)
+        errs.append(np.abs(out - pre[:, t]))
+    errs = np.stack(errs)
+    assert errs.max() <= QMAX and errs.mean() <= QMEAN, (errs.max(), errs.mean())
