@@ -244,13 +244,14 @@ ND_API int nd_swa_sink_decode_step(const void *q, const nd_kv_cache *cache,
 /*
  * nd_swa_sink_decode_step with the step's inputs and outputs in host memory,
  * for a caller whose token and query live on the host: the call enqueues on
- * `stream` the copies of q, k_new and v_new to the device, the step exactly
- * as nd_swa_sink_decode_step, and the copies of out (and lse, when lse_host
- * is not NULL) back to the host.  The host results are valid once the stream
- * has passed the call (synchronise the stream, or an event recorded after the
- * call).  Page-locked, 16-byte aligned host buffers are copied by a kernel
- * over the host link (one launch per direction); other host memory by one
- * cudaMemcpyAsync per buffer, synchronous for pageable memory.
+ * `stream` the step exactly as nd_swa_sink_decode_step, reading q, k_new and
+ * v_new from the host and writing out (and lse, when lse_host is not NULL)
+ * to it.  The host results are valid once the stream has passed the call
+ * (synchronise the stream, or an event recorded after the call).
+ * Page-locked, 16-byte aligned host buffers are read and written in place
+ * by the step's kernels over the host link (no copies); other host memory
+ * is staged in the workspace by one cudaMemcpyAsync per buffer each way
+ * (synchronous for pageable memory).
  *   q_host, out_host        bf16 [batch][n_q_heads][head_dim], host memory
  *   k_new_host, v_new_host  bf16 [batch][n_kv_heads][head_dim], host memory
  *   lse_host                fp32 [batch][n_q_heads], host memory, or NULL
@@ -271,18 +272,19 @@ ND_API int nd_swa_sink_decode_step_host(const void *q_host, const nd_kv_cache *c
                                         size_t workspace_bytes, nd_stream_t stream);
 
 /*
- * nd_swa_sink_decode_step_host with the step's host buffers packed, so each
- * direction is one copy (each copy pays a fixed latency of a few
- * microseconds, which dominates a step of this size):
+ * nd_swa_sink_decode_step_host with the step's host buffers packed (one
+ * allocation each way: one page-locked lookup each, or one copy each for
+ * memory that has to be staged):
  *   in_host   one host allocation holding, back to back,
  *             q     bf16 [batch][n_q_heads][head_dim],
  *             k_new bf16 [batch][n_kv_heads][head_dim],
  *             v_new bf16 [batch][n_kv_heads][head_dim]
  *   out_host  one host allocation holding out bf16 [batch][n_q_heads][head_dim]
  *             followed, when with_lse != 0, by lse fp32 [batch][n_q_heads]
- * (one allocation each: a copy may not span two page-locked allocations that
- * merely sit next to each other).  Workspace, stream semantics and errors as
- * nd_swa_sink_decode_step_host; the workspace size is the same query.
+ * (one allocation each: an access may not span two page-locked allocations
+ * that merely sit next to each other).  Workspace, stream semantics and
+ * errors as nd_swa_sink_decode_step_host; the workspace size is the same
+ * query.
  */
 ND_API int nd_swa_sink_decode_step_host_packed(const void *in_host, const nd_kv_cache *cache,
                                                int n_q_heads, int window, void *out_host,

@@ -32,8 +32,9 @@
 //          (max, sum, O) partials that a combine kernel merges.
 // The kernel is a dependent launch: it may be scheduled while the previous
 // kernel on the stream runs, and waits for it before its first global read.
-// Also here: the copy kernel the host-buffer step uses to move its inputs and
-// outputs between page-locked host memory and the device.
+// q, k_new / v_new and out / lse may be page-locked host memory (the
+// host-buffer step passes its buffers in place): every access to them is an
+// ordinary load or store.
 #include <atomic>
 
 #include "nd_common.cuh"
@@ -723,49 +724,6 @@ cudaError_t launch_decode(const void *q, const nd_kv_cache &c, int n_q_heads, in
     return ctas >= kManyPairs64 ? launch_d<64, 4, 4>(p, grid, stream) : launch_d<64, 4>(p, grid, stream);
   }
   return cudaErrorInvalidValue;
-}
-
-// ------------------------------------------------------------------ host copies
-// Copies between page-locked host memory and device memory done by a kernel
-// (loads and stores over the host link) rather than the copy engines: for the
-// few tens of KB a decode step moves, a copy engine's fixed latency is the
-// larger cost.  Up to three (src, dst, bytes) segments, one per grid row;
-// 16-byte chunks, the last bytes of a segment by single bytes.  A dependent
-// launch: it waits for the kernel before it (which may read the destination
-// or write the source) before it touches either.
-namespace {
-struct CopySegs {
-  const uint8_t *src[3];
-  uint8_t *dst[3];
-  size_t bytes[3];
-};
-__global__ void __launch_bounds__(256) copy_segments_kernel(const CopySegs c) {
-  pdl_wait();
-  const int sg = blockIdx.y;
-  const size_t n = c.bytes[sg], n16 = n / 16;
-  const uint4 *src = reinterpret_cast<const uint4 *>(c.src[sg]);
-  uint4 *dst = reinterpret_cast<uint4 *>(c.dst[sg]);
-  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += size_t(gridDim.x) * blockDim.x)
-    dst[i] = src[i];
-  if (blockIdx.x == 0 && threadIdx.x < n - n16 * 16) c.dst[sg][n16 * 16 + threadIdx.x] = c.src[sg][n16 * 16 + threadIdx.x];
-}
-}  // namespace
-
-cudaError_t launch_copy_segments(int n, const void *const *src, void *const *dst, const size_t *bytes,
-                                 cudaStream_t stream) {
-  if (n < 1 || n > 3) return cudaErrorInvalidValue;
-  CopySegs c = {};
-  size_t most = 0;
-  for (int i = 0; i < n; ++i) {
-    c.src[i] = static_cast<const uint8_t *>(src[i]);
-    c.dst[i] = static_cast<uint8_t *>(dst[i]);
-    c.bytes[i] = bytes[i];
-    most = bytes[i] > most ? bytes[i] : most;
-  }
-  size_t blocks = (most / 16 + 255) / 256;
-  if (blocks < 1) blocks = 1;
-  if (blocks > 1024) blocks = 1024;
-  return launch_pdl(copy_segments_kernel, dim3(unsigned(blocks), unsigned(n)), dim3(256), 0, stream, c);
 }
 
 }  // namespace nd

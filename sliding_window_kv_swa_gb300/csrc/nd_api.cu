@@ -310,10 +310,11 @@ static void *mapped_host(const void *p) {
 }
 
 // The host-buffer step.  packed_in: q_host holds q, k_new, v_new back to
-// back (one copy); packed_out: lse follows out in out_host (one copy).
-// Page-locked, 16-byte aligned host buffers move by copy kernels over the
-// host link (a few microseconds less per copy than a copy engine at these
-// sizes); any other host memory by cudaMemcpyAsync.
+// back; packed_out: lse follows out in out_host.  Page-locked, 16-byte
+// aligned host buffers are read (q, k_new, v_new) and written (out, lse) in
+// place by the step's own kernels over the host link -- no copy launches
+// and no staging; any other host memory is staged in the workspace by
+// cudaMemcpyAsync (one copy per buffer each way).
 static int decode_step_host(const void *q_host, const nd_kv_cache *cache, const void *k_new_host,
                             const void *v_new_host, bool packed_in, int n_q_heads, int window,
                             void *out_host, float *lse_host, bool packed_out, void *workspace,
@@ -330,60 +331,62 @@ static int decode_step_host(const void *q_host, const nd_kv_cache *cache, const 
   char *ws = static_cast<char *>(workspace);
   const size_t qb = size_t(B) * n_q_heads * d * 2, kb = size_t(B) * Hkv * d * 2;
   const size_t lb = size_t(B) * n_q_heads * sizeof(float);
-  cudaError_t e;
-  const void *src[3];
-  void *dst[3];
-  size_t nb[3];
-  int nseg = 0;
-  {
-    const void *hin[3] = {q_host, k_new_host, v_new_host};
-    const size_t off[3] = {L.q, L.kn, L.vn}, len[3] = {packed_in ? qb + 2 * kb : qb, kb, kb};
-    for (int i = 0; i < (packed_in ? 1 : 3); ++i) {
-      void *dp = mapped_host(hin[i]);
-      if (!dp || !aligned16(dp)) {
-        nseg = -1;
-        break;
-      }
-      src[nseg] = dp;
-      dst[nseg] = ws + off[i];
-      nb[nseg++] = len[i];
+  // device-addressable host buffers (NULL: not page-locked or not 16-byte
+  // aligned -- staged instead)
+  auto direct = [](const void *h) -> char * {
+    void *dp = mapped_host(h);
+    return dp && aligned16(dp) ? static_cast<char *>(dp) : nullptr;
+  };
+  cudaError_t e = cudaSuccess;
+  // inputs: q, k_new, v_new (qb and kb are multiples of 128 bytes, so the
+  // packed pieces stay 16-byte aligned)
+  const char *qd, *kd, *vd;
+  if (packed_in) {
+    const char *in = direct(q_host);
+    if (!in) {
+      e = cudaMemcpyAsync(ws + L.q, q_host, qb + 2 * kb, cudaMemcpyHostToDevice, s);
+      in = ws + L.q;
     }
-  }
-  if (nseg > 0) {
-    e = launch_copy_segments(nseg, src, dst, nb, s);
-  } else if (packed_in) {
-    e = cudaMemcpyAsync(ws + L.q, q_host, qb + 2 * kb, cudaMemcpyHostToDevice, s);
+    qd = in, kd = in + qb, vd = in + qb + kb;
   } else {
-    e = cudaMemcpyAsync(ws + L.q, q_host, qb, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.kn, k_new_host, kb, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.vn, v_new_host, kb, cudaMemcpyHostToDevice, s);
+    const void *h[3] = {q_host, k_new_host, v_new_host};
+    const size_t off[3] = {L.q, L.kn, L.vn}, len[3] = {qb, kb, kb};
+    const char *dd[3];
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+      dd[i] = direct(h[i]);
+      if (!dd[i]) {
+        e = cudaMemcpyAsync(ws + off[i], h[i], len[i], cudaMemcpyHostToDevice, s);
+        dd[i] = ws + off[i];
+      }
+    }
+    qd = dd[0], kd = dd[1], vd = dd[2];
   }
   if (e != cudaSuccess) return finish(e);
+  // outputs: out and (optional) lse, written in place or staged
   const bool want_lse = packed_out || lse_host;
-  float *lse_dev = want_lse ? reinterpret_cast<float *>(ws + L.lse) : nullptr;
-  st = decode_step_device(ws + L.q, cache, ws + L.kn, ws + L.vn, n_q_heads, window, ws + L.out, lse_dev,
-                          ws + L.split, workspace_bytes - L.split, s);
-  if (st != ND_OK) return st;
-  nseg = 0;
-  {
-    void *hout[2] = {out_host, packed_out ? nullptr : lse_host};
-    const size_t off[2] = {L.out, L.lse}, len[2] = {packed_out ? qb + lb : qb, lb};
-    for (int i = 0; i < 2; ++i) {
-      if (!hout[i]) continue;
-      void *dp = mapped_host(hout[i]);
-      if (!dp || !aligned16(dp)) {
-        nseg = -1;
-        break;
-      }
-      src[nseg] = ws + off[i];
-      dst[nseg] = dp;
-      nb[nseg++] = len[i];
+  char *od = direct(out_host);
+  const bool out_direct = od != nullptr;
+  float *ld = nullptr;
+  bool lse_direct = false;
+  if (packed_out) {
+    if (!out_direct) od = ws + L.out;  // L.lse follows L.out: out | lse stay back to back
+    ld = reinterpret_cast<float *>(od + qb);
+    lse_direct = out_direct;
+  } else {
+    if (!out_direct) od = ws + L.out;
+    if (lse_host) {
+      char *lp = direct(lse_host);
+      lse_direct = lp != nullptr;
+      ld = reinterpret_cast<float *>(lse_direct ? lp : ws + L.lse);
     }
   }
-  if (nseg > 0) return finish(launch_copy_segments(nseg, src, dst, nb, s));
-  e = cudaMemcpyAsync(out_host, ws + L.out, packed_out ? qb + lb : qb, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && lse_host && !packed_out)
-    e = cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, s);
+  st = decode_step_device(qd, cache, kd, vd, n_q_heads, window, od, want_lse ? ld : nullptr, ws + L.split,
+                          workspace_bytes - L.split, s);
+  if (st != ND_OK) return st;
+  if (!out_direct)
+    e = cudaMemcpyAsync(out_host, od, packed_out ? qb + lb : qb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && lse_host && !packed_out && !lse_direct)
+    e = cudaMemcpyAsync(lse_host, ld, lb, cudaMemcpyDeviceToHost, s);
   return finish(e);
 }
 

@@ -96,12 +96,6 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Kernel copy of n (1..3) segments (16-byte aligned addresses; any byte
-// count), e.g. between page-locked host memory and device memory; a
-// dependent launch.
-cudaError_t launch_copy_segments(int n, const void *const *src, void *const *dst, const size_t *bytes,
-                                 cudaStream_t stream);
-
 // theta^(-2i/head_dim) for i < head_dim/2, in double (head_dim <= 256).
 constexpr int kMaxHalf = 128;
 struct Freqs {

@@ -302,7 +302,7 @@ def test_decode_step_matches_append_then_decode(B, Hq, Hkv, d, S, W, fill):
     (64, 8, 2, 64, 64, 256, True),    # packed host buffers: one copy each way
     (10, 32, 8, 128, 64, 32, False),  # append and decode as two launches
     (10, 32, 8, 128, 64, 32, True),
-    (3, 3, 1, 64, 8, 16, False),      # lse of 36 bytes: the copy kernels' byte tail
+    (3, 3, 1, 64, 8, 16, False),      # lse of 36 bytes, written in place
     (3, 3, 1, 64, 8, 16, True),
 ])
 def test_decode_step_host_buffers(B, Hq, Hkv, d, S, W, packed):
@@ -385,9 +385,9 @@ def test_decode_steps_back_to_back(B, Hq, Hkv, d, S, W):
 
 
 def test_decode_steps_host_packed_back_to_back():
-    """The packed host-buffer step (copy kernels, the step, copy kernels) for
-    several steps without synchronisation in between: the staging area in
-    the workspace is reused by every step."""
+    """The packed host-buffer step (the step's kernels read and write the
+    page-locked buffers in place) for several steps without synchronisation
+    in between, each step on its own buffers."""
     B, Hq, Hkv, d, S, W = 64, 8, 2, 64, 64, 256
     w = decode_cache(B, Hq, Hkv, d, S, W, seed=795, full=True)
     ref = oracle_cache(w, S, W)
@@ -416,7 +416,7 @@ def test_decode_steps_host_packed_back_to_back():
 @pytest.mark.parametrize("packed", [False, True])
 def test_decode_step_host_pageable_and_no_lse(packed):
     """Host buffers that are not page-locked take the copy-engine path
-    (cudaMemcpyAsync) instead of the copy kernels; the packed form without
+    (cudaMemcpyAsync) instead of being accessed in place; the packed form without
     lse copies the output alone.  Same results as the oracle either way."""
     B, Hq, Hkv, d, S, W = 8, 8, 2, 64, 16, 48
     w = decode_cache(B, Hq, Hkv, d, S, W, seed=798 + packed, full=True)
