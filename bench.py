@@ -321,10 +321,11 @@ def bench_decode(torch, nd, B, Hq, Hkv, d, S, W, steps, warmup, seed, pk, dist=N
 
 def e2e_decode(torch, nd, state, B, Hq, Hkv, d, S, W, steps, warmup, n_buffers=8):
     """The same step through the public API with host buffers: one
-    nd_swa_sink_decode_step_host_packed call per step, which enqueues the
-    copy of the step's query and new token from page-locked host memory, the
-    append + decode, and the copy of the output back; all inside the timed
-    region.  The steps walk the same cache replicas as the timed step."""
+    nd_swa_sink_decode_step_host_packed call per step on page-locked host
+    memory.  The step's kernels read the query and new token and write the
+    output over the host link in place, so every input and output byte
+    crosses it inside the timed region.  The steps walk the same cache
+    replicas as the timed step."""
     reps, _ = state
     nq, nk = B * Hq * d, B * Hkv * d
     ins, outs = [], []
@@ -408,7 +409,8 @@ def bench_compressed_decode(torch, nd, steps, warmup, pk, dist=None, B=128, H=16
                        f"pooled blocks (b{block}) + {W} exact keys, int8 g32, RoPE; append + incremental pooling",
                 ms_per_step=t, bytes_per_step=per_step, replicas=replicas, launches=(3 if split else 2) * steps,
                 roofline=roofline("hbm", per_step, t, pk["hbm"], "GB/s",
-                                  "compressed_append_kernel + decode_kernel (whole step)", pk["src"]))
+                                  "compressed_append_kernel + decode_kernel (whole step)", pk["src"],
+                                  load_traffic(f"compressed_decode@b{B}")))
 
 
 def bench_window_sweep(torch, nd, steps, warmup, pk, dist, windows=(160, 256, 512, 1024), B=128):
@@ -522,7 +524,8 @@ def bench_chunk(torch, nd, steps, warmup, pk, dist=None, B=8, Tc=4096, Hq=32, Hk
                 algorithmic=roofline("tensor", flops, t, pk["bf16"], "TFLOP/s", "whole call (visible pairs)",
                                      pk["src"]),
                 roofline=roofline("tensor", tile_flops, t, pk["bf16"], "TFLOP/s",
-                                  "whole call (tiles the attention kernel's plan performed)", pk["src"]),
+                                  "whole call (tiles the attention kernel's plan performed)", pk["src"],
+                                  load_traffic(f"chunk_prefill@b{B}")),
                 launches=4 * steps)
 
 
@@ -681,7 +684,7 @@ def bench_tiny_fp32(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None):
         res[name] = dict(ms_per_call=t, visible_pairs=pairs, tok_s=512 / (t * 1e-3), oracle=orow,
                          roofline=roofline("alu", flops, t, alu_fp32_peak_tflops(), "TFLOP/s",
                                            "prefill_simt_kernel (fp32 FFMA)", "derived: 152 SMs x 128 FP32 lanes x "
-                                           "2 flops x 2.07 GHz"))
+                                           "2 flops x 2.07 GHz", load_traffic(f"prefill_simt@tiny_{name}")))
     return dict(config="tiny prefill B1 T512 Hq4 Hkv1 d64 fp32, 48-token sink prefix, W256", **res)
 
 
@@ -838,7 +841,7 @@ def bench_fill(torch, nd, steps, warmup, pk, dist=None, S=512, W=256):
                        f"into {S} sink + {W} ring slots per segment", ms_per_launch=t, kept_tokens=kept,
                 bytes_per_launch=per, replicas=replicas,
                 roofline=roofline("hbm", per, t, pk["hbm"], "GB/s", "kv_fill_plan_kernel + kv_fill_kernel",
-                                  pk["src"]))
+                                  pk["src"], load_traffic("cache_handoff@packed")))
 
 
 # ----------------------------------------------------------------------------
