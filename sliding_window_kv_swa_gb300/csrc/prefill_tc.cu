@@ -23,14 +23,17 @@
 //                    domain; bf16 P(g) goes back into TMEM over the front of
 //                    S(g)'s buffer (already read out).
 //   warp 8         : TMA loader: Q (two buffers), K tiles (freed as soon as
-//                    both blocks' S MMAs have read them) and the exact tiles'
-//                    segment / sink records (cp.async, freed once the
-//                    softmax warps have built their masks); at d = 64 also V.
+//                    both blocks' S MMAs have read them) and, for the packing
+//                    mask, the tiles' segment / sink records (cp.async, freed
+//                    once the softmax warps have built their masks); at
+//                    d = 64 also V.
 //   warps 9, 10    : one MMA issuer per row block: S(g) = Q K(g)^T (M128
-//                    N64) into S buffer g % NS once PV(g - NS) has read the P
-//                    it held, then O += P(g-1) V(g-1) (M128, N=d, P read from
-//                    TMEM, V an MN-major shared operand), so neither block
-//                    waits behind the other's.
+//                    N64) into S buffer g % NS, then O += P(g-1) V(g-1)
+//                    (M128, N=d, P read from TMEM, V an MN-major shared
+//                    operand), so neither block waits behind the other's.
+//                    The MMAs one thread issues run in issue order, so S(g)
+//                    needs no wait for PV(g - NS), the last reader of the P
+//                    its buffer held.
 //   warp 11        : V loader at d = 128 (V tiles, freed after both blocks'
 //                    PV); idle at d = 64.
 //   warps 12-15    : epilogue: rotate the next item's Q in shared memory
@@ -41,7 +44,10 @@
 // O accumulates in TMEM; a row's O is rescaled (TMEM load / multiply / store)
 // only when its running max grows by more than 2^8, so most tiles touch O
 // only through the MMA.  Tiles every row of a warp fully sees skip the
-// per-element mask.  Every mbarrier wait is bounded; a wait that gives up
+// per-element mask; tiles no row of a warp sees skip the scores and the
+// softmax and store a zero P.  Waits first probe the barrier without
+// blocking (a completed phase costs tens of cycles that way, against
+// hundreds for the blocking try_wait).  Every mbarrier wait is bounded; a wait that gives up
 // raises the device error flag and a shared abort flag, and all roles then run
 // to the common exit, which frees TMEM.
 #include <cuda.h>
@@ -386,6 +392,10 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Bounded wait that also gives up at once when another role already did.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
                                               volatile int *abort_flag) {
+  // A phase that has already completed is seen by the non-blocking probe in
+  // tens of cycles; try_wait costs hundreds even then, so it is only the
+  // fallback for a phase still in progress.
+  if (mbar_test_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_flag) return false;
@@ -437,8 +447,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // Bounded like wait_or_abort: at most kWaitLimit / 64 polls of at most 2 us.
 __device__ __forceinline__ bool warp_wait_sleep(uint64_t *bar, uint32_t parity, int *err,
                                                 volatile int *abort_flag) {
-  bool ok = false;
-  for (uint32_t i = 0; i < kWaitLimit / 64; ++i) {
+  bool ok = mbar_test_wait(bar, parity);
+  for (uint32_t i = 0; i < kWaitLimit / 64 && !ok; ++i) {
     if (mbar_try_wait_sleep(bar, parity)) {
       ok = true;
       break;
@@ -468,8 +478,9 @@ struct Lay {
   static constexpr int oM = oV + NV * kKV;         // TileMeta[NM stages]
   static constexpr int kBytes = oM + NM * int(sizeof(TileMeta)) + 1024;  // + alignment slack
   static_assert(NM >= NK, "tile records ride with K tiles");
-  // S buffers per block: P(g) is written over the front of S(g)'s buffer, so
-  // S(g + NS) waits for PV(g); at d = 64 three fit beside O
+  // S buffers per block: P(g) is written over the front of S(g)'s buffer,
+  // which S(g + NS) reuses once PV(g) (issued before it) has read P(g); at
+  // d = 64 three fit beside O
   static constexpr int NS = D == 64 ? 3 : 2;
   // TMEM columns: S[block][NS buffers] (BN fp32 each; P(g), BN/2 columns of
   // bf16 pairs, overwrites the front of S(g)'s buffer), O[block] (D fp32 each)
@@ -661,17 +672,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool pooled = kPooled && ((e >> 20) & 1);
         const int jt = e & 0xFFFFF;
         const int g = gt + j, st = g % NK, sm = g % NM;
-        if (!((g < NK || lwait(&k_empty[st], ((g / NK) - 1) & 1)) && (g < NM || lwait(&m_empty[sm], ((g / NM) - 1) & 1))))
+        if (!((g < NK || lwait(&k_empty[st], ((g / NK) - 1) & 1)) &&
+              (kPooled || g < NM || lwait(&m_empty[sm], ((g / NM) - 1) & 1))))
           return false;
         expect_tx(&k_full[st], L::kKV, leader);
         for (int x = 0; x < L::kBoxes; ++x)
           tma_load_4d(sK(st) + x * BN * 128, pooled ? &tm_pk : &tm_k, 64 * x, I.hk, jt * BN, I.b, &k_full[st], leader);
-        // the exact tile's record (384 bytes) rides along asynchronously;
-        // pooled tiles need none, but every lane still arrives
-        constexpr int kChunks = int(sizeof(TileMeta)) / 16;
-        if (!pooled && lane < kChunks)
-          cp_async16(sM(sm) + lane * 16, reinterpret_cast<const char *>(p.meta + size_t(I.b) * p.n_kt + jt) + lane * 16);
-        cp_async_arrive(&m_full[sm]);
+        // the tile's record (384 bytes) rides along asynchronously; the
+        // compressed variant's masks need none
+        if constexpr (!kPooled) {
+          constexpr int kChunks = int(sizeof(TileMeta)) / 16;
+          if (lane < kChunks)
+            cp_async16(sM(sm) + lane * 16, reinterpret_cast<const char *>(p.meta + size_t(I.b) * p.n_kt + jt) + lane * 16);
+          cp_async_arrive(&m_full[sm]);
+        }
         __syncwarp();
         return true;
       };
@@ -707,9 +721,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma0 || warp == kWarpMma0 + 1) {
     // ------------------------------------------------ MMA issuers, one per block
     //   Per tile g of the block (g: running tile count over its items):
-    //   S(g) = Q K(g)^T into S buffer g&1 once PV(g-2) has read the P that
-    //   buffer held and K(g) has landed; then O += P(g-1) V(g-1) once P(g-1)
-    //   is in TMEM and V(g-1) has landed.
+    //   S(g) = Q K(g)^T into S buffer g % NS once K(g) has landed; then
+    //   O += P(g-1) V(g-1) once P(g-1) is in TMEM and V(g-1) has landed.
     const int rb = warp - kWarpMma0;
     const uint32_t leader = elect_one();
     constexpr uint32_t kIdS = idesc_bf16(BM, BN, 0);
@@ -717,9 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int gt = 0, used = 0;  // used: items so far whose O went through TMEM
     // PV(g) is issued after S(g + 1), also across items (the next item's
-    // first S goes out before this item's last PV).  S(g) waits for
-    // PV(g - NS), issued NS - 1 iterations earlier: with NS = 3 that wait
-    // has a tile of slack, with NS = 2 it follows the PV just issued.
+    // first S goes out before this item's last PV).  PV(g - NS), the last
+    // reader of the buffer S(g) overwrites, was issued NS - 1 iterations
+    // earlier by this thread.
     constexpr int kLag = 1;
     int pv_g[2] = {-1, -1}, pv_first[2] = {0, 0}, pv_ofree[2] = {-1, -1};  // pending PVs, oldest first
     int npend = 0;
@@ -731,9 +744,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       --npend;
       // an item's first PV overwrites O: the epilogue warps must have read
       // out the O of the previous item that used it
-      ok = (ofree < 0 || warp_wait(&o_free[rb], ofree, p.err, abort_flag)) &&
-           warp_wait(&p_full[rb][u], (g / NS) & 1, p.err, abort_flag) &&
-           warp_wait(&v_full[sv], (g / NV) & 1, p.err, abort_flag);
+      // the three conditions are probed together first (non-blocking, their
+      // latencies overlap); only one still in progress takes the blocking path
+      const bool ready = D == 64 && __all_sync(0xffffffffu, (ofree < 0 || mbar_test_wait(&o_free[rb], ofree)) &
+                                                                mbar_test_wait(&p_full[rb][u], (g / NS) & 1) &
+                                                                mbar_test_wait(&v_full[sv], (g / NV) & 1));
+      ok = ready || ((ofree < 0 || warp_wait(&o_free[rb], ofree, p.err, abort_flag)) &&
+                     warp_wait(&p_full[rb][u], (g / NS) & 1, p.err, abort_flag) &&
+                     warp_wait(&v_full[sv], (g / NV) & 1, p.err, abort_flag));
       if (!ok) return;
       tc_fence_after();
 #pragma unroll
@@ -752,9 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(p.rope_cs ? &q_rot[qb] : &q_full[qb], (it >> 1) & 1, p.err, abort_flag);
       for (int j = 0; j < I.n && ok; ++j) {
         const int g = gt + j, st = g % NK;
-        // the buffer holds P(g - NS) until PV(g - NS) has read it
-        ok = (g < NS || warp_wait(&pv_done[rb][g % NS], ((g - NS) / NS) & 1, p.err, abort_flag)) &&
-             warp_wait(&k_full[st], (g / NK) & 1, p.err, abort_flag);
+        // The buffer holds P(g - NS) until PV(g - NS) has read it.  This
+        // thread issued that PV before this S, and the MMAs a thread issues
+        // run in issue order, so S(g) cannot overwrite P(g - NS) early.
+        ok = warp_wait(&k_full[st], (g / NK) & 1, p.err, abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -954,22 +973,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j + 1 < n) e_next = I.tiles[j + 1];
       const bool pooled = kPooled && ((e >> 20) & 1);
       const int k0 = (e & 0xFFFFF) * BN;
-      if (!fail && !(wait_or_abort(&s_full[rb][g % NS], (g / NS) & 1, p.err, abort_flag) &&
-                     wait_or_abort(&m_full[sm], (g / NM) & 1, p.err, abort_flag)))
-        fail = true;
+      // The row's visibility over the tile comes first (it needs only the
+      // tile record), so it overlaps the S MMA; a tile no row of the warp
+      // sees skips the score load and the softmax and stores a zero P.
+      // (the compressed variant reads no tile records: no handshake)
+      if (!kPooled && !fail && !wait_or_abort(&m_full[sm], (g / NM) & 1, p.err, abort_flag)) fail = true;
       __syncwarp();
-      tc_fence_after();
-      // one 64-register row buffer: raw scores, then masked scores, then p
-      uint32_t v[BN];
-      tmem_ld32(tS(rb, g % NS) + lane_base, v);
-      tmem_ld32(tS(rb, g % NS) + lane_base + 32, v + 32);
-      tmem_ld_wait();
       constexpr uint32_t kNegInf = 0xff800000u;
       // This row's 64-bit visibility word over the tile (bit x = key k0 + x),
       // built from shifts: a prefix for pooled columns (j visible iff
       // (j+1)*block <= q-W+1), (causal bound) and (window or sink) and (the
-      // row's segment) for exact keys.  Whole-warp all-visible tiles skip
-      // the per-key select.
+      // row's segment) for exact keys.
       const unsigned long long all1 = ~0ull;
       auto prefix = [&](int last) {  // bits 0..last
         return last < 0 ? 0ull : (last >= 63 ? all1 : (all1 >> (63 - last)));
@@ -1015,6 +1029,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           vis = myseg > 0 ? (vis & cw) : 0ull;
         }
       }
+      __syncwarp();
+      if (!kPooled && lane == 0) mbar_arrive(&m_empty[sm]);  // this warp is done with the tile record
+      const bool none = __all_sync(0xffffffffu, vis == 0ull);
+      if (!fail && !wait_or_abort(&s_full[rb][g % NS], (g / NS) & 1, p.err, abort_flag)) fail = true;
+      __syncwarp();
+      tc_fence_after();
+      if (none) {
+        // P(g) = 0 for this warp's rows (the MMA reads all 128 lanes)
+        uint32_t z[BN / 2];
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) z[i] = 0u;
+        if constexpr (D == 64) {
+          tmem_st16(tS(rb, g % NS) + lane_base, z);
+          tmem_st16(tS(rb, g % NS) + lane_base + 16, z + 16);
+        } else {
+          tmem_st32(tS(rb, g % NS) + lane_base, z);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[rb][g % NS]);
+        continue;
+      }
+      // one 64-register row buffer: raw scores, then masked scores, then p
+      uint32_t v[BN];
+      tmem_ld32(tS(rb, g % NS) + lane_base, v);
+      tmem_ld32(tS(rb, g % NS) + lane_base + 32, v + 32);
+      tmem_ld_wait();
+      // whole-warp all-visible tiles skip the per-key select
       if (!__all_sync(0xffffffffu, vis == all1)) {
         const uint32_t v0 = uint32_t(vis), v1 = uint32_t(vis >> 32);
 #pragma unroll
@@ -1023,8 +1065,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[x] = bit ? v[x] : kNegInf;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&m_empty[sm]);  // this warp is done with the tile record
       // row max: three-input max over 8 independent chains (keys i, i+8, ...,
       // i+56 on chain i)
       static_assert(BN == 64, "max chains cover 64 keys");
