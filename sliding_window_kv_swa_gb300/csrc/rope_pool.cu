@@ -12,6 +12,8 @@
 // pos * freq and the reduction mod 2*pi are done in double (two flops per
 // (position, pair), amortised over every head), then sincosf on the reduced
 // angle, so the rotation error is ~1e-7 rad even at position 4095.
+#include <algorithm>
+
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -367,6 +369,185 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
   }
 }
 
+// The fused pass fed by bulk copies.  The rows of nj_max consecutive pooled
+// blocks of one sequence are one contiguous stretch of K, of V and of the
+// angle table, so one thread moves each stretch into shared memory with a
+// single cp.async.bulk; a ring of kBulkStages chunks keeps the next ones in
+// flight while all threads work from shared memory: K rows rotated and
+// stored, K and V pooled, pooled K rotated at the block midpoint (one thread
+// per (block, head, 8 channel pairs) of K or of V).  The CTAs are persistent
+// and walk the chunks with a stride of the grid, then rotate the positions
+// outside whole blocks.  Sums, means, angles and roundings are those of
+// pool_rope_kernel, so the results are the same bits.
+constexpr int kBulkStages = 3;
+constexpr int kBulkBytes = 16384;  // K (and V) bytes per chunk, at most
+constexpr int kBulkMaxJ = 4;       // pooled blocks per chunk, at most
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void lds4(uint32_t addr, uint32_t *w) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+}
+__global__ void __launch_bounds__(256) pool_rope_bulk_kernel(const uint16_t *__restrict__ k,
+                                                             const uint16_t *__restrict__ v,
+                                                             uint16_t *__restrict__ k_rot, uint16_t *__restrict__ pk,
+                                                             uint16_t *__restrict__ pv, int B, int T, int H, int D,
+                                                             int block, int pos0, int nj_max,
+                                                             const float2 *__restrict__ cs, int *err) {
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  __shared__ __align__(8) uint64_t full[kBulkStages];
+  pdl_wait();  // the angle table (or what the previous kernel wrote) is in
+  const int nblk = (T - pos0) / block, per_seq = (nblk + nj_max - 1) / nj_max, n_chunks = B * per_seq;
+  const int half = D / 2, groups = half / 8;
+  const uint32_t row_bytes = uint32_t(H) * D * 2, tensor_bytes = uint32_t(nj_max) * block * row_bytes;
+  const uint32_t cs_row = uint32_t(half) * 8, cs_bytes = cs ? uint32_t(nj_max) * block * cs_row : 0u;
+  const uint32_t stage_bytes = 2 * tensor_bytes + cs_bytes;
+  const uint32_t base = smem_u32(stage_mem);
+  const size_t rstride = size_t(H) * D;
+  auto chunk = [&](int c, int &b, int &j0, int &nj) {
+    b = c / per_seq;
+    j0 = (c % per_seq) * nj_max;
+    nj = min(nj_max, nblk - j0);
+  };
+  auto issue = [&](int c, int st) {  // one thread
+    int b, j0, nj;
+    chunk(c, b, j0, nj);
+    const int t0 = pos0 + j0 * block;
+    const uint32_t bytes = uint32_t(nj) * block * row_bytes, cb = cs ? uint32_t(nj) * block * cs_row : 0u;
+    const size_t off = (size_t(b) * T + t0) * rstride;
+    const uint32_t dst = base + st * stage_bytes;
+    mbar_arrive_expect_tx(&full[st], 2 * bytes + cb);
+    bulk_g2s(dst, k + off, bytes, &full[st]);
+    bulk_g2s(dst + tensor_bytes, v + off, bytes, &full[st]);
+    if (cs) bulk_g2s(dst + 2 * tensor_bytes, cs + size_t(t0) * half, cb, &full[st]);
+  };
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kBulkStages; ++st) mbar_init(&full[st], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kBulkStages; ++i)
+      if (blockIdx.x + i * gridDim.x < n_chunks) issue(blockIdx.x + i * gridDim.x, i);
+  const float fblock = float(block);
+  bool ok = true;
+  for (int i = 0, c = blockIdx.x; c < n_chunks && ok; ++i, c += gridDim.x) {
+    const int st = i % kBulkStages;
+    int b, j0, nj;
+    chunk(c, b, j0, nj);
+    const uint32_t par = (i / kBulkStages) & 1;
+    ok = mbar_test_wait(&full[st], par) || mbar_wait(&full[st], par, err);
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    const uint32_t sk = base + st * stage_bytes, scs = sk + 2 * tensor_bytes;
+    const int per_kv = nj * H * groups;
+    for (int idx = threadIdx.x; idx < 2 * per_kv; idx += blockDim.x) {
+      const bool is_v = idx >= per_kv;
+      const int w = is_v ? idx - per_kv : idx;
+      const int g = w % groups, rest = w / groups;
+      const int h = rest % H, jj = rest / H;
+      const int i0 = g * 8;
+      const bool rot = cs && !is_v;
+      float sa[8], sb[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sa[e] = sb[e] = 0.f;
+      const uint32_t src = sk + (is_v ? tensor_bytes : 0u) + uint32_t(jj * block) * row_bytes + uint32_t(h * D + i0) * 2;
+      // rotated rotation angles of this row's pairs: 8 float2 at (row, i0)
+      auto angles = [&](int r, float *cc, float *ss) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          lds4(scs + uint32_t(jj * block + r) * cs_row + uint32_t(i0 + 2 * q4) * 8, wv);
+          cc[2 * q4] = __uint_as_float(wv[0]), ss[2 * q4] = __uint_as_float(wv[1]);
+          cc[2 * q4 + 1] = __uint_as_float(wv[2]), ss[2 * q4 + 1] = __uint_as_float(wv[3]);
+        }
+      };
+      const size_t grow0 = (size_t(b) * T + pos0 + size_t(j0 + jj) * block) * rstride + size_t(h) * D;
+      for (int r = 0; r < block; ++r) {
+        uint32_t a[4], bb[4];
+        lds4(src + r * row_bytes, a);
+        lds4(src + r * row_bytes + half * 2, bb);
+        float xa[8], xb[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xa[2 * e] = bf16_lo(a[e]), xa[2 * e + 1] = bf16_hi(a[e]);
+          xb[2 * e] = bf16_lo(bb[e]), xb[2 * e + 1] = bf16_hi(bb[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sa[e] += xa[e];
+          sb[e] += xb[e];
+        }
+        if (rot) {
+          float cc[8], ss[8], ya[8], yb[8];
+          angles(r, cc, ss);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) rope_pair(xa[e], xb[e], cc[e], ss[e], ya[e], yb[e]);
+          st8(k_rot + grow0 + size_t(r) * rstride + i0, ya);
+          st8(k_rot + grow0 + size_t(r) * rstride + i0 + half, yb);
+        }
+      }
+      float ya[8], yb[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sa[e] /= fblock;
+        sb[e] /= fblock;
+        ya[e] = sa[e];
+        yb[e] = sb[e];
+      }
+      if (rot) {  // the midpoint row j*block + block/2 lies inside the block
+        float cc[8], ss[8];
+        angles(block / 2, cc, ss);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rope_pair(sa[e], sb[e], cc[e], ss[e], ya[e], yb[e]);
+      }
+      uint16_t *y = is_v ? pv : pk;
+      const size_t orow = ((size_t(b) * nblk + j0 + jj) * H + h) * D;
+      st8(y + orow + i0, ya);
+      st8(y + orow + i0 + half, yb);
+    }
+    __syncthreads();  // the stage is free again
+    if (threadIdx.x == 0 && c + kBulkStages * int(gridDim.x) < n_chunks) {
+      // the async-proxy refill follows the threads' generic-proxy reads
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(c + kBulkStages * gridDim.x, st);
+    }
+  }
+  if (!ok) {  // a copy that never landed: give any still in flight time to land before the CTA exits
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+    return;
+  }
+  // positions before pos0 and past the last whole block: K's rotation only
+  if (!cs) return;
+  const int tail = T - pos0 - nblk * block, n_rest = pos0 + tail;
+  const size_t n_items = size_t(B) * n_rest * H * groups;
+  for (size_t idx = size_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < n_items; idx += size_t(gridDim.x) * blockDim.x) {
+    const int g = int(idx % groups);
+    size_t rest = idx / groups;
+    const int h = int(rest % H);
+    rest /= H;
+    const int u = int(rest % n_rest), b = int(rest / n_rest), i0 = g * 8;
+    const int t = u < pos0 ? u : pos0 + nblk * block + (u - pos0);
+    const size_t row = (size_t(b) * T + t) * rstride + size_t(h) * D;
+    float xa[8], xb[8], ya[8], yb[8];
+    ld8(k + row + i0, xa);
+    ld8(k + row + i0 + half, xb);
+    const float4 *t4 = reinterpret_cast<const float4 *>(cs + size_t(t) * half + i0);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const float4 wv = t4[q4];
+      rope_pair(xa[2 * q4], xb[2 * q4], wv.x, wv.y, ya[2 * q4], yb[2 * q4]);
+      rope_pair(xa[2 * q4 + 1], xb[2 * q4 + 1], wv.z, wv.w, ya[2 * q4 + 1], yb[2 * q4 + 1]);
+    }
+    st8(k_rot + row + i0, ya);
+    st8(k_rot + row + i0 + half, yb);
+  }
+}
+
 }  // namespace
 
 // The angle table (when theta != 0), then the fused pass; the table kernel
@@ -386,6 +567,25 @@ cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk
     if (e != cudaSuccess) return e;
   }
   const int nblk = (T - pos0) / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
+  const size_t block_bytes = size_t(block) * n_heads * head_dim * 2;
+  if (nblk > 0 && block_bytes <= size_t(kBulkBytes)) {
+    const int nj_max = int(std::min<size_t>(kBulkMaxJ, kBulkBytes / block_bytes));
+    const int n_chunks = batch * ((nblk + nj_max - 1) / nj_max);
+    const size_t stage = 2 * nj_max * block_bytes + (cs ? size_t(nj_max) * block * (head_dim / 2) * 8 : 0);
+    const int smem = int(kBulkStages * stage);
+    cudaError_t e = cudaFuncSetAttribute(pool_rope_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int sms = 0, dev = 0, per_sm = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pool_rope_bulk_kernel, 256, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = std::min(n_chunks, std::max(1, per_sm) * sms);
+    return launch_pdl(pool_rope_bulk_kernel, dim3(unsigned(grid)), dim3(256), size_t(smem), stream,
+                      static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
+                      static_cast<uint16_t *>(k_rot), static_cast<uint16_t *>(pk), static_cast<uint16_t *>(pv), batch,
+                      T, n_heads, head_dim, block, pos0, nj_max, static_cast<const float2 *>(cs),
+                      device_error_word());
+  }
   const int per_seq = n_grp + (T - nblk * block > 0 ? 1 : 0);
   if (per_seq == 0) return cudaSuccess;
   return launch_pdl(pool_rope_kernel, dim3(unsigned(size_t(batch) * per_seq)), dim3(256), 0, stream,
