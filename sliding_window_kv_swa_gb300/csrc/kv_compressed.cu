@@ -63,6 +63,38 @@ __global__ void __launch_bounds__(512) compressed_append_kernel(const Compressed
   // once per CTA (the double-precision reduction is off every row's chain)
   __shared__ float2 s_cs[2][D / 2];
   pdl_wait();
+  // Each warp's first kPre items read their inputs (the new token's row, the
+  // block's running sums, a query row) now, so those loads overlap the
+  // metadata read and the angle setup below instead of following them.
+  const int Hkv = c.n_kv_heads, nslot = c.sink_cap + c.ring_cap;
+  const int n_items = 2 * Hkv + p.Hq;
+  const int c0 = lane * CPL;
+  constexpr int kPre = 4;
+  auto load = [&](const uint16_t *src, float *x) {
+    if constexpr (CPL == 4) {
+      const uint2 w = reinterpret_cast<const uint2 *>(src)[lane];
+      x[0] = bf16_lo(w.x), x[1] = bf16_hi(w.x), x[2] = bf16_lo(w.y), x[3] = bf16_hi(w.y);
+    } else {
+      const uint32_t w = reinterpret_cast<const uint32_t *>(src)[lane];
+      x[0] = bf16_lo(w), x[1] = bf16_hi(w);
+    }
+  };
+  auto fetch = [&](int item, float *x, float *sum) {
+    if (item >= 2 * Hkv) {
+      load(p.q + (size_t(b) * p.Hq + (item - 2 * Hkv)) * D, x);
+      return;
+    }
+    const size_t pair = size_t(b) * Hkv + (item >> 1);
+    const bool is_v = item & 1;
+    load((is_v ? p.v_new : p.k_new) + pair * D, x);
+    const float *sp = (is_v ? p.v_sum : p.k_sum) + pair * D + c0;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) sum[e] = sp[e];
+  };
+  float px[kPre][CPL], ps[kPre][CPL];
+#pragma unroll
+  for (int t = 0; t < kPre; ++t)
+    if (warp + t * nw < n_items) fetch(warp + t * nw, px[t], ps[t]);
   if (threadIdx.x == 0) {
     const int sl = c.sink_len[b], rs = c.ring_start[b], rl = c.ring_len[b], pos = c.seq_len[b];
     const bool sane = sl >= 0 && sl <= c.sink_cap && rl >= 0 && rl <= c.ring_cap && rs >= 0 &&
@@ -109,10 +141,8 @@ __global__ void __launch_bounds__(512) compressed_append_kernel(const Compressed
   for (int i = threadIdx.x; i < D; i += blockDim.x)
     s_cs[i / (D / 2)][i % (D / 2)] = rot_cs(double(i < D / 2 ? pos : mid), p.fr.f[i % (D / 2)]);
   __syncthreads();
-  const int Hkv = c.n_kv_heads, nslot = c.sink_cap + c.ring_cap;
   // this lane's channel pairs: lanes 0-15 hold x_i, lanes 16-31 the partner
   // x_{i + D/2} of the same pairs (lane ^ 16)
-  const int c0 = lane * CPL;
   const int i0 = c0 % (D / 2);
   const bool hi = lane >= 16;
   auto rotate = [&](float *x, int which) {  // which: 0 at the position, 1 at the block midpoint
@@ -132,15 +162,6 @@ __global__ void __launch_bounds__(512) compressed_append_kernel(const Compressed
       }
     }
   };
-  auto load = [&](const uint16_t *src, float *x) {
-    if constexpr (CPL == 4) {
-      const uint2 w = reinterpret_cast<const uint2 *>(src)[lane];
-      x[0] = bf16_lo(w.x), x[1] = bf16_hi(w.x), x[2] = bf16_lo(w.y), x[3] = bf16_hi(w.y);
-    } else {
-      const uint32_t w = reinterpret_cast<const uint32_t *>(src)[lane];
-      x[0] = bf16_lo(w), x[1] = bf16_hi(w);
-    }
-  };
   auto store_quant = [&](const float *x, int8_t *codes, float *scales) {
     int code[CPL];
     const float scale = quant_lanes<CPL>(x, code);
@@ -151,27 +172,27 @@ __global__ void __launch_bounds__(512) compressed_append_kernel(const Compressed
     else reinterpret_cast<uint16_t *>(codes)[lane] = uint16_t(packed);
     if (lane % (32 / CPL) == 0) scales[lane / (32 / CPL)] = scale;
   };
-  const int n_items = 2 * Hkv + p.Hq;
-  for (int item = warp; item < n_items; item += nw) {
+  // item: its inputs x (the row) and sum (the block's running sums), fetched
+  auto process = [&](int item, const float *x_in, const float *sum_in) {
     if (item >= 2 * Hkv) {  // a query head: rotated at pos, rounded to bf16
       const int h = item - 2 * Hkv;
       const size_t off = (size_t(b) * p.Hq + h) * D;
       float x[CPL];
-      load(p.q + off, x);
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) x[e] = x_in[e];
       rotate(x, 0);
       if constexpr (CPL == 4)
         reinterpret_cast<uint2 *>(p.q_rot + off)[lane] = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
       else
         reinterpret_cast<uint32_t *>(p.q_rot + off)[lane] = pack_bf16x2(x[0], x[1]);
-      continue;
+      return;
     }
     const int h = item >> 1;
     const bool is_v = item & 1;
     const size_t pair = size_t(b) * Hkv + h;
     float x[CPL], raw[CPL];
-    load((is_v ? p.v_new : p.k_new) + pair * D, x);
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) raw[e] = x[e];
+    for (int e = 0; e < CPL; ++e) raw[e] = x[e] = x_in[e];
     // the exact key (rotated at pos, rounded to bf16) or value
     if (!is_v) {
       rotate(x, 0);
@@ -180,16 +201,16 @@ __global__ void __launch_bounds__(512) compressed_append_kernel(const Compressed
     }
     store_quant(x, (is_v ? c.v_codes : c.k_codes) + (pair * nslot + exact) * D,
                 (is_v ? c.v_scale : c.k_scale) + (pair * nslot + exact) * (D / 32));
-    if (pinned) continue;
+    if (pinned) return;
     // the block's running sums (fp32, in position order, before rotation)
     float *sum = (is_v ? p.v_sum : p.k_sum) + pair * D + c0;
     float acc[CPL];
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) acc[e] = (mode & 1) ? raw[e] : sum[e] + raw[e];
+    for (int e = 0; e < CPL; ++e) acc[e] = (mode & 1) ? raw[e] : sum_in[e] + raw[e];
     if (!(mode & 2)) {
 #pragma unroll
       for (int e = 0; e < CPL; ++e) sum[e] = acc[e];
-      continue;
+      return;
     }
     // the block is complete: its mean, K rotated at the block midpoint
     const float fb = float(p.block);
@@ -201,6 +222,14 @@ __global__ void __launch_bounds__(512) compressed_append_kernel(const Compressed
     if (pooled >= 0)
       store_quant(acc, (is_v ? c.v_codes : c.k_codes) + (pair * nslot + pooled) * D,
                   (is_v ? c.v_scale : c.k_scale) + (pair * nslot + pooled) * (D / 32));
+  };
+#pragma unroll
+  for (int t = 0; t < kPre; ++t)
+    if (warp + t * nw < n_items) process(warp + t * nw, px[t], ps[t]);
+  for (int item = warp + kPre * nw; item < n_items; item += nw) {
+    float x[CPL], sum[CPL];
+    fetch(item, x, sum);
+    process(item, x, sum);
   }
   __syncthreads();
   if (threadIdx.x == 0) {

@@ -379,11 +379,15 @@ def test_prefill_tile_count_reported_by_the_kernel_plan(Hq, Hkv, d):
 
 
 @pytest.mark.parametrize("block,T,d,theta", [(4, 4096, 64, 10000.0), (3, 301, 64, 10000.0), (8, 1000, 128, 500000.0),
-                                             (1, 77, 64, 10000.0), (4, 258, 128, 0.0), (16, 10, 64, 10000.0)])
+                                             (1, 77, 64, 10000.0), (4, 258, 128, 0.0), (16, 10, 64, 10000.0),
+                                             (64, 300, 64, 10000.0)])
 def test_pool_rope_pass_matches_the_separate_passes(block, T, d, theta):
     """nd_kv_compress_pool_rope (one read of K and V) gives bit for bit the
     rotated keys of nd_rope_apply and the pooled blocks of nd_kv_compress_pool
-    (positions past the last whole block are rotated too)."""
+    (positions past the last whole block are rotated too).  The cases cover
+    both forms of the pass: chunks of whole blocks moved by bulk copies, and
+    the per-thread form for a pooled block of more than 16 KB (block 64 here)
+    or a sequence shorter than one block."""
     rng = philox(1950 + block + T + d)
     B, H = 2, 3
     kb, _ = normal_bf16(rng, (B, T, H, d))
