@@ -12,9 +12,11 @@
 // head); eight threads share a row and split the head dimension (short
 // dot-product chains, two partial sums each, and four times the CTAs of a
 // two-threads-per-row layout for the small problems this path serves).  Key
-// tiles of 64 are staged in shared memory; a tile is skipped when no row of
-// the CTA can see any of its keys (causal bound, window bound without sinks,
-// or disjoint segment-id ranges).  Online softmax in the log2 domain.
+// tiles of 64 are copied into shared memory with cp.async, the next tile's
+// copies in flight while the current one is used; a tile is skipped when no
+// row of the CTA can see any of its keys (causal bound, window bound without
+// sinks, or disjoint segment-id ranges, found by warp reductions).  Eight
+// keys per online-softmax step, in the log2 domain.
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -27,43 +29,37 @@ namespace {
 constexpr int kTpr = 8;  // threads per query row
 constexpr int kRows = 16, kKeys = 64, kThreads = kRows * kTpr;
 
-template <typename E>
-__device__ __forceinline__ float ld_elem(const E *p, size_t i);
-template <>
-__device__ __forceinline__ float ld_elem<float>(const float *p, size_t i) { return p[i]; }
-template <>
-__device__ __forceinline__ float ld_elem<uint16_t>(const uint16_t *p, size_t i) {
-  return __uint_as_float(uint32_t(p[i]) << 16);
+__device__ __forceinline__ void cp_async16z(uint32_t dst, const void *src, bool valid) {
+  // 16 bytes, or zeros (source size 0) for a key past the end
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
-template <typename E>
-__device__ __forceinline__ void st_elem(E *p, size_t i, float x);
-template <>
-__device__ __forceinline__ void st_elem<float>(float *p, size_t i, float x) { p[i] = x; }
-template <>
-__device__ __forceinline__ void st_elem<uint16_t>(uint16_t *p, size_t i, float x) {
-  p[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename E, int D>
+template <int D>
 __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArgs a) {
   constexpr int H2 = D / kTpr;  // channels per thread
-  extern __shared__ float smem[];
-  float *sk = smem;                 // [kKeys][D]
-  float *sv = sk + kKeys * D;       // [kKeys][D]
+  constexpr int kTile = kKeys * D;  // floats of one K (or V) tile
+  extern __shared__ __align__(16) float smem[];
+  // two stages of [K tile][V tile]: the next tile's copies land while this
+  // one is used
   __shared__ int s_seg[kKeys];
   __shared__ unsigned char s_sink[kKeys];
+  __shared__ int s_red[3][2];
   __shared__ int s_qseg_lo, s_qseg_hi;
 
   const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
   const int T = a.T, G = a.Hq / a.Hkv, hk = hq / G;
   const int r = threadIdx.x / kTpr, part = threadIdx.x % kTpr;  // part: this thread's channel slice
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = qt * kRows;
   const int q = q0 + r;
   const bool row_ok = q < T;
   const int q_last = min(q0 + kRows, T) - 1;
-  const E *Q = static_cast<const E *>(a.q);
-  const E *K = static_cast<const E *>(a.k);
-  const E *V = static_cast<const E *>(a.v);
+  const float *Q = static_cast<const float *>(a.q);
   const int W = a.window;
   const int my_seg = (a.seg_ids && row_ok) ? a.seg_ids[size_t(b) * T + q] : (row_ok ? 1 : 0);
 
@@ -81,17 +77,18 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
   float qr[H2], o[H2];
 #pragma unroll
   for (int c = 0; c < H2; ++c) {
-    qr[c] = row_ok ? ld_elem(Q, ((size_t(b) * T + q) * a.Hq + hq) * D + part * H2 + c) * qscale : 0.f;
+    qr[c] = row_ok ? Q[((size_t(b) * T + q) * a.Hq + hq) * D + part * H2 + c] * qscale : 0.f;
     o[c] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
   __syncthreads();
   const int qseg_lo = s_qseg_lo, qseg_hi = s_qseg_hi;
+  const uint32_t sbase = smem_u32(smem);
 
   // One pass over a column source: pooled (src = 1) or exact keys (src = 0).
   auto run = [&](int src, int n_cols) {
-    const E *KK = src ? static_cast<const E *>(a.pooled_k) : K;
-    const E *VV = src ? static_cast<const E *>(a.pooled_v) : V;
+    const float *KK = static_cast<const float *>(src ? a.pooled_k : a.k);
+    const float *VV = static_cast<const float *>(src ? a.pooled_v : a.v);
     const int TK = src ? (T / a.block) : T;
     int col_end;  // exclusive bound on useful columns for this CTA
     if (src) {
@@ -101,83 +98,79 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
     } else {
       col_end = q_last + 1;
     }
-    for (int k0 = 0; k0 < col_end; k0 += kKeys) {
-      // ---- tile metadata and skip test (exact keys only)
+    const int n_tiles = (col_end + kKeys - 1) / kKeys;
+    // a thread copies 16-byte chunks idx = tid + u*kThreads of each tile
+    auto stage = [&](int t) {
+      const int k0 = t * kKeys;
+      const uint32_t dk = sbase + uint32_t((t & 1) * 2 * kTile) * 4, dv = dk + kTile * 4;
+      constexpr int kPer = kTile / 4 / kThreads;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int idx = threadIdx.x + u * kThreads;
+        const int kk = idx / (D / 4), c4 = idx % (D / 4);
+        const int k = k0 + kk;
+        const bool ok = k < TK;
+        const size_t off = ((size_t(b) * TK + (ok ? k : 0)) * a.Hkv + hk) * D + 4 * c4;
+        cp_async16z(dk + idx * 16, KK + off, ok);
+        cp_async16z(dv + idx * 16, VV + off, ok);
+      }
+    };
+    if (n_tiles > 0) stage(0);
+    cp_async_commit_group();
+    for (int t = 0; t < n_tiles; ++t) {
+      const int k0 = t * kKeys;
+      // the next tile's copies go out first (one commit group per tile,
+      // empty past the last)
+      if (t + 1 < n_tiles) stage(t + 1);
+      cp_async_commit_group();
+      // this tile's copies land before anything else: a skipped tile's
+      // buffer takes the copies of tile t + 2 next
+      cp_async_wait_group<1>();
+      // ---- tile metadata and skip test (exact keys only): the tile's
+      //      segment-id range and sink presence by warp reductions
       if (!src) {
+        int sg = 0, sk = 0;
         if (threadIdx.x < kKeys) {
           const int k = k0 + threadIdx.x;
-          s_seg[threadIdx.x] = (k < T) ? (a.seg_ids ? a.seg_ids[size_t(b) * T + k] : 1) : 0;
-          s_sink[threadIdx.x] = (k < T && a.sink) ? a.sink[size_t(b) * T + k] : 0;
+          sg = (k < T) ? (a.seg_ids ? a.seg_ids[size_t(b) * T + k] : 1) : 0;
+          sk = (k < T && a.sink) ? a.sink[size_t(b) * T + k] : 0;
+          s_seg[threadIdx.x] = sg;
+          s_sink[threadIdx.x] = (unsigned char)sk;
+          const int lo = __reduce_min_sync(0xffffffffu, sg > 0 ? sg : INT_MAX);
+          const int hi = __reduce_max_sync(0xffffffffu, sg > 0 ? sg : INT_MIN);
+          const int any = __reduce_or_sync(0xffffffffu, unsigned(sk)) != 0u;
+          if (lane == 0) {
+            s_red[0][warp] = lo;
+            s_red[1][warp] = hi;
+            s_red[2][warp] = any;
+          }
         }
         __syncthreads();
-        int any_sink = 0, lo = INT_MAX, hi = INT_MIN;
-        for (int i = 0; i < kKeys; ++i) {
-          if (s_seg[i] > 0) {
-            lo = min(lo, s_seg[i]);
-            hi = max(hi, s_seg[i]);
-          }
-          any_sink |= s_sink[i];
-        }
+        const int lo = min(s_red[0][0], s_red[0][1]), hi = max(s_red[1][0], s_red[1][1]);
+        const bool any_sink = (s_red[2][0] | s_red[2][1]) != 0;
         const bool in_window = (W == 0) || (k0 + kKeys - 1 >= q0 - W + 1);
         const bool seg_overlap = lo <= qseg_hi && hi >= qseg_lo;
         if (!seg_overlap || (!in_window && !any_sink)) {
-          __syncthreads();
+          __syncthreads();  // (the metadata is rewritten for the next tile)
           continue;
         }
       }
-      // ---- stage K and V tile (fp32): 16-byte loads, a thread's loads all
-      //      issued before its shared-memory stores
-      if constexpr (sizeof(E) == 4) {
-        constexpr int kVec = kKeys * D / 4, kPer = kVec / kThreads;
-        float4 kx[kPer], vx[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int idx = threadIdx.x + u * kThreads;
-          const int kk = idx / (D / 4), c4 = idx % (D / 4);
-          const int k = k0 + kk;
-          kx[u] = vx[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (k < TK) {
-            const size_t off = ((size_t(b) * TK + k) * a.Hkv + hk) * D + 4 * c4;
-            kx[u] = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(KK) + off);
-            vx[u] = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(VV) + off);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int idx = threadIdx.x + u * kThreads;
-          reinterpret_cast<float4 *>(sk)[idx] = kx[u];
-          reinterpret_cast<float4 *>(sv)[idx] = vx[u];
-        }
-      } else {
-        for (int idx = threadIdx.x; idx < kKeys * D; idx += kThreads) {
-          const int kk = idx / D, c = idx % D;
-          const int k = k0 + kk;
-          float kv = 0.f, vv = 0.f;
-          if (k < TK) {
-            const size_t off = ((size_t(b) * TK + k) * a.Hkv + hk) * D + c;
-            kv = ld_elem(KK, off);
-            vv = ld_elem(VV, off);
-          }
-          sk[idx] = kv;
-          sv[idx] = vv;
-        }
-      }
-      __syncthreads();
-      // four keys per step: four independent dot products, then one max,
-      // one rescale and four exponentials (the online softmax's serial
-      // chain is a quarter as long)
-      constexpr int kStepKeys = 4;
+      __syncthreads();  // every thread's copies of this tile are visible
+      const float *sk = smem + (t & 1) * 2 * kTile, *sv = sk + kTile;
+      // eight keys per step: eight independent dot products, one shuffle
+      // tree for all eight, then one max, one rescale and eight exponentials
+      constexpr int kStepKeys = 8;
       for (int kk0 = 0; kk0 < kKeys; kk0 += kStepKeys) {
-        float sv4[kStepKeys];
-        bool vis4[kStepKeys];
+        float sc[kStepKeys];
+        bool vis[kStepKeys];
 #pragma unroll
         for (int u = 0; u < kStepKeys; ++u) {
           const int kk = kk0 + u, k = k0 + kk;
           if (src) {
-            vis4[u] = row_ok && k < n_cols && (k + 1) * a.block <= q - W + 1;
+            vis[u] = row_ok && k < n_cols && (k + 1) * a.block <= q - W + 1;
           } else {
-            vis4[u] = row_ok && k <= q && my_seg > 0 && s_seg[kk] == my_seg &&
-                      (W == 0 || q - k < W || s_sink[kk]);
+            vis[u] = row_ok && k <= q && my_seg > 0 && s_seg[kk] == my_seg &&
+                     (W == 0 || q - k < W || s_sink[kk]);
           }
           const float *kr = sk + kk * D + part * H2;
           float s0 = 0.f, s1 = 0.f;
@@ -186,16 +179,16 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
             s0 = fmaf(qr[c], kr[c], s0);
             s1 = fmaf(qr[c + 1], kr[c + 1], s1);
           }
-          sv4[u] = s0 + s1;
+          sc[u] = s0 + s1;
         }
 #pragma unroll
         for (int off = 1; off < kTpr; off <<= 1)
 #pragma unroll
-          for (int u = 0; u < kStepKeys; ++u) sv4[u] += __shfl_xor_sync(0xffffffffu, sv4[u], off);
+          for (int u = 0; u < kStepKeys; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
         float mx = m;
 #pragma unroll
         for (int u = 0; u < kStepKeys; ++u)
-          if (vis4[u]) mx = fmaxf(mx, sv4[u]);
+          if (vis[u]) mx = fmaxf(mx, sc[u]);
         if (mx == -INFINITY) continue;  // nothing visible yet
         if (mx > m) {
           const float f = ex2(m - mx);  // m = -inf: f = 0
@@ -206,37 +199,37 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
         }
 #pragma unroll
         for (int u = 0; u < kStepKeys; ++u) {
-          if (!vis4[u]) continue;
-          const float pr = ex2(sv4[u] - m);
+          if (!vis[u]) continue;
+          const float pr = ex2(sc[u] - m);
           l += pr;
           const float *vr = sv + (kk0 + u) * D + part * H2;
 #pragma unroll
           for (int c = 0; c < H2; ++c) o[c] = fmaf(pr, vr[c], o[c]);
         }
       }
-      __syncthreads();
+      __syncthreads();  // the stage and the metadata are free again
     }
+    cp_async_wait_group<0>();
   };
 
   if (a.block > 0) run(1, T / a.block);
   run(0, T);
 
   if (row_ok) {
-    E *O = static_cast<E *>(a.out);
+    float *O = static_cast<float *>(a.out);
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int c = 0; c < H2; ++c)
-      st_elem(O, ((size_t(b) * T + q) * a.Hq + hq) * D + part * H2 + c, o[c] * inv);
+    for (int c = 0; c < H2; ++c) O[((size_t(b) * T + q) * a.Hq + hq) * D + part * H2 + c] = o[c] * inv;
     if (a.lse && part == 0)
       a.lse[(size_t(b) * a.Hq + hq) * T + q] =
           l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
 }
 
-template <typename E, int D>
+template <int D>
 cudaError_t launch_simt(const PrefillArgs &a, cudaStream_t stream) {
-  const size_t smem = size_t(2) * kKeys * D * sizeof(float);
-  auto kern = prefill_simt_kernel<E, D>;
+  const size_t smem = size_t(2) * 2 * kKeys * D * sizeof(float);  // two stages of K and V tiles
+  auto kern = prefill_simt_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((a.T + kRows - 1) / kRows, a.Hq, a.batch);
@@ -250,8 +243,8 @@ cudaError_t launch_simt(const PrefillArgs &a, cudaStream_t stream) {
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream) {
   if (size_t(a.batch) * a.T == 0) return cudaSuccess;
   if (a.dtype != ND_F32) return cudaErrorInvalidValue;
-  if (a.d == 64) return launch_simt<float, 64>(a, stream);
-  if (a.d == 128) return launch_simt<float, 128>(a, stream);
+  if (a.d == 64) return launch_simt<64>(a, stream);
+  if (a.d == 128) return launch_simt<128>(a, stream);
   return cudaErrorInvalidValue;
 }
 
