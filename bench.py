@@ -661,7 +661,9 @@ def bench_tiny_fp32(torch, nd, steps, warmup, pk, dist=None, cpu_budget=None):
         q, k, v = (torch.from_numpy(w[x]).cuda() for x in ("q", "k", "v"))
         seg, sink = torch.from_numpy(w["seg_ids"]).cuda(), torch.from_numpy(w["sink"]).cuda()
         out = torch.empty_like(q)
-        ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+        B_, T_, Hq_, d_ = q.shape
+        nbytes = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, B_, T_, Hq_, k.shape[2], d_, 0.0, 0)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
 
         def step(i):
             nd.nd_swa_sink_prefill(q, k, v, seg, sink, w["window"], out=out, workspace=ws)

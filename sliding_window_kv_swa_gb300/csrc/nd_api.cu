@@ -473,6 +473,7 @@ size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T, int 
                                           int block) {
   if (batch <= 0 || T <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return 0;
   size_t bytes = prefill_rotation_bytes(dtype, batch, T, n_q_heads, n_kv_heads, head_dim, rope_theta);
+  if (dtype == ND_F32) bytes += prefill_f32_partial_bytes(batch, T, n_q_heads, head_dim);
   if (dtype == ND_BF16)
     bytes += round_up(prefill_plan_bytes(batch, T, block), 256) +
              prefill_pooled_bytes(batch, T, n_kv_heads, head_dim, block);
@@ -596,7 +597,9 @@ static int prefill_impl(const void *q, const void *k, const void *v, nd_dtype dt
     else a.rope_cs = table;
   }
   if (e != cudaSuccess) return fail_cuda(e);
-  if (f32) return finish(launch_prefill_f32(a, s));
+  if (f32)
+    return finish(launch_prefill_f32(
+        a, ws + prefill_rotation_bytes(dtype, batch, T, n_q_heads, n_kv_heads, head_dim, rope_theta), s));
   return finish(launch_prefill_tc(a, ws, device_error_word(), s));
 }
 

@@ -150,7 +150,11 @@ struct PrefillArgs {
 };
 
 size_t prefill_plan_bytes(int batch, int T, int block);
-cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
+// fp32 prefill; small problems split their keys over several CTAs and merge
+// the partial states in `partials` (prefill_f32_partial_bytes; 0 bytes and
+// NULL otherwise)
+size_t prefill_f32_partial_bytes(int batch, int T, int n_q_heads, int head_dim);
+cudaError_t launch_prefill_f32(const PrefillArgs &a, void *partials, cudaStream_t stream);
 // The tensor-core path in two launches: the tile records and plan (an
 // ordinary launch, first of the call), then the attention kernel (a dependent
 // launch: it waits for the kernel before it, which may be the rotation pass).

@@ -16,7 +16,11 @@
 // copies in flight while the current one is used; a tile is skipped when no
 // row of the CTA can see any of its keys (causal bound, window bound without
 // sinks, or disjoint segment-id ranges, found by warp reductions).  Eight
-// keys per online-softmax step, in the log2 domain.
+// keys per online-softmax step, in the log2 domain.  A problem of at most
+// 256 such CTAs, which leaves most SMs idle and each CTA walking every key
+// tile of its rows in turn, splits each row tile's key tiles over four CTAs
+// and merges their softmax states (max, sum, weighted values) in a second
+// pass.
 #include "nd_common.cuh"
 #include "nd_internal.h"
 
@@ -39,8 +43,11 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArgs a) {
+// Small problems split each row tile's keys over kSplit CTAs (split s takes
+// key tiles s, s + kSplit, ...); each writes its rows' partial softmax state
+// (max, sum, weighted values) and simt_combine_kernel merges them.
+template <int D, int kSplit>
+__global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArgs a, float *partials) {
   constexpr int H2 = D / kTpr;  // channels per thread
   constexpr int kTile = kKeys * D;  // floats of one K (or V) tile
   extern __shared__ __align__(16) float smem[];
@@ -51,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
   __shared__ int s_red[3][2];
   __shared__ int s_qseg_lo, s_qseg_hi;
 
-  const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+  const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z / kSplit, split = blockIdx.z % kSplit;
   const int T = a.T, G = a.Hq / a.Hkv, hk = hq / G;
   const int r = threadIdx.x / kTpr, part = threadIdx.x % kTpr;  // part: this thread's channel slice
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,10 +106,13 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
       col_end = q_last + 1;
     }
     const int n_tiles = (col_end + kKeys - 1) / kKeys;
+    // this CTA's tiles: split, split + kSplit, ...; the i-th of them uses
+    // stage i & 1
+    const int n_mine = n_tiles > split ? (n_tiles - split + kSplit - 1) / kSplit : 0;
     // a thread copies 16-byte chunks idx = tid + u*kThreads of each tile
-    auto stage = [&](int t) {
-      const int k0 = t * kKeys;
-      const uint32_t dk = sbase + uint32_t((t & 1) * 2 * kTile) * 4, dv = dk + kTile * 4;
+    auto stage = [&](int i) {
+      const int k0 = (split + i * kSplit) * kKeys;
+      const uint32_t dk = sbase + uint32_t((i & 1) * 2 * kTile) * 4, dv = dk + kTile * 4;
       constexpr int kPer = kTile / 4 / kThreads;
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
@@ -115,13 +125,13 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
         cp_async16z(dv + idx * 16, VV + off, ok);
       }
     };
-    if (n_tiles > 0) stage(0);
+    if (n_mine > 0) stage(0);
     cp_async_commit_group();
-    for (int t = 0; t < n_tiles; ++t) {
-      const int k0 = t * kKeys;
+    for (int i = 0; i < n_mine; ++i) {
+      const int k0 = (split + i * kSplit) * kKeys;
       // the next tile's copies go out first (one commit group per tile,
       // empty past the last)
-      if (t + 1 < n_tiles) stage(t + 1);
+      if (i + 1 < n_mine) stage(i + 1);
       cp_async_commit_group();
       // this tile's copies land before anything else: a skipped tile's
       // buffer takes the copies of tile t + 2 next
@@ -156,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
         }
       }
       __syncthreads();  // every thread's copies of this tile are visible
-      const float *sk = smem + (t & 1) * 2 * kTile, *sv = sk + kTile;
+      const float *sk = smem + (i & 1) * 2 * kTile, *sv = sk + kTile;
       // eight keys per step: eight independent dot products, one shuffle
       // tree for all eight, then one max, one rescale and eight exponentials
       constexpr int kStepKeys = 8;
@@ -215,6 +225,19 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
   if (a.block > 0) run(1, T / a.block);
   run(0, T);
 
+  if (kSplit > 1) {
+    // [B][Hq][T][kSplit] records of D values, then the max and the sum
+    if (row_ok) {
+      float *rec = partials + ((((size_t(b) * a.Hq + hq) * T + q) * kSplit) + split) * (D + 2);
+#pragma unroll
+      for (int c = 0; c < H2; ++c) rec[part * H2 + c] = o[c];
+      if (part == 0) {
+        rec[D] = m;
+        rec[D + 1] = l;
+      }
+    }
+    return;
+  }
   if (row_ok) {
     float *O = static_cast<float *>(a.out);
     const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -226,25 +249,75 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
   }
 }
 
-template <int D>
-cudaError_t launch_simt(const PrefillArgs &a, cudaStream_t stream) {
+// Merge of the split partial states of one (row, channel): m = max m_s,
+// l = sum l_s 2^(m_s - m), o = sum o_s 2^(m_s - m) / l (log2 domain).
+template <int D, int kSplit>
+__global__ void __launch_bounds__(256) simt_combine_kernel(const PrefillArgs a, const float *partials) {
+  const size_t idx = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t rows = size_t(a.batch) * a.Hq * a.T;
+  if (idx >= rows * D) return;
+  const size_t row = idx / D;  // (b, hq, q)
+  const int c = int(idx % D);
+  const float *rec = partials + row * kSplit * (D + 2);
+  float mx = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kSplit; ++s) mx = fmaxf(mx, rec[s * (D + 2) + D]);
+  float l = 0.f, o = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int s = 0; s < kSplit; ++s) {
+      const float f = ex2(rec[s * (D + 2) + D] - mx);  // an empty split: 2^-inf = 0
+      l += rec[s * (D + 2) + D + 1] * f;
+      o += rec[s * (D + 2) + c] * f;
+    }
+  }
+  const int q = int(row % a.T);
+  const size_t bh = row / a.T;  // b * Hq + hq
+  const int hq = int(bh % a.Hq), b = int(bh / a.Hq);
+  static_cast<float *>(a.out)[((size_t(b) * a.T + q) * a.Hq + hq) * D + c] = l > 0.f ? o / l : 0.f;
+  if (a.lse && c == 0) a.lse[bh * a.T + q] = l > 0.f ? (mx + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+}
+
+constexpr int kSplitSmall = 4;  // key splits for problems of at most kSplitCtas row-tile CTAs
+constexpr long kSplitCtas = 256;
+
+int simt_splits(int batch, int T, int Hq) {
+  const long ctas = long(batch) * Hq * ((T + kRows - 1) / kRows);
+  return ctas <= kSplitCtas ? kSplitSmall : 1;
+}
+
+template <int D, int kSplit>
+cudaError_t launch_simt(const PrefillArgs &a, float *partials, cudaStream_t stream) {
   const size_t smem = size_t(2) * 2 * kKeys * D * sizeof(float);  // two stages of K and V tiles
-  auto kern = prefill_simt_kernel<D>;
+  auto kern = prefill_simt_kernel<D, kSplit>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid((a.T + kRows - 1) / kRows, a.Hq, a.batch);
-  kern<<<grid, kThreads, smem, stream>>>(a);
+  dim3 grid((a.T + kRows - 1) / kRows, a.Hq, a.batch * kSplit);
+  kern<<<grid, kThreads, smem, stream>>>(a, partials);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || kSplit == 1) return e;
+  const size_t n = size_t(a.batch) * a.Hq * a.T * D;
+  simt_combine_kernel<D, kSplit><<<unsigned((n + 255) / 256), 256, 0, stream>>>(a, partials);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t prefill_f32_partial_bytes(int batch, int T, int Hq, int head_dim) {
+  const int S = simt_splits(batch, T, Hq);
+  if (S == 1) return 0;
+  return (size_t(batch) * Hq * T * S * (head_dim + 2) * sizeof(float) + 255) / 256 * 256;
+}
+
 // fp32 inputs on CUDA cores (bf16 inputs always take the tensor-core kernel).
-cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream) {
+cudaError_t launch_prefill_f32(const PrefillArgs &a, void *partials, cudaStream_t stream) {
   if (size_t(a.batch) * a.T == 0) return cudaSuccess;
   if (a.dtype != ND_F32) return cudaErrorInvalidValue;
-  if (a.d == 64) return launch_simt<64>(a, stream);
-  if (a.d == 128) return launch_simt<128>(a, stream);
+  float *pw = static_cast<float *>(partials);
+  const bool split = simt_splits(a.batch, a.T, a.Hq) > 1;
+  if (split && !pw) return cudaErrorInvalidValue;
+  if (a.d == 64) return split ? launch_simt<64, kSplitSmall>(a, pw, stream) : launch_simt<64, 1>(a, pw, stream);
+  if (a.d == 128) return split ? launch_simt<128, kSplitSmall>(a, pw, stream) : launch_simt<128, 1>(a, pw, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -201,9 +201,15 @@ def test_bf16_prefill_workspace_holds_no_rotated_q():
     k_bytes = B * T * Hkv * d * 2            # rotated K, bf16 (a multiple of 256 here)
     table_bytes = T * (d // 2) * 8           # (cos, sin) fp32 per position and pair
     assert with_rope - no_rope == k_bytes + table_bytes
-    # the fp32 path still keeps rotated copies of both q and k
+    # the fp32 path still keeps rotated copies of both q and k; a problem this
+    # small (at most 256 CTAs of 16 rows) splits its keys over four CTAs per
+    # row tile, whose partial states -- D values, max and sum per row and
+    # split -- follow
     f32 = nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, B, T, Hq, Hkv, d, 10000.0, 0)
-    assert f32 == B * T * Hq * d * 4 + B * T * Hkv * d * 4 + table_bytes
+    partials = B * Hq * T * 4 * (d + 2) * 4
+    assert f32 == B * T * Hq * d * 4 + B * T * Hkv * d * 4 + table_bytes + partials
+    # a large one does not split
+    assert nd.nd_swa_sink_prefill_workspace_size(nd.ND_F32, 8, 4096, 32, 8, 128, 0.0, 0) == 0
 
 
 def test_empty_problems_return_ok_without_a_device():

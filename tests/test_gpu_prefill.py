@@ -74,6 +74,21 @@ def test_fp32_variants():
         assert_close_f32(host(out), want, f"fp32 W={window} theta={theta}")
 
 
+def test_fp32_unsplit():
+    """Above 256 CTAs of 16 rows the fp32 kernel keeps each row tile's keys in
+    one CTA (smaller problems split them over four and merge): B2 T700 Hq8
+    (704 CTAs), packed segments with sinks, a window."""
+    rng = philox(710)
+    B, T, Hq, Hkv, d = 2, 700, 8, 2, 64
+    q, k, v = (rng.standard_normal((B, T, H, d), dtype=np.float32) for H in (Hq, Hkv, Hkv))
+    seg, sink = packed_segments(rng, B, T, 2, 4, 60, 5, 40)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
+    out = nd().nd_swa_sink_prefill(dev(q), dev(k), dev(v), dev(seg), dev(sink), 100, lse=lse)
+    want, wlse = oracle.swa_sink_prefill(q, k, v, seg, sink, 100)
+    assert_close_f32(host(out), want, "fp32 unsplit")
+    np.testing.assert_allclose(host(lse).transpose(0, 2, 1), wlse, atol=1e-4, rtol=0)
+
+
 # ---------------------------------------------------------------- bf16
 
 @pytest.mark.parametrize("d", [64, 128])
