@@ -429,6 +429,15 @@ ND_API int nd_compressed_decode_step(const void *q, const nd_compressed_cache *c
  *
  * dtype ND_F32 runs on CUDA cores in fp32; ND_BF16 runs on the tensor cores
  * (bf16 operands, fp32 accumulation).  head_dim 64 or 128.
+ *
+ * workspace: device memory of at least nd_swa_sink_prefill_workspace_size()
+ * bytes, 16-byte aligned, owned by the caller and scratch between calls: the
+ * rotated copies when rope_theta != 0 (q too on the fp32 path) and the angle
+ * table; bf16: the tile records and tile plan (nd_swa_sink_prefill_tiles
+ * reads the plan back), and the pooled blocks when the call pools; fp32
+ * problems of at most 256 sixteen-row CTAs (batch x n_q_heads x
+ * ceil(T / 16)): the partial softmax states of the four CTAs that share each
+ * row tile's keys.  A size of 0 means no workspace is needed (NULL allowed).
  */
 ND_API size_t nd_swa_sink_prefill_workspace_size(nd_dtype dtype, int batch, int T,
                                           int n_q_heads, int n_kv_heads,
