@@ -361,21 +361,42 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
   const int n_tok = min(kFillTokens, n_kept - c0), Hkv = c.n_kv_heads;
   const int n_rows = n_tok * Hkv * 2, nslot = c.sink_cap + c.ring_cap;
   const int sub = lane / (D / 8);
+  // row r = (token j, head h, K or V) = 2 (j Hkv + h) + (r & 1).  With two
+  // or more rows per warp-iteration (RPI even) a lane's rows advance by
+  // whole (token, head) pairs and keep their K/V side, so each lane divides
+  // once per iteration and steps its (j, h) from there.
   for (int r0 = warp * RPI * kUnroll; r0 < n_rows; r0 += NW * RPI * kUnroll) {
     uint4 w[kUnroll];
-    int rows[kUnroll], slots[kUnroll];
+    int rows[kUnroll], slots[kUnroll], heads[kUnroll];
+    int j = 0, h = 0;
+    if constexpr (RPI >= 2) {
+      const int pair0 = (r0 >> 1) + (sub >> 1);
+      j = pair0 / Hkv;
+      h = pair0 - j * Hkv;
+    }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int r = r0 + u * RPI + sub;
+      if constexpr (RPI == 1) {  // (head_dim 256: one row per iteration)
+        j = (r >> 1) / Hkv;
+        h = (r >> 1) - j * Hkv;
+      }
       rows[u] = r;
+      heads[u] = h;
       w[u] = make_uint4(0, 0, 0, 0);
       slots[u] = 0;
       if (r < n_rows) {
-        const int j = r / (2 * Hkv), h = (r >> 1) % Hkv;
         const int t = s_pos[j];
         slots[u] = s_slot[j];
         const uint16_t *src = ((r & 1) ? p.v : p.k) + ((size_t(b) * p.T + t) * Hkv + h) * D;
         w[u] = *reinterpret_cast<const uint4 *>(src + (lane % (D / 8)) * 8);
+      }
+      if constexpr (RPI >= 2) {
+        h += RPI / 2;  // this lane's next row: RPI/2 pairs on, same side
+        while (h >= Hkv) {
+          h -= Hkv;
+          ++j;
+        }
       }
     }
 #pragma unroll
@@ -385,7 +406,7 @@ __global__ void __launch_bounds__(kFillThreads) kv_fill_kernel(const FillParams 
       const uint2 q8 = quant8(w[u], scale);
       const int r = rows[u];
       if (r < n_rows) {
-        const int h = (r >> 1) % Hkv, ch = (lane % (D / 8)) * 8;
+        const int h = heads[u], ch = (lane % (D / 8)) * 8;
         const bool is_v = r & 1;
         const size_t row = (size_t(e) * Hkv + h) * nslot + slots[u];
         *reinterpret_cast<uint2 *>((is_v ? c.v_codes : c.k_codes) + row * D + ch) = q8;

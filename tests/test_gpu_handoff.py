@@ -62,7 +62,7 @@ def compare_filled(cache, ref, rows):
             np.testing.assert_array_equal(got[f][e][:, occ], getattr(ref, f)[e][:, occ], err_msg=f"{f} row {e}")
 
 
-@pytest.mark.parametrize("d,Hkv", [(64, 2), (128, 3), (32, 1)])
+@pytest.mark.parametrize("d,Hkv", [(64, 2), (128, 3), (32, 1), (64, 3), (256, 2)])
 def test_fill_matches_oracle_replay(d, Hkv):
     rng = philox(3000 + d)
     B, T, S, W = 2, 700, 160, 48
