@@ -128,11 +128,14 @@ __device__ __forceinline__ float2 rot_cs(double pos, double freq) {
 // <= 2.3e-5 (|x/scale| <= 127.5 for codec inputs), so rint(p) equals
 // rint(fl(x/scale)) unless p lies within that distance of a half-integer;
 // within 1e-4 of one (or for scales so small that 1/scale could overflow) the
-// quotient is taken with the IEEE divide.  inv = __frcp_rn(scale).
+// quotient is taken with the IEEE divide.  inv = __frcp_rn(scale).  The
+// distance of p from the nearest half-integer is | |p - rint(p)| - 1/2 |;
+// p - rint(p) and the subtraction of 1/2 are exact in fp32 wherever that
+// distance is below 1/4, so rint(p) serves both the test and the result.
 __device__ __forceinline__ float codec_rint(float x, float scale, float inv) {
   const float p = x * inv;
-  const float f = p - floorf(p);
-  if (fabsf(f - 0.5f) > 1e-4f && scale >= 1e-30f) return rintf(p);
+  const float r = rintf(p);
+  if (fabsf(fabsf(p - r) - 0.5f) > 1e-4f && scale >= 1e-30f) return r;
   return rintf(__fdiv_rn(x, scale));
 }
 
