@@ -196,13 +196,17 @@ __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint
 // and an SM keeps more loads in flight.  The sums, the mean and the rotation
 // follow pool_kernel's order.
 constexpr int kPoolJ = 2;
+// A CTA takes the same kPoolJ blocks of up to kPoolB sequences: the midpoint
+// angles depend on the block only, so they are built once for all of them
+// (the double-precision reduction is the costly part of the pass).
+constexpr int kPoolB = 4;
 __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const uint16_t *v,
-                                                       uint16_t *pk, uint16_t *pv, int T, int H,
+                                                       uint16_t *pk, uint16_t *pv, int B, int T, int H,
                                                        int D, int block, int apply_rope, Freqs fr) {
   __shared__ float2 cs[kPoolJ][kMaxHalf];
   const int nblk = T / block, n_grp = (nblk + kPoolJ - 1) / kPoolJ;
-  const int b = blockIdx.x / n_grp, j0 = (blockIdx.x % n_grp) * kPoolJ;
-  const int nj = min(kPoolJ, nblk - j0);
+  const int b0 = (blockIdx.x / n_grp) * kPoolB, j0 = (blockIdx.x % n_grp) * kPoolJ;
+  const int nj = min(kPoolJ, nblk - j0), nbt = min(kPoolB, B - b0);
   const int half = D / 2, groups = half / 8;
   const int per_kv = nj * H * groups;
   if (apply_rope)
@@ -213,9 +217,10 @@ __global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const 
     }
   __syncthreads();
   const float fblock = float(block);
-  for (int idx = threadIdx.x; idx < 2 * per_kv; idx += blockDim.x) {
-    const bool is_v = idx >= per_kv;
-    const int w = is_v ? idx - per_kv : idx;
+  for (int idx = threadIdx.x; idx < 2 * nbt * per_kv; idx += blockDim.x) {
+    const int bi = idx / (2 * per_kv), wi = idx % (2 * per_kv), b = b0 + bi;
+    const bool is_v = wi >= per_kv;
+    const int w = is_v ? wi - per_kv : wi;
     const int g = w % groups, rest = w / groups;
     const int h = rest % H, jj = rest / H;
     const int i0 = g * 8, j = j0 + jj;
@@ -648,9 +653,9 @@ cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T,
                                           15) == 0;
   if (vec) {
     const int n_grp = (nblk + kPoolJ - 1) / kPoolJ;
-    pool_vec_kernel<<<batch * n_grp, 256, 0, stream>>>(
+    pool_vec_kernel<<<((batch + kPoolB - 1) / kPoolB) * n_grp, 256, 0, stream>>>(
         static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), static_cast<uint16_t *>(pk),
-        static_cast<uint16_t *>(pv), T, n_heads, head_dim, block, theta != 0.f ? 1 : 0, fr);
+        static_cast<uint16_t *>(pv), batch, T, n_heads, head_dim, block, theta != 0.f ? 1 : 0, fr);
     return cudaGetLastError();
   }
   pool_kernel<<<batch * nblk, 128, 0, stream>>>(
