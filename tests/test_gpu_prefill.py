@@ -245,7 +245,7 @@ def test_rope_matches_oracle(d):
 
 
 @pytest.mark.parametrize("block,T,d", [(4, 4096, 64), (1, 100, 64), (3, 101, 64), (8, 64, 64), (4, 1000, 128),
-                                       (5, 203, 48), (64, 4096, 64), (2, 50, 62)])
+                                       (5, 203, 48), (64, 4096, 64), (2, 50, 62), (1, 8192, 64)])
 def test_compress_pool_matches_oracle(block, T, d):
     # d = 62 (not a multiple of 16) takes the scalar pooling kernel, the rest
     # the 16-byte one; T % block leaves a dropped tail in several cases
