@@ -168,6 +168,32 @@ __device__ __forceinline__ float ldsf(uint32_t a) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 lds64f(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+// The NG group scales of one slot, which sit together in the stage (16 or 8
+// bytes).  At head_dim 128 one 16-byte load replaces four 4-byte loads for
+// each of the eight K and V scale rows a thread reads per step (the kernel
+// is issue-bound there: 4-5 points of HBM at B128-B512); at head_dim 64 the
+// two 4-byte loads stay, since the 8-byte form adds a spill to the 96-register
+// builds.
+template <int NG>
+__device__ __forceinline__ void lds_scales(uint32_t a, float *s) {
+  if constexpr (NG == 4) {
+    const float4 v = lds128f(a);
+    s[0] = v.x, s[1] = v.y, s[2] = v.z, s[3] = v.w;
+  } else {
+    s[0] = ldsf(a);
+    s[1] = ldsf(a + 4);
+  }
+}
 
 // ST: cp.async stages per warp (ST - 1 steps in flight).  d = 128 has two
 // builds: 4 stages at three CTAs per SM, and 5 stages at two CTAs per SM for
@@ -402,6 +428,9 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : (NW ==
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int row = 8 * j + g;
+      float ks0[NG], ks1[NG];  // K scales of this thread's two columns
+      lds_scales<NG>(st + 2 * S::kCodes + (8 * j + 2 * t) * NG * 4, ks0);
+      lds_scales<NG>(st + 2 * S::kCodes + (8 * j + 2 * t + 1) * NG * 4, ks1);
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
         const uint2 kw = lds64(st + swz(uint32_t(row * D + 32 * grp + 8 * t)));
@@ -411,9 +440,8 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : (NW ==
                       codes_to_half2(w0, kSelBytes01), codes_to_half2(w0, kSelBytes23));
         mma_f16_16816(d0, d1, d2, d3, qa[grp][1][0], 0u, qa[grp][1][1], 0u,
                       codes_to_half2(w1, kSelBytes01), codes_to_half2(w1, kSelBytes23));
-        const uint32_t ksc = st + 2 * S::kCodes + (8 * j + 2 * t) * NG * 4 + grp * 4;
-        sc[2 * j] = fmaf(ldsf(ksc), d0, sc[2 * j]);
-        sc[2 * j + 1] = fmaf(ldsf(ksc + NG * 4), d1, sc[2 * j + 1]);
+        sc[2 * j] = fmaf(ks0[grp], d0, sc[2 * j]);
+        sc[2 * j + 1] = fmaf(ks1[grp], d1, sc[2 * j + 1]);
       }
     }
     // ---- online softmax for head g (log2 domain)
@@ -441,12 +469,16 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : (NW ==
     float vsc[NG][4];
     float vm = 0.f;
 #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float vs_i[NG];
+      lds_scales<NG>(st + 2 * S::kCodes + S::kScales + col[i] * NG * 4, vs_i);
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) vsc[grp][i] = vs_i[grp];
+    }
+#pragma unroll
     for (int grp = 0; grp < NG; ++grp)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        vsc[grp][i] = ldsf(st + 2 * S::kCodes + S::kScales + col[i] * NG * 4 + grp * 4);
-        vm = fmaxf(vm, vis[i] ? vsc[grp][i] : 0.f);
-      }
+      for (int i = 0; i < 4; ++i) vm = fmaxf(vm, vis[i] ? vsc[grp][i] : 0.f);
     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
     vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
     const int e_step = vm > 0.f ? 14 - int(kLazyLog2) - ilog2_floor(vm) : 127;

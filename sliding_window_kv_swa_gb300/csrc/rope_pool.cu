@@ -189,18 +189,20 @@ __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint
 }
 
 // Vector form of the pooling (head_dim a multiple of 16, 16-byte aligned
-// rows): a CTA takes kPoolJ consecutive pooled blocks of one sequence and
-// builds their midpoint angles in shared memory; each thread pools 8 channel
-// pairs (i0..i0+7 and i0+half..) of one (block, head) of K or of V with
-// 16-byte loads -- K and V on separate threads, so a thread holds 16 sums
-// and an SM keeps more loads in flight.  The sums, the mean and the rotation
-// follow pool_kernel's order.
-constexpr int kPoolJ = 2;
+// rows): a CTA of 128 threads takes kPoolJ pooled blocks and builds their
+// midpoint angles in shared memory; each thread pools 8 channel pairs
+// (i0..i0+7 and i0+half..) of one (block, head) of K or of V with 16-byte
+// loads -- K and V on separate threads, so a thread holds 16 sums and an SM
+// keeps more loads in flight.  One block per CTA makes many small CTAs that
+// all fit at once and spread evenly over the SMs (at two blocks per 256-thread
+// CTA, some SMs held four CTAs and others three, and the pass ran 13% longer).
+// The sums, the mean and the rotation follow pool_kernel's order.
+constexpr int kPoolJ = 1;
 // A CTA takes the same kPoolJ blocks of up to kPoolB sequences: the midpoint
 // angles depend on the block only, so they are built once for all of them
 // (the double-precision reduction is the costly part of the pass).
 constexpr int kPoolB = 4;
-__global__ void __launch_bounds__(256) pool_vec_kernel(const uint16_t *k, const uint16_t *v,
+__global__ void __launch_bounds__(128, 8) pool_vec_kernel(const uint16_t *k, const uint16_t *v,
                                                        uint16_t *pk, uint16_t *pv, int B, int T, int H,
                                                        int D, int block, int apply_rope, Freqs fr) {
   __shared__ float2 cs[kPoolJ][kMaxHalf];
@@ -380,13 +382,16 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
 // single cp.async.bulk; a ring of kBulkStages chunks keeps the next ones in
 // flight while all threads work from shared memory: K rows rotated and
 // stored, K and V pooled, pooled K rotated at the block midpoint (one thread
-// per (block, head, 8 channel pairs) of K or of V).  The CTAs are persistent
+// per (block, head, 8 channel pairs) of K or of V, so a CTA has as many
+// threads as a chunk has such lanes, up to 256).  The CTAs are persistent
 // and walk the chunks with a stride of the grid, then rotate the positions
-// outside whole blocks.  Sums, means, angles and roundings are those of
-// pool_rope_kernel, so the results are the same bits.
+// outside whole blocks.  A chunk is one pooled block: small chunks and small
+// CTAs put four CTAs on an SM, which measured faster than chunks of four
+// blocks at two CTAs per SM.  Sums, means, angles and roundings are those
+// of pool_rope_kernel, so the results are the same bits.
 constexpr int kBulkStages = 3;
 constexpr int kBulkBytes = 16384;  // K (and V) bytes per chunk, at most
-constexpr int kBulkMaxJ = 4;       // pooled blocks per chunk, at most
+constexpr int kBulkMaxJ = 1;       // pooled blocks per chunk, at most
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
@@ -582,10 +587,11 @@ cudaError_t launch_pool_rope(const void *k, const void *v, void *k_rot, void *pk
     int sms = 0, dev = 0, per_sm = 0;
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pool_rope_bulk_kernel, 256, smem);
+    const int lanes = nj_max * n_heads * head_dim / 8, threads = std::min(256, (lanes + 31) / 32 * 32);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pool_rope_bulk_kernel, threads, smem);
     if (e != cudaSuccess) return e;
     const int grid = std::min(n_chunks, std::max(1, per_sm) * sms);
-    return launch_pdl(pool_rope_bulk_kernel, dim3(unsigned(grid)), dim3(256), size_t(smem), stream,
+    return launch_pdl(pool_rope_bulk_kernel, dim3(unsigned(grid)), dim3(unsigned(threads)), size_t(smem), stream,
                       static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
                       static_cast<uint16_t *>(k_rot), static_cast<uint16_t *>(pk), static_cast<uint16_t *>(pv), batch,
                       T, n_heads, head_dim, block, pos0, nj_max, static_cast<const float2 *>(cs),
@@ -653,7 +659,7 @@ cudaError_t launch_compress_pool(const void *k, const void *v, int batch, int T,
                                           15) == 0;
   if (vec) {
     const int n_grp = (nblk + kPoolJ - 1) / kPoolJ;
-    pool_vec_kernel<<<((batch + kPoolB - 1) / kPoolB) * n_grp, 256, 0, stream>>>(
+    pool_vec_kernel<<<((batch + kPoolB - 1) / kPoolB) * n_grp, 128, 0, stream>>>(
         static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), static_cast<uint16_t *>(pk),
         static_cast<uint16_t *>(pv), batch, T, n_heads, head_dim, block, theta != 0.f ? 1 : 0, fr);
     return cudaGetLastError();

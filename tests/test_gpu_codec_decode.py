@@ -208,11 +208,12 @@ def test_decode_large_magnitudes_and_tiny_values():
         assert err < 1e-2, (mag, err)
 
 
-@pytest.mark.parametrize("B", [32, 512])
+@pytest.mark.parametrize("B", [32, 64, 128, 512])
 def test_decode_sweep_full_size_all_sequences(B):
     """Configuration of the large-batch sweep (Hq32 Hkv8 d128, 1024 sinks + 256
     ring) at full size, in the bench's launch configuration: every sequence
-    (out and lse) against the oracle."""
+    (out and lse) against the oracle.  B64 and B128 leave a partial last wave
+    of (sequence, KV head) pairs, B32 less than one wave."""
     rng = philox(500 + B)
     Hq, Hkv, d, S, W = 32, 8, 128, 1024, 256
     kc, ks, vc, vs = random_codes(rng, B, Hkv, S + W, d)
