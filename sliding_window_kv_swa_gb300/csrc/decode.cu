@@ -297,10 +297,28 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : (NW ==
   // column chunk lane % (D/16); fixed for every step
   constexpr int kChunks = kStep * D / 16, kPerLane = kChunks / 32, kRowStride = 32 * 16 / D;
   const int my_row0 = lane / (D / 16), my_ch = lane % (D / 16);
+  // this lane's sources at slot 0 (a whole step adds base rows)
+  const int8_t *kc_lane = kc + size_t(my_row0) * D + my_ch * 16;
+  const int8_t *vc_lane = vc + size_t(my_row0) * D + my_ch * 16;
+  const float *sc_lane = ((lane >> 4) ? vs : ks) + size_t(lane & 15) * NG;
   auto issue = [&](int n) {
     if (n < n_steps) {
       const int base = base_of(n);
       const uint32_t st = my_stages + (n % kStages) * S::kBytes;
+      if (D == 128 && base + kStep <= v_end) {  // a whole step: no slot past the range
+        const size_t boff = size_t(base) * D;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const uint32_t off = swz(uint32_t((my_row0 + k * kRowStride) * D + my_ch * 16));
+          cp_async16(st + off, kc_lane + boff + k * kRowStride * D);
+          cp_async16(st + S::kCodes + off, vc_lane + boff + k * kRowStride * D);
+        }
+        const uint32_t dst = st + 2 * S::kCodes + (lane >> 4) * S::kScales + (lane & 15) * NG * 4;
+        if constexpr (NG == 4) cp_async16(dst, sc_lane + size_t(base) * NG);
+        else cp_async8(dst, sc_lane + size_t(base) * NG);
+        cp_async_commit();
+        return;
+      }
 #pragma unroll
       for (int k = 0; k < kPerLane; ++k) {
         const int row = my_row0 + k * kRowStride;
