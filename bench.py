@@ -768,7 +768,7 @@ def bench_pool_rope(torch, nd, steps, warmup, pk, dist=None, block=4):
     return dict(config=f"pooling fused with K's rotation, B{B} T{T} H{H} d{d} b{block}: read K and V once, write "
                        f"rotated K and the pooled blocks (+ the 0.5 MB angle table)",
                 ms_per_step=t, bytes_per_launch=per, replicas=replicas,
-                roofline=roofline("hbm", per, t, pk["hbm"], "GB/s", "rope_table_kernel + pool_rope_kernel", pk["src"],
+                roofline=roofline("hbm", per, t, pk["hbm"], "GB/s", "rope_table_kernel + pool_rope_bulk_kernel", pk["src"],
                                   load_traffic(f"pool_rope@compressed_b{block}")))
 
 
