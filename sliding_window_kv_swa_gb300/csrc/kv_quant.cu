@@ -183,16 +183,28 @@ __device__ __forceinline__ uint2 quant8(const uint4 w, float &scale) {
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   scale = __fdiv_rn(amax, 127.0f);
+  if (amax == 0.f) return make_uint2(0u, 0u);
   const float inv = __frcp_rn(scale);
-  uint32_t lo = 0, hi = 0;
+  // Round-to-integer by adding and subtracting 1.5 * 2^23 (the classic
+  // "magic number" rounding): for |p| < 2^22 the sum t has a unit ulp, so it
+  // is p rounded to the nearest integer (ties to even, as rint), and t's low
+  // mantissa byte is that integer's two's-complement byte -- the code.  The
+  // decision to trust p is codec_rint's; outside its tie band, with a normal
+  // scale, |p| <= 127 * (1 + 3 * 2^-24) < 127.5, so the code needs no clamp.
+  // Inside the band the IEEE quotient decides (and is clamped), as there.
+  uint32_t wd[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float r = 0.f;
-    if (amax != 0.f) r = fminf(fmaxf(codec_rint(x[i], scale, inv), -127.f), 127.f);
-    const uint32_t cb = uint32_t(int(r)) & 0xffu;
-    if (i < 4) lo |= cb << (8 * i);
-    else hi |= cb << (8 * (i - 4));
+    const float p = __fmul_rn(x[i], inv);
+    const float t = __fadd_rn(p, 12582912.0f);
+    const float r = __fsub_rn(t, 12582912.0f);
+    wd[i] = __float_as_uint(t);
+    if (!(fabsf(fabsf(__fsub_rn(p, r)) - 0.5f) > 1e-4f && scale >= 1e-30f))
+      wd[i] = uint32_t(int(fminf(fmaxf(rintf(__fdiv_rn(x[i], scale)), -127.f), 127.f)));
   }
+  // byte 0 of each word, four to a register
+  const uint32_t lo = prmt(prmt(wd[0], wd[1], 0x0040u), prmt(wd[2], wd[3], 0x0040u), 0x5410u);
+  const uint32_t hi = prmt(prmt(wd[4], wd[5], 0x0040u), prmt(wd[6], wd[7], 0x0040u), 0x5410u);
   return make_uint2(lo, hi);
 }
 

@@ -87,6 +87,33 @@ def test_fill_matches_oracle_replay(d, Hkv):
     assert int(host(cache.sink_len)[n - 1]) == 5
 
 
+@pytest.mark.parametrize("T", [4099, 8200])
+def test_fill_rows_longer_than_one_planning_pass(T):
+    """Batch rows longer than the planner's single pass of 4096 positions
+    (both walks then loop), with and without a whole number of 4-position
+    quads per row."""
+    rng = philox(3050 + T)
+    B, Hkv, d, S, W = 1, 1, 32, 64, 96
+    kb, kf = normal_bf16(rng, (B, T, Hkv, d))
+    vb, vf = normal_bf16(rng, (B, T, Hkv, d))
+    seg = np.ones((B, T), np.int32)
+    seg[0, T // 3:] = 2
+    seg[0, T - 50:] = 0                                   # trailing padding
+    sink = np.zeros((B, T), np.uint8)
+    sink[0, :40] = 1                                      # segment 1: 40 sinks
+    sink[0, T // 3:T // 3 + 70] = 1                       # segment 2: 70 sinks > S (rejected past 64)
+    entries = [(0, 1), (0, 2)]
+    src_row = np.array([b for b, _ in entries], np.int32)
+    src_seg = np.array([s for _, s in entries], np.int32)
+    cache = nd().KVCache.empty(len(entries), Hkv, d, S, W)
+    nd().nd_kv_cache_from_prefill(cache, dev_bf16(kb), dev_bf16(vb), dev(src_row), dev(seg), dev(sink),
+                                  dev(src_seg))
+    assert nd().nd_device_errors(clear=True) == 2          # segment 2's rejected sinks (metadata flag)
+    ref, rejected = replay(kf, vf, seg, sink, entries, Hkv, d, S, W)
+    assert rejected == [0, 6]
+    compare_filled(cache, ref, list(range(len(entries))))
+
+
 def test_fill_rejections_and_scattered_segments():
     """Segment ids that repeat out of order (a segment's tokens are not one
     run), sink flags after the ring has started (rejected), sink prefixes
