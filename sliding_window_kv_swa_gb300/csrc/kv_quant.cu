@@ -231,7 +231,8 @@ struct FillParams {
 // a token, sink tokens are rejected.  Two walks over the batch row, four
 // positions per thread per pass: totals and the first ring token's rank,
 // then every token's rank; the kept tokens' (position, slot) pairs go to the
-// plan, the row's metadata to the cache.
+// plan, the row's metadata to the cache.  A row of at most one pass keeps
+// its flags and prefix sums in registers for the second walk.
 __global__ void __launch_bounds__(kPlanThreads) kv_fill_plan_kernel(const FillParams p) {
   constexpr int NW = kPlanThreads / 32, kPer = 4, kPass = kPer * kPlanThreads;
   __shared__ int s_wsum[NW][2];
@@ -253,10 +254,29 @@ __global__ void __launch_bounds__(kPlanThreads) kv_fill_plan_kernel(const FillPa
   __syncthreads();
   const int32_t *sg = p.seg_ids ? p.seg_ids + size_t(b) * p.T : nullptr;
   const uint8_t *sk = p.sink ? p.sink + size_t(b) * p.T : nullptr;
+  // a thread's four positions are consecutive: one 16-byte load of their
+  // segment ids and one 4-byte load of their sink flags where the row allows
+  const bool vec = (p.T % kPer) == 0 && (reinterpret_cast<uintptr_t>(p.seg_ids) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(p.sink) & 3) == 0;
   auto load_flags = [&](int base, bool *in, bool *snk) {
+    const int t0 = base + kPer * tid;
+    if (vec && t0 + kPer <= p.T) {
+      int sv[kPer] = {seg, seg, seg, seg};
+      if (sg) {
+        const int4 q = *reinterpret_cast<const int4 *>(sg + t0);
+        sv[0] = q.x, sv[1] = q.y, sv[2] = q.z, sv[3] = q.w;
+      }
+      const uint32_t f = sk ? *reinterpret_cast<const uint32_t *>(sk + t0) : 0u;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        in[j] = sv[j] == seg;
+        snk[j] = in[j] && ((f >> (8 * j)) & 0xffu) != 0u;
+      }
+      return;
+    }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int t = base + kPer * tid + j;
+      const int t = t0 + j;
       in[j] = t < p.T && (!sg || sg[t] == seg);
       snk[j] = in[j] && sk && sk[t];
     }
@@ -279,6 +299,11 @@ __global__ void __launch_bounds__(kPlanThreads) kv_fill_plan_kernel(const FillPa
     }
     __syncthreads();  // s_wsum is reused by the next call
   };
+  // a row of at most kPass positions is one pass: its flags and prefix sums
+  // serve the second walk as they are
+  const bool one_pass = p.T <= kPass;
+  bool in1[kPer], snk1[kPer];
+  int ea1 = 0, es1 = 0;
   int tot_seg = 0, tot_snk = 0;
   for (int base = 0; base < p.T; base += kPass) {
     bool in[kPer], snk[kPer];
@@ -292,6 +317,11 @@ __global__ void __launch_bounds__(kPlanThreads) kv_fill_plan_kernel(const FillPa
     }
     int ea, es, ta, ts;
     block_scan(a, s, ea, es, ta, ts);
+    if (one_pass) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) in1[j] = in[j], snk1[j] = snk[j];
+      ea1 = ea, es1 = es;
+    }
     if (first_local >= 0) atomicMin(&s_first_r, tot_seg + ea + first_local);
     tot_seg += ta;
     tot_snk += ts;
@@ -315,12 +345,18 @@ __global__ void __launch_bounds__(kPlanThreads) kv_fill_plan_kernel(const FillPa
   int carry_seg = 0, carry_snk = 0;
   for (int base = 0; base < p.T; base += kPass) {
     bool in[kPer], snk[kPer];
-    load_flags(base, in, snk);
-    int a = 0, s = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) a += in[j], s += snk[j];
     int ea, es, ta, ts;
-    block_scan(a, s, ea, es, ta, ts);
+    if (one_pass) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) in[j] = in1[j], snk[j] = snk1[j];
+      ea = ea1, es = es1, ta = tot_seg, ts = tot_snk;
+    } else {
+      load_flags(base, in, snk);
+      int a = 0, s = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) a += in[j], s += snk[j];
+      block_scan(a, s, ea, es, ta, ts);
+    }
     int rank = carry_seg + ea, rsnk = carry_snk + es;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
