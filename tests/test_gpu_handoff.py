@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from gpu_util import assert_close_bf16, dev, dev_bf16, host, need_gpu, no_device_errors
-from workloads import normal_bf16, packed_prefill, packed_segments, philox
+from workloads import bf16_bits_to_f32, normal_bf16, packed_prefill, packed_segments, philox, to_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -112,6 +112,50 @@ def test_fill_rows_longer_than_one_planning_pass(T):
     ref, rejected = replay(kf, vf, seg, sink, entries, Hkv, d, S, W)
     assert rejected == [0, 6]
     compare_filled(cache, ref, list(range(len(entries))))
+
+
+def test_fill_codes_at_and_beside_half_integer_quotients():
+    """The handoff's quantiser on groups whose quotients x / scale sit exactly
+    on half-integers (ties to even) and one or two bf16 steps either side,
+    at several scales, plus a group whose scale is subnormal (the quotient
+    path and its clamp) and an all-zero group: codes and scales bit for bit
+    against the oracle's codec, through a whole-row handoff."""
+    groups = []
+    for k in (-20, -3, 0, 5, 17):
+        sc = 2.0 ** k
+        for n in range(-127, 127, 3):
+            base = (n + 0.5) * sc
+            vals = [base]
+            b = to_bf16_bits(np.array([base], np.float32)).astype(np.int32)[0]
+            for dlt in (-2, -1, 1, 2):
+                vals.append(float(bf16_bits_to_f32(np.array([b + dlt], np.uint16))[0]))
+            g = np.zeros(32, np.float32)
+            g[0] = 127.0 * sc
+            g[1:1 + len(vals)] = vals
+            g[6:] = np.linspace(-126.0, 126.0, 26, dtype=np.float32) * sc
+            groups.append(g)
+    tiny = np.zeros(32, np.float32)
+    tiny[:8] = np.float32(2.0 ** -130) * np.arange(1, 9, dtype=np.float32)   # subnormal scale
+    tiny[8:16] = -tiny[:8]
+    groups += [tiny, np.zeros(32, np.float32)]
+    d = 128
+    while len(groups) % (d // 32):
+        groups.append(groups[0])
+    x = np.stack(groups).reshape(1, -1, 1, d)                   # [B=1][T][Hkv=1][d]
+    bits = to_bf16_bits(x)
+    xf = bf16_bits_to_f32(bits)
+    T = x.shape[1]
+    S, W = 8, T + 8                                            # every token lands in the ring, in order
+    cache = nd().KVCache.empty(1, 1, d, S, W)
+    nd().nd_kv_cache_from_prefill(cache, dev_bf16(bits), dev_bf16(bits[:, ::-1].copy()),
+                                  dev(np.zeros(1, np.int32)))
+    wc, ws = oracle.quant_g32(xf[0, :, 0])
+    vc, vs = oracle.quant_g32(xf[0, ::-1, 0])
+    np.testing.assert_array_equal(host(cache.k_codes)[0, 0, S:S + T], wc)
+    np.testing.assert_array_equal(host(cache.k_scale)[0, 0, S:S + T].view(np.uint32), ws.view(np.uint32))
+    np.testing.assert_array_equal(host(cache.v_codes)[0, 0, S:S + T], vc)
+    np.testing.assert_array_equal(host(cache.v_scale)[0, 0, S:S + T].view(np.uint32), vs.view(np.uint32))
+    assert int(host(cache.ring_len)[0]) == T and int(host(cache.ring_start)[0]) == 0
 
 
 def test_fill_rejections_and_scattered_segments():
