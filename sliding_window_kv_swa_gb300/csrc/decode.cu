@@ -173,11 +173,6 @@ __device__ __forceinline__ float4 lds128f(uint32_t a) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
   return v;
 }
-__device__ __forceinline__ float2 lds64f(uint32_t a) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-  return v;
-}
 // The NG group scales of one slot, which sit together in the stage (16 or 8
 // bytes).  At head_dim 128 one 16-byte load replaces four 4-byte loads for
 // each of the eight K and V scale rows a thread reads per step (the kernel
@@ -305,7 +300,10 @@ __global__ void __launch_bounds__(NW * 32, D == 128 ? (ST == 4 ? 3 : 2) : (NW ==
     if (n < n_steps) {
       const int base = base_of(n);
       const uint32_t st = my_stages + (n % kStages) * S::kBytes;
-      if (D == 128 && base + kStep <= v_end) {  // a whole step: no slot past the range
+      // a whole step (no slot past the range) needs no per-slot clamp; at
+      // head_dim 64 the extra lane pointers would spill in the 96-register
+      // builds, so there every step takes the clamped form below
+      if (D == 128 && base + kStep <= v_end) {
         const size_t boff = size_t(base) * D;
 #pragma unroll
         for (int k = 0; k < kPerLane; ++k) {
