@@ -403,8 +403,9 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
 // and walk the chunks with a stride of the grid, then rotate the positions
 // outside whole blocks.  A chunk is one pooled block: small chunks and small
 // CTAs put four CTAs on an SM, which measured faster than chunks of four
-// blocks at two CTAs per SM; two stages measured faster than three.  Sums, means, angles and roundings are those
-// of pool_rope_kernel, so the results are the same bits.
+// blocks at two CTAs per SM; two stages measured faster than three.  Sums,
+// means, angles and roundings are those of pool_rope_kernel, so the results
+// are the same bits.
 constexpr int kBulkStages = 2;
 constexpr int kBulkBytes = 16384;  // K (and V) bytes per chunk, at most
 constexpr int kBulkMaxJ = 1;       // pooled blocks per chunk, at most
