@@ -82,6 +82,17 @@ __global__ void rope_table_kernel(float2 *cs, int T, int half, Freqs fr, int wai
   if (!wait_first) pdl_wait();
 }
 
+// The block mean's divide, x / block, bit for bit: for a power-of-two block
+// the product with the exact reciprocal 2^-k is the same correctly rounded
+// value (one multiply instead of an IEEE divide per channel).
+struct BlockMean {
+  float f, r;
+  bool pow2;
+  __device__ explicit BlockMean(int block)
+      : f(float(block)), r(1.f / float(block)), pow2((block & (block - 1)) == 0) {}
+  __device__ float operator()(float x) const { return pow2 ? __fmul_rn(x, r) : __fdiv_rn(x, f); }
+};
+
 __device__ __forceinline__ void ld8(const uint16_t *p, float *x) {
   const uint4 w = *reinterpret_cast<const uint4 *>(p);
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -171,10 +182,11 @@ __global__ void __launch_bounds__(128) pool_kernel(const uint16_t *k, const uint
       va += __uint_as_float(uint32_t(v[row + i]) << 16);
       vb += __uint_as_float(uint32_t(v[row + i + half]) << 16);
     }
-    ka /= float(block);
-    kb /= float(block);
-    va /= float(block);
-    vb /= float(block);
+    const BlockMean mean(block);
+    ka = mean(ka);
+    kb = mean(kb);
+    va = mean(va);
+    vb = mean(vb);
     float ko = ka, ko2 = kb;
     if (apply_rope) {
       const float2 c = cs[i];
@@ -234,7 +246,7 @@ __global__ void __launch_bounds__(128, 8) pool_vec_kernel(const uint16_t *k, con
       cs[jj][i] = rot_cs(double(mid), fr.f[i]);
     }
   __syncthreads();
-  const float fblock = float(block);
+  const BlockMean mean(block);
   for (int idx = threadIdx.x; idx < 2 * nbt * per_kv; idx += blockDim.x) {
     const int bi = idx / (2 * per_kv), wi = idx % (2 * per_kv), b = b0 + bi;
     const bool is_v = wi >= per_kv;
@@ -263,8 +275,8 @@ __global__ void __launch_bounds__(128, 8) pool_vec_kernel(const uint16_t *k, con
     float ya[8], yb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      sa[e] /= fblock;
-      sb[e] /= fblock;
+      sa[e] = mean(sa[e]);
+      sb[e] = mean(sb[e]);
       ya[e] = sa[e];
       yb[e] = sb[e];
       if (apply_rope && !is_v) {
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
     return;
   }
   const int j0 = grp * kPoolJ, nj = min(kPoolJ, nblk - j0);
-  const float fblock = float(block);
+  const BlockMean mean(block);
   const int per_kv = nj * H * groups;
   for (int idx = threadIdx.x; idx < 2 * per_kv; idx += blockDim.x) {
     const bool is_v = idx >= per_kv;
@@ -379,8 +391,8 @@ __global__ void __launch_bounds__(256) pool_rope_kernel(const uint16_t *__restri
     float ya[8], yb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      sa[e] /= fblock;
-      sb[e] /= fblock;
+      sa[e] = mean(sa[e]);
+      sb[e] = mean(sb[e]);
       ya[e] = sa[e];
       yb[e] = sb[e];
     }
@@ -458,6 +470,9 @@ __global__ void __launch_bounds__(256) pool_rope_bulk_kernel(const uint16_t *__r
   if (threadIdx.x == 0)
     for (int i = 0; i < kBulkStages; ++i)
       if (blockIdx.x + i * gridDim.x < n_chunks) issue(blockIdx.x + i * gridDim.x, i);
+  // (the plain divide for the mean, not BlockMean: the multiply frees
+  // registers, the occupancy query then gives six CTAs per SM instead of
+  // four, and that grid measured slower; the results are the same bits)
   const float fblock = float(block);
   bool ok = true;
   for (int i = 0, c = blockIdx.x; c < n_chunks && ok; ++i, c += gridDim.x) {
